@@ -1,0 +1,186 @@
+"""Plain CPU oracle for the AWQ W4A16 / W4A8 quantized linear layer.
+
+TEST INFRASTRUCTURE ONLY: used by ``tests/``, ``__graft_entry__.smoke()`` and
+the CPU-baseline / reference legs of ``bench.py``; never by the product path.
+
+Sources (web pages, cited by title and section):
+
+* "Speed up AWQ 2.5x with updated kernel" (vLLM pull request), casper-hansen's
+  list of format differences: the older ("GEMM") AWQ format packs eight 4-bit
+  values per int32 with the order map [0, 2, 4, 6, 1, 3, 5, 7]; zeros are
+  packed the same way.  The dispatch snippet on the same page names the
+  operands of the kernels: inputs, qweight, scales, qzeros, group_size
+  (and split_k_iters for the M > 8 kernel).
+* "Marlin symmetric quantization and inference" (AutoAWQ pull request),
+  perplexity section: the symmetric variant has no zero points.
+* "Support W4A8 quantization for vllm" (vLLM pull request #5218):
+  the dynamic per-token activation quantization in brisker's consistency
+  script (absmax over the row divided by 127, round, clamp to [-128, 127]);
+  HandH1998's answer on per-channel dequantization (int4 to int8 by a left
+  shift of 4, the channel scale applied on the output); alexm's review note
+  that the reduction works on int32 elements.
+
+Readings taken where the pages are silent (each one is pinned by a test in
+``tests/test_oracle_pins.py``):
+
+* order map direction: nibble slot ``i`` (bits 4i..4i+3) of packed word ``c``
+  holds logical column ``8c + AWQ_ORDER[i]``;
+* dequantization: ``W = fp16_RN((q - z) * s)``, one rounding, subtract first;
+  symmetric W4A16 uses z = 8;
+* the W4A16 product is reported unrounded in float64 (``linear_f64``) and,
+  as the fp32-accumulated variant, in float32 with k ascending
+  (``linear_f32acc``); the fp16 output is one RN of the accumulated value;
+* W4A8 activation scale: fp16-rounded ``absmax / 127`` widened to fp32 (the
+  consistency script divides an fp16 absmax by 127 before converting to
+  float); a zero row gets scale 0 and codes 0;
+* W4A8 weights: signed int4 q in [-8, 7] stored with the same packing as
+  ``u = q + 8``; the int32 accumulator is exact; the output is
+  ``fp16_RN((fp32(acc) * s_tok) * fp32(s_ch))``.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+# Older-format AWQ order map ("Speed up AWQ 2.5x with updated kernel",
+# casper-hansen's list of format differences).
+AWQ_ORDER = (0, 2, 4, 6, 1, 3, 5, 7)
+
+
+def unpack(packed: np.ndarray) -> np.ndarray:
+    """Unpack an AWQ-packed int32 array [R, C] to 4-bit codes uint8 [R, 8C].
+
+    Nibble slot i of word c holds logical column 8c + AWQ_ORDER[i].
+    Pins: hand-worked words (golden file), pack/unpack round trip.
+    """
+    words = np.ascontiguousarray(packed).view(np.uint32)
+    rows, cols = words.shape
+    out = np.empty((rows, 8 * cols), dtype=np.uint8)
+    for slot, col in enumerate(AWQ_ORDER):
+        nib = (words >> np.uint32(4 * slot)) & np.uint32(0xF)
+        out[:, col::8] = nib.astype(np.uint8)
+    return out
+
+
+def pack(q: np.ndarray) -> np.ndarray:
+    """Pack 4-bit codes uint8 [R, N] (N % 8 == 0) into AWQ int32 words [R, N/8].
+
+    Codes above 15 are clamped to 15 (the W4A8 page reports a packer bug from
+    a missing clamp; clamping is the defined behaviour here).
+    Pins: hand-worked words (golden file), round trip with ``unpack``.
+    """
+    q = np.asarray(q)
+    if q.ndim != 2 or q.shape[1] % 8 != 0:
+        raise ValueError("pack expects a 2-D array whose column count is a multiple of 8")
+    codes = np.minimum(q.astype(np.uint32), np.uint32(15))
+    rows, n = codes.shape
+    words = np.zeros((rows, n // 8), dtype=np.uint32)
+    for slot, col in enumerate(AWQ_ORDER):
+        words |= codes[:, col::8] << np.uint32(4 * slot)
+    return words.view(np.int32)
+
+
+def dequant(qweight: np.ndarray, qzeros: np.ndarray | None, scales: np.ndarray,
+            group_size: int) -> np.ndarray:
+    """Group-wise dequantization W[k, n] = fp16_RN((q[k, n] - z[k // g, n]) * s[k // g, n]).
+
+    qweight int32 [K, N/8], qzeros int32 [K/g, N/8] or None (symmetric, z = 8),
+    scales fp16 [K/g, N].  Returns fp16 [K, N].
+
+    The product (q - z) * s is exact in float64 (a 5-bit integer times an
+    11-bit significand), so the single float64 -> float16 conversion is the
+    one correctly rounded step.  Pins: hand-worked values (golden file) and an
+    exhaustive (q, z) x scale sweep against exact rational rounding.
+    """
+    q = unpack(qweight).astype(np.int64)
+    k_dim, n_dim = q.shape
+    g = int(group_size)
+    if g <= 0 or k_dim % g != 0:
+        raise ValueError("group_size must divide K")
+    n_groups = k_dim // g
+    if scales.shape != (n_groups, n_dim):
+        raise ValueError("scales must have shape [K/group_size, N]")
+    if qzeros is None:
+        z = np.full((n_groups, n_dim), 8, dtype=np.int64)
+    else:
+        z = unpack(qzeros).astype(np.int64)
+        if z.shape != (n_groups, n_dim):
+            raise ValueError("qzeros must have shape [K/group_size, N/8]")
+    group_of_row = np.arange(k_dim) // g
+    diff = (q - z[group_of_row, :]).astype(np.float64)
+    s = scales.astype(np.float64)[group_of_row, :]
+    return (diff * s).astype(np.float16)
+
+
+def linear_f64(x: np.ndarray, w: np.ndarray) -> np.ndarray:
+    """y[m, n] = sum_k x[m, k] * W[k, n] in float64 (products of two fp16 are exact).
+
+    Pin: brute force with exact rationals at K = 8 (tests).
+    """
+    return x.astype(np.float64) @ w.astype(np.float64)
+
+
+def linear_f32acc(x: np.ndarray, w: np.ndarray) -> np.ndarray:
+    """The same sum accumulated in float32, k ascending (slow; small shapes only).
+
+    Every product of two fp16 values is exact in float32, so only the
+    accumulation rounds.  Pin: within K * 2^-24 * sum|x*W| of the exact value.
+    """
+    x32 = x.astype(np.float32)
+    w32 = w.astype(np.float32)
+    acc = np.zeros((x.shape[0], w.shape[1]), dtype=np.float32)
+    for k in range(x.shape[1]):
+        acc += x32[:, k:k + 1] * w32[k:k + 1, :]
+    return acc
+
+
+def awq_linear(x: np.ndarray, qweight: np.ndarray, qzeros: np.ndarray | None,
+               scales: np.ndarray, group_size: int) -> np.ndarray:
+    """The W4A16 layer: dequantize, then the float64 product (unrounded)."""
+    return linear_f64(x, dequant(qweight, qzeros, scales, group_size))
+
+
+def quant_act(x: np.ndarray):
+    """Per-token dynamic int8 quantization of fp16 activations [M, K].
+
+    s[m] = fp32(fp16_RN(fp32(absmax_k |x[m, k]|) / 127)),
+    xq[m, k] = clamp(rint(fp32(x[m, k]) / s[m]), -128, 127)   (IEEE fp32 division,
+    round half to even).  A row of zeros gets s = 0 and xq = 0.
+    Returns (xq int8 [M, K], s float32 [M]).
+    Pins: the hand examples in the golden file; |xq| <= 127 with the row's
+    absmax element at +-127; zero rows.
+    """
+    x16 = np.asarray(x, dtype=np.float16)
+    absmax = np.abs(x16).max(axis=1).astype(np.float32)
+    s = (absmax / np.float32(127.0)).astype(np.float16).astype(np.float32)
+    xq = np.zeros(x16.shape, dtype=np.int8)
+    nz = s > 0
+    if np.any(nz):
+        ratio = x16[nz].astype(np.float32) / s[nz, None]
+        xq[nz] = np.clip(np.rint(ratio), -128, 127).astype(np.int8)
+    return xq, s
+
+
+def w4a8_accumulate(xq: np.ndarray, wq_packed: np.ndarray) -> np.ndarray:
+    """Exact integer accumulator acc[m, n] = sum_k xq[m, k] * (u[k, n] - 8), int64.
+
+    wq_packed holds u = q + 8 in the AWQ packing.  Pin: brute-force integer
+    sums on tiny inputs; the result must fit in int32.
+    """
+    q = unpack(wq_packed).astype(np.int64) - 8
+    acc = xq.astype(np.int64) @ q
+    if acc.size and (acc.max() > np.iinfo(np.int32).max or acc.min() < np.iinfo(np.int32).min):
+        raise OverflowError("W4A8 accumulator does not fit in int32")
+    return acc
+
+
+def w4a8_linear(xq: np.ndarray, s_tok: np.ndarray, wq_packed: np.ndarray,
+                s_ch: np.ndarray):
+    """W4A8 output y = fp16_RN((fp32(acc) * s_tok[m]) * fp32(s_ch[n])).
+
+    Returns (y fp16 [M, N], acc int64 [M, N]).
+    """
+    acc = w4a8_accumulate(xq, wq_packed)
+    y32 = (acc.astype(np.float32) * np.asarray(s_tok, dtype=np.float32)[:, None])
+    y32 = y32 * np.asarray(s_ch, dtype=np.float16).astype(np.float32)[None, :]
+    return y32.astype(np.float16), acc

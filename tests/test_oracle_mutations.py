@@ -1,0 +1,114 @@
+"""Planted mistakes in the oracle (on the CPU) must each fail at least one pin.
+
+Each mutant replaces one oracle function with a plausible wrong variant for the
+duration of the named pin tests; at least one of them must then fail.  This
+shows that the pins in ``test_oracle_pins.py`` constrain the oracle rather than
+restate it.
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import awq_oracle as O
+from tests import test_oracle_pins as pins
+
+
+def _unpack_inverse_map(packed):
+    # wrong direction of the order map
+    words = np.ascontiguousarray(packed).view(np.uint32)
+    rows, cols = words.shape
+    out = np.empty((rows, 8 * cols), dtype=np.uint8)
+    for col, slot in enumerate(O.AWQ_ORDER):
+        out[:, col::8] = ((words >> np.uint32(4 * slot)) & np.uint32(0xF)).astype(np.uint8)
+    return out
+
+
+def _pack_no_clamp(q):
+    codes = np.asarray(q).astype(np.uint32)
+    rows, n = codes.shape
+    words = np.zeros((rows, n // 8), dtype=np.uint32)
+    for slot, col in enumerate(O.AWQ_ORDER):
+        words |= codes[:, col::8] << np.uint32(4 * slot)
+    return words.view(np.int32)
+
+
+def _dequant_factory(sign=1, group_mod=False, flip_cols=False, zero=8):
+    def dequant(qweight, qzeros, scales, group_size):
+        q = O.unpack(qweight).astype(np.int64)
+        k_dim, n_dim = q.shape
+        g = int(group_size)
+        ng = k_dim // g
+        z = np.full((ng, n_dim), zero, np.int64) if qzeros is None else O.unpack(qzeros).astype(np.int64)
+        gi = (np.arange(k_dim) % ng) if group_mod else (np.arange(k_dim) // g)
+        s = scales.astype(np.float64)
+        if flip_cols:
+            s = s[:, ::-1]
+        return (sign * (q - z[gi]).astype(np.float64) * s[gi]).astype(np.float16)
+    return dequant
+
+
+def _linear_transposed(x, w):
+    return (w.astype(np.float64).T @ x.astype(np.float64).T).T[:, ::-1]
+
+
+def _linear_f32acc_fp16_accum(x, w):
+    acc = np.zeros((x.shape[0], w.shape[1]), dtype=np.float16)
+    for k in range(x.shape[1]):
+        acc += x[:, k:k + 1] * w[k:k + 1, :]
+    return acc.astype(np.float32)
+
+
+def _quant_act_fp32_scale(x):
+    x16 = np.asarray(x, dtype=np.float16)
+    s = np.abs(x16).max(axis=1).astype(np.float32) / np.float32(127)
+    xq = np.zeros(x16.shape, np.int8)
+    nz = s > 0
+    xq[nz] = np.clip(np.rint(x16[nz].astype(np.float32) / s[nz, None]), -128, 127).astype(np.int8)
+    return xq, s
+
+
+def _quant_act_half_up(x):
+    x16 = np.asarray(x, dtype=np.float16)
+    s = (np.abs(x16).max(axis=1).astype(np.float32) / np.float32(127)).astype(np.float16).astype(np.float32)
+    xq = np.zeros(x16.shape, np.int8)
+    nz = s > 0
+    xq[nz] = np.clip(np.floor(x16[nz].astype(np.float32) / s[nz, None] + 0.5), -128, 127).astype(np.int8)
+    return xq, s
+
+
+def _w4a8_acc_offset7(xq, wq):
+    return xq.astype(np.int64) @ (O.unpack(wq).astype(np.int64) - 7)
+
+
+MUTANTS = [
+    ("unpack", _unpack_inverse_map, ["test_unpack_pack_golden"]),
+    ("pack", _pack_no_clamp, ["test_pack_clamps_codes_above_15"]),
+    ("dequant", _dequant_factory(sign=-1), ["test_dequant_golden"]),
+    ("dequant", _dequant_factory(group_mod=True), ["test_dequant_group_index_closed_form"]),
+    ("dequant", _dequant_factory(flip_cols=True), ["test_dequant_per_column_scale_and_zero_not_transposed"]),
+    ("dequant", _dequant_factory(zero=7), ["test_dequant_symmetric_uses_zero_eight"]),
+    ("linear_f64", _linear_transposed, ["test_linear_bruteforce_exact_rationals"]),
+    ("linear_f32acc", _linear_f32acc_fp16_accum, ["test_linear_bruteforce_exact_rationals"]),
+    ("quant_act", _quant_act_fp32_scale, ["test_quant_act_golden"]),
+    ("quant_act", _quant_act_half_up, ["test_quant_act_golden"]),
+    ("w4a8_accumulate", _w4a8_acc_offset7, ["test_w4a8_accumulate_bruteforce"]),
+]
+
+
+@pytest.mark.parametrize("name,mutant,pin_names", MUTANTS,
+                         ids=[f"{m[0]}-{i}" for i, m in enumerate(MUTANTS)])
+def test_planted_mistake_fails_a_pin(monkeypatch, golden_dir, name, mutant, pin_names):
+    monkeypatch.setattr(O, name, mutant)
+    monkeypatch.setattr(oracle, name, mutant)
+    failed = False
+    for pin in pin_names:
+        fn = getattr(pins, pin)
+        try:
+            if "golden_dir" in fn.__code__.co_varnames[:fn.__code__.co_argcount]:
+                fn(golden_dir)
+            else:
+                fn()
+        except Exception:
+            failed = True
+    assert failed, f"mutant of {name} passed {pin_names}"

@@ -1,0 +1,271 @@
+"""Pins for the CPU oracle: each function is held to something other than itself.
+
+* packing: hand-worked words (golden file) and the pack/unpack round trip;
+* dequantization: hand-worked values (golden file), an exhaustive (q, z) x
+  scale sweep against exact rational round-to-nearest-even, and closed-form
+  cases that fail on a wrong group or column index;
+* the product: exact rational brute force at K = 8, the fp32 accumulation
+  bound, and closed-form special cases (zero weights, one-hot copy);
+* W4A8: hand-worked quantization examples (golden file), invariants of the
+  per-token scale, and brute-force integer sums.
+"""
+
+import os
+from fractions import Fraction
+from math import floor
+
+import numpy as np
+
+import oracle
+from bit_weight_only_awq_gb300 import synth
+
+
+# ---------------------------------------------------------------- helpers
+def fp16_rn_exact(v: Fraction) -> Fraction:
+    """IEEE binary16 round-to-nearest-even of an exact rational (finite range only)."""
+    if v == 0:
+        return Fraction(0)
+    sign = -1 if v < 0 else 1
+    a = abs(v)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    while Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    e = max(e, -14)                      # subnormals share the 2^-24 spacing
+    ulp = Fraction(2) ** (e - 10)
+    m = a / ulp
+    f = floor(m)
+    r = m - f
+    if r > Fraction(1, 2) or (r == Fraction(1, 2) and f % 2 == 1):
+        f += 1
+    return sign * f * ulp
+
+
+def half_from_hex(h: int) -> np.float16:
+    return np.array([h], dtype=np.uint16).view(np.float16)[0]
+
+
+def read_golden(golden_dir, name):
+    with open(os.path.join(golden_dir, name)) as fh:
+        return [ln.strip() for ln in fh if ln.strip() and not ln.startswith("#")]
+
+
+# ---------------------------------------------------------------- packing
+def test_unpack_pack_golden(golden_dir):
+    n_unpack = n_pack = 0
+    for line in read_golden(golden_dir, "awq_order_words.txt"):
+        kind, rest = line.split(None, 1)
+        lhs, rhs = (s.strip() for s in rest.split(":"))
+        if kind == "unpack":
+            word = np.array([[int(lhs, 16)]], dtype=np.uint32).view(np.int32)
+            want = [int(t) for t in rhs.split()]
+            assert oracle.unpack(word)[0].tolist() == want, line
+            n_unpack += 1
+        else:
+            codes = np.array([[int(t) for t in lhs.split()]], dtype=np.uint8)
+            got = int(oracle.pack(codes).view(np.uint32)[0, 0])
+            assert got == int(rhs, 16), (line, hex(got))
+            n_pack += 1
+    assert n_unpack >= 5 and n_pack >= 5
+
+
+def test_pack_unpack_round_trip():
+    codes = synth.random_codes(37, 96, seed=11)
+    assert np.array_equal(oracle.unpack(oracle.pack(codes)), codes)
+    words = synth.random_words(np.random.default_rng(5), 19, 24)
+    assert np.array_equal(oracle.pack(oracle.unpack(words)), words)
+
+
+def test_pack_clamps_codes_above_15():
+    codes = synth.random_codes(8, 64, seed=12, high=64)
+    assert np.array_equal(oracle.unpack(oracle.pack(codes)), np.minimum(codes, 15))
+
+
+def test_unpack_column_order_is_a_permutation_per_word():
+    # every word's 8 nibbles land in 8 distinct columns of that word's block
+    words = np.array([[0x76543210, 0xFEDCBA98]], dtype=np.uint32).view(np.int32)
+    u = oracle.unpack(words)[0]
+    assert sorted(u[:8].tolist()) == list(range(8))
+    assert sorted(u[8:].tolist()) == list(range(8, 16))
+
+
+# ---------------------------------------------------------------- dequant
+def _one_word_problem(q, z, s_half):
+    """A single group (g = 1) of 8 columns with every code q, zero z and scale s."""
+    codes = np.full((1, 8), q, dtype=np.uint8)
+    zeros = np.full((1, 8), z, dtype=np.uint8)
+    scales = np.full((1, 8), s_half, dtype=np.float16)
+    return oracle.pack(codes), oracle.pack(zeros), scales
+
+
+def test_dequant_golden(golden_dir):
+    rows = read_golden(golden_dir, "dequant_examples.txt")
+    for line in rows:
+        lhs, want = line.split("->")
+        q, z, sh = lhs.split()
+        qw, qz, sc = _one_word_problem(int(q), int(z), half_from_hex(int(sh, 16)))
+        w = oracle.dequant(qw, qz, sc, group_size=1)
+        assert np.all(w.astype(np.float64) == float(want.strip())), line
+    assert len(rows) >= 8
+
+
+def test_dequant_exhaustive_against_exact_rounding():
+    # all 16 x 16 (q, z) pairs against a sweep of fp16 scales incl. subnormal and tie-prone ones
+    rng = np.random.default_rng(3)
+    sweep = [0x0001, 0x0003, 0x03FF, 0x0400, 0x1819, 0x251F, 0x3C01, 0x3C03, 0x3BFF, 0x4A3D, 0x57FF]
+    sweep += rng.integers(0x0001, 0x5800, size=24).tolist()
+    qs, zs = np.meshgrid(np.arange(16), np.arange(16), indexing="ij")
+    qs, zs = qs.ravel(), zs.ravel()
+    codes = qs.astype(np.uint8)[None, :]          # 1 row x 256 columns, one group
+    zeros = zs.astype(np.uint8)[None, :]
+    for h in sweep:
+        s = half_from_hex(int(h))
+        scales = np.full((1, 256), s, dtype=np.float16)
+        w = oracle.dequant(oracle.pack(codes), oracle.pack(zeros), scales, group_size=1)
+        s_exact = Fraction(float(s))
+        for i in range(256):
+            want = fp16_rn_exact((int(qs[i]) - int(zs[i])) * s_exact)
+            assert Fraction(float(w[0, i])) == want, (hex(h), qs[i], zs[i])
+
+
+def test_dequant_symmetric_uses_zero_eight():
+    codes = np.arange(16, dtype=np.uint8).repeat(8)[None, :]          # 1 x 128
+    scales = np.ones((1, 128), dtype=np.float16)
+    w = oracle.dequant(oracle.pack(codes), None, scales, group_size=1)
+    assert np.array_equal(w[0].astype(np.int64), codes[0].astype(np.int64) - 8)
+
+
+def test_dequant_group_index_closed_form():
+    # K = 3 groups of 4 rows; codes 9 everywhere; zeros 8, 7, 6 per group;
+    # scales 1, 2, 4 per group -> rows of group j equal (j + 1) * 2^j.
+    g, n = 4, 16
+    codes = np.full((3 * g, n), 9, dtype=np.uint8)
+    zeros = np.stack([np.full(n, 8 - j, dtype=np.uint8) for j in range(3)])
+    scales = np.stack([np.full(n, 2.0 ** j, dtype=np.float16) for j in range(3)])
+    w = oracle.dequant(oracle.pack(codes), oracle.pack(zeros), scales, group_size=g)
+    for k in range(3 * g):
+        j = k // g
+        assert np.all(w[k] == (j + 1) * 2 ** j), k
+
+
+def test_dequant_per_column_scale_and_zero_not_transposed():
+    # distinct per-column zero points and scales: column n has z = n % 16 and s = 2^-(n % 4)
+    n = 32
+    codes = np.full((1, n), 15, dtype=np.uint8)
+    zeros = (np.arange(n) % 16).astype(np.uint8)[None, :]
+    scales = (2.0 ** -(np.arange(n) % 4)).astype(np.float16)[None, :]
+    w = oracle.dequant(oracle.pack(codes), oracle.pack(zeros), scales, group_size=1)
+    want = (15 - (np.arange(n) % 16)) * 2.0 ** -(np.arange(n) % 4)
+    assert np.array_equal(w[0].astype(np.float64), want)
+
+
+# ---------------------------------------------------------------- product
+def test_linear_bruteforce_exact_rationals():
+    p = synth.awq_problem(3, 8, 24, seed=21, group_size=8)
+    w = oracle.dequant(p["qweight"], p["qzeros"], p["scales"], 8)
+    y64 = oracle.linear_f64(p["x"], w)
+    y32 = oracle.linear_f32acc(p["x"], w)
+    assert y64.shape == (3, 24)
+    for m in range(3):
+        for n in range(24):
+            terms = [Fraction(float(p["x"][m, k])) * Fraction(float(w[k, n])) for k in range(8)]
+            exact = sum(terms)
+            mag = sum(abs(t) for t in terms)
+            assert abs(Fraction(float(y64[m, n])) - exact) <= mag * Fraction(8, 2 ** 53)
+            assert abs(Fraction(float(y32[m, n])) - exact) <= mag * Fraction(8, 2 ** 24)
+
+
+def test_linear_zero_weights_give_zero():
+    # every row of each group carries the group's zero points as codes: q == z everywhere
+    p = synth.awq_problem(4, 256, 64, seed=22)
+    codes = synth.random_codes(256, 64, seed=23)
+    same = np.repeat(codes[:1], 256, axis=0)
+    w = oracle.dequant(oracle.pack(same), oracle.pack(same[:2]), p["scales"], 128)
+    assert np.all(w == 0)
+    assert np.all(oracle.linear_f64(p["x"], w) == 0)
+
+
+def test_linear_one_hot_copies_integer_row():
+    k_dim, n = 128, 64
+    codes = synth.random_codes(k_dim, n, seed=24)
+    zeros = np.zeros((1, n), dtype=np.uint8)
+    scales = np.ones((1, n), dtype=np.float16)
+    w = oracle.dequant(oracle.pack(codes), oracle.pack(zeros), scales, 128)
+    x = np.zeros((2, k_dim), dtype=np.float16)
+    x[0, 5] = 1.0
+    x[1, 77] = 1.0
+    y = oracle.linear_f64(x, w)
+    assert np.array_equal(y[0], codes[5].astype(np.float64))
+    assert np.array_equal(y[1], codes[77].astype(np.float64))
+
+
+def test_awq_linear_word_column_locality():
+    p = synth.awq_problem(5, 256, 40, seed=25)
+    y = oracle.awq_linear(p["x"], p["qweight"], p["qzeros"], p["scales"], 128)
+    assert y.shape == (5, 40)
+    # outputs 8c..8c+7 depend only on word column c: zeroing word column 2 (codes and zeros)
+    # changes exactly those outputs, to zero
+    qw = p["qweight"].copy()
+    qz = p["qzeros"].copy()
+    qw[:, 2] = 0
+    qz[:, 2] = 0
+    y2 = oracle.awq_linear(p["x"], qw, qz, p["scales"], 128)
+    assert np.array_equal(y2[:, :16], y[:, :16]) and np.array_equal(y2[:, 24:], y[:, 24:])
+    assert np.all(y2[:, 16:24] == 0)
+
+
+# ---------------------------------------------------------------- W4A8
+def test_quant_act_golden(golden_dir):
+    rows = read_golden(golden_dir, "w4a8_quant_examples.txt")
+    for line in rows:
+        xs, s_want, q_want = (part.strip() for part in line.split(";"))
+        x = np.array([[float(t) for t in xs.split()]], dtype=np.float16)
+        xq, s = oracle.quant_act(x)
+        assert float(s[0]) == float(s_want), line
+        assert xq[0].tolist() == [int(t) for t in q_want.split()], line
+    assert len(rows) >= 4
+
+
+def test_quant_act_invariants():
+    x = synth.activations(np.random.default_rng(7), 16, 1000)
+    xq, s = oracle.quant_act(x)
+    assert xq.dtype == np.int8 and s.dtype == np.float32
+    assert np.all(np.abs(xq.astype(np.int32)) <= 127)
+    am = np.argmax(np.abs(x.astype(np.float32)), axis=1)
+    assert np.all(np.abs(xq[np.arange(16), am].astype(np.int32)) == 127)
+    # reconstruction error at most half a step (plus the fp16 rounding of the scale)
+    err = np.abs(xq.astype(np.float64) * s[:, None] - x.astype(np.float64))
+    assert np.all(err <= 0.5 * s[:, None] * (1 + 1e-3) + 1e-7)
+
+
+def test_w4a8_accumulate_bruteforce():
+    p = synth.w4a8_problem(3, 24, 16, seed=31)
+    xq, _ = oracle.quant_act(p["x"])
+    acc = oracle.w4a8_accumulate(xq, p["wq"])
+    words = p["wq"].view(np.uint32)
+    for m in range(3):
+        for n in range(16):
+            total = 0
+            for k in range(24):
+                word = int(words[k, n // 8])
+                slot = oracle.AWQ_ORDER.index(n % 8)
+                u = (word >> (4 * slot)) & 0xF
+                total += int(xq[m, k]) * (u - 8)
+            assert acc[m, n] == total
+
+
+def test_w4a8_unit_scales_return_integers():
+    # s_tok = s_ch = 1 and small accumulators: the fp16 output is the integer accumulator itself
+    p = synth.w4a8_problem(2, 8, 16, seed=32)
+    xq = np.array([[1, -1, 2, 0, 0, 3, -2, 1], [0, 0, 0, 0, 0, 0, 0, 5]], dtype=np.int8)
+    y, acc = oracle.w4a8_linear(xq, np.ones(2, np.float32), p["wq"], np.ones(16, np.float16))
+    assert np.array_equal(y.astype(np.float64), acc.astype(np.float64))
+    # linearity of the accumulator in the activation codes
+    acc2 = oracle.w4a8_accumulate((2 * xq).astype(np.int8), p["wq"])
+    assert np.array_equal(acc2, 2 * acc)
+
+
+def test_w4a8_extremes_fit_int32_at_k21760():
+    # worst case |acc| <= K * 128 * 8 stays below 2^31 at the largest K of the workloads
+    assert 21760 * 128 * 8 < 2 ** 31
