@@ -1,0 +1,186 @@
+"""ctypes binding over libawq.so (declared in include/awq.h), same entry-point names.
+
+Argument marshalling only: every step of the computation runs in the library's
+CUDA kernels.  PyTorch provides device memory (outputs and workspaces allocated
+here when the caller passes none) and the current CUDA stream.  Importing this
+module loads the library and raises ImportError when it has not been built;
+there is no fallback path.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libawq.so")
+_HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "awq.h")
+
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(f"{_LIB_PATH} is missing: build it with `python -m bit_weight_only_awq_gb300.build`")
+lib = ctypes.CDLL(_LIB_PATH)
+
+STATUS = {0: "AWQ_OK", -1: "AWQ_EINVAL", -2: "AWQ_EALIGN", -3: "AWQ_EARCH", -4: "AWQ_ECUDA",
+          -5: "AWQ_ETIMEOUT", -6: "AWQ_EWORKSPACE", -7: "AWQ_ENULL"}
+OP_GEMV, OP_GEMM, OP_W4A8_GEMM = 0, 1, 2
+GROUP_SIZE = 128
+
+_p = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_i32 = ctypes.c_int32
+_sz = ctypes.c_size_t
+
+_SIGS = {
+    "awq_status_string": (ctypes.c_char_p, [_i32]),
+    "awq_pack": (_i32, [_p, _i64, _i64, _p, _p]),
+    "awq_unpack": (_i32, [_p, _i64, _i64, _p, _p]),
+    "awq_dequant": (_i32, [_p, _p, _p, _i64, _i64, _i32, _p, _p]),
+    "awq_workspace_bytes": (_sz, [_i32, _i64, _i64, _i64, _i32]),
+    "awq_gemv": (_i32, [_p, _p, _p, _p, _p, _i64, _i64, _i64, _i32, _i32, _p, _sz, _p]),
+    "awq_gemm": (_i32, [_p, _p, _p, _p, _p, _i64, _i64, _i64, _i32, _i32, _p, _sz, _p]),
+    "w4a8_quant_act": (_i32, [_p, _p, _p, _i64, _i64, _p]),
+    "w4a8_gemm": (_i32, [_p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _i32, _p, _sz, _p]),
+    "awq_last_device_error": (_i32, [ctypes.POINTER(_i32)]),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _fn = getattr(lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+
+
+def header_functions() -> list[str]:
+    """Names of the functions declared in include/awq.h."""
+    with open(_HEADER) as fh:
+        text = fh.read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*((?:awq|w4a8)_[a-z0-9_]+)\s*\(", text, re.M)))
+
+
+class AwqError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        msg = lib.awq_status_string(status).decode()
+        super().__init__(f"{fn}: {msg}")
+        self.status = status
+
+
+def _check(fn: str, status: int) -> None:
+    if status != 0:
+        raise AwqError(fn, status)
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+# One zero-filled workspace per device, grown on demand.  The library leaves its tile
+# counters at zero after every call, so reuse on one stream needs no re-zeroing.
+_workspaces: dict[int, torch.Tensor] = {}
+
+
+def device_workspace(nbytes: int, device: torch.device) -> torch.Tensor | None:
+    if nbytes == 0:
+        return None
+    idx = device.index if device.index is not None else torch.cuda.current_device()
+    ws = _workspaces.get(idx)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.zeros(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
+        _workspaces[idx] = ws
+    return ws
+
+
+def awq_workspace_bytes(op: int, M: int, K: int, N: int, split_k: int = 0) -> int:
+    return int(lib.awq_workspace_bytes(op, M, K, N, split_k))
+
+
+def awq_pack(q: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    rows, n = q.shape
+    if out is None:
+        out = torch.empty((rows, n // 8), dtype=torch.int32, device=q.device)
+    _check("awq_pack", lib.awq_pack(_ptr(q), rows, n, _ptr(out), _stream(stream)))
+    return out
+
+
+def awq_unpack(packed: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    rows, nw = packed.shape
+    if out is None:
+        out = torch.empty((rows, nw * 8), dtype=torch.uint8, device=packed.device)
+    _check("awq_unpack", lib.awq_unpack(_ptr(packed), rows, nw * 8, _ptr(out), _stream(stream)))
+    return out
+
+
+def awq_dequant(qweight, qzeros, scales, group_size: int = GROUP_SIZE, out=None, stream=None) -> torch.Tensor:
+    K, nw = qweight.shape
+    if out is None:
+        out = torch.empty((K, nw * 8), dtype=torch.float16, device=qweight.device)
+    _check("awq_dequant", lib.awq_dequant(_ptr(qweight), _ptr(qzeros), _ptr(scales), K, nw * 8, group_size,
+                                          _ptr(out), _stream(stream)))
+    return out
+
+
+def _gemm_like(name, op, x, qweight, qzeros, scales, group_size, split_k, out, ws, stream):
+    M, K = x.shape
+    N = qweight.shape[1] * 8
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    need = awq_workspace_bytes(op, M, K, N, split_k)
+    if ws is None:
+        ws = device_workspace(need, x.device)
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    fn = getattr(lib, name)
+    _check(name, fn(_ptr(x), _ptr(qweight), _ptr(qzeros), _ptr(scales), _ptr(out), M, K, N, group_size,
+                    split_k, _ptr(ws), nbytes, _stream(stream)))
+    return out
+
+
+def awq_gemv(x, qweight, qzeros, scales, group_size: int = GROUP_SIZE, split_k: int = 0, out=None,
+             workspace=None, stream=None) -> torch.Tensor:
+    return _gemm_like("awq_gemv", OP_GEMV, x, qweight, qzeros, scales, group_size, split_k, out, workspace, stream)
+
+
+def awq_gemm(x, qweight, qzeros, scales, group_size: int = GROUP_SIZE, split_k: int = 0, out=None,
+             workspace=None, stream=None) -> torch.Tensor:
+    return _gemm_like("awq_gemm", OP_GEMM, x, qweight, qzeros, scales, group_size, split_k, out, workspace, stream)
+
+
+def awq_linear(x, qweight, qzeros, scales, group_size: int = GROUP_SIZE, **kw) -> torch.Tensor:
+    """The pages' dispatch: the GEMV kernel for M <= 8 tokens, the GEMM kernel above."""
+    fn = awq_gemv if x.shape[0] <= 8 else awq_gemm
+    return fn(x, qweight, qzeros, scales, group_size, **kw)
+
+
+def w4a8_quant_act(x, xq=None, s_tok=None, stream=None):
+    M, K = x.shape
+    if xq is None:
+        xq = torch.empty((M, K), dtype=torch.int8, device=x.device)
+    if s_tok is None:
+        s_tok = torch.empty((M,), dtype=torch.float32, device=x.device)
+    _check("w4a8_quant_act", lib.w4a8_quant_act(_ptr(x), _ptr(xq), _ptr(s_tok), M, K, _stream(stream)))
+    return xq, s_tok
+
+
+def w4a8_gemm(xq, s_tok, wq, s_ch, split_k: int = 0, out=None, acc_out=None, workspace=None, stream=None):
+    M, K = xq.shape
+    N = wq.shape[1] * 8
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=xq.device)
+    need = awq_workspace_bytes(OP_W4A8_GEMM, M, K, N, split_k)
+    ws = workspace if workspace is not None else device_workspace(need, xq.device)
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check("w4a8_gemm", lib.w4a8_gemm(_ptr(xq), _ptr(s_tok), _ptr(wq), _ptr(s_ch), _ptr(out), _ptr(acc_out), M, K,
+                                      N, split_k, _ptr(ws), nbytes, _stream(stream)))
+    return out
+
+
+def awq_last_device_error() -> int:
+    code = _i32(0)
+    status = lib.awq_last_device_error(ctypes.byref(code))
+    if status not in (0, -5):
+        raise AwqError("awq_last_device_error", status)
+    return int(code.value)

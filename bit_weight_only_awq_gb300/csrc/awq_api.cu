@@ -1,0 +1,241 @@
+// C ABI of libawq: argument checks, workspace planning, dispatch to the kernels.
+// Declarations and the meaning of every argument: include/awq.h.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "../../include/awq.h"
+#include "awq_internal.h"
+
+namespace awq {
+namespace {
+
+__device__ int g_device_error = 0;  // id of the last bounded device wait that expired (0 = none)
+
+constexpr int kMaxDevices = 64;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Compute capability 10.3 check, cached per device.
+awq_status check_arch() {
+  static int cached[kMaxDevices] = {0};  // 0 unknown, 1 ok, -1 wrong arch
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return AWQ_ECUDA;
+  if (dev < 0 || dev >= kMaxDevices) return AWQ_ECUDA;
+  if (cached[dev] == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return AWQ_ECUDA;
+    cached[dev] = (major == 10 && minor == 3) ? 1 : -1;
+  }
+  return cached[dev] == 1 ? AWQ_OK : AWQ_EARCH;
+}
+
+awq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? AWQ_OK : AWQ_ECUDA; }
+
+awq_status check_workspace(size_t need, const void* ws, size_t have) {
+  if (need == 0) return AWQ_OK;
+  if (ws == nullptr || have < need) return AWQ_EWORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return AWQ_EALIGN;
+  return AWQ_OK;
+}
+
+}  // namespace
+
+int* device_error_ptr() {
+  static int* ptrs[kMaxDevices] = {nullptr};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<int*>(p);
+  }
+  return ptrs[dev];
+}
+
+}  // namespace awq
+
+using namespace awq;
+
+extern "C" {
+
+const char* awq_status_string(awq_status status) {
+  switch (status) {
+    case AWQ_OK: return "AWQ_OK";
+    case AWQ_EINVAL: return "AWQ_EINVAL: size or shape argument out of range";
+    case AWQ_EALIGN: return "AWQ_EALIGN: pointer not 16-byte aligned (workspace: 256-byte)";
+    case AWQ_EARCH: return "AWQ_EARCH: current device is not compute capability 10.3";
+    case AWQ_ECUDA: return "AWQ_ECUDA: CUDA runtime call or kernel launch failed";
+    case AWQ_ETIMEOUT: return "AWQ_ETIMEOUT: a bounded device-side wait expired";
+    case AWQ_EWORKSPACE: return "AWQ_EWORKSPACE: workspace missing or too small";
+    case AWQ_ENULL: return "AWQ_ENULL: required pointer is NULL";
+    default: return "AWQ: unknown status";
+  }
+}
+
+awq_status awq_pack(const uint8_t* q, int64_t rows, int64_t n, int32_t* packed, awq_stream_t stream) {
+  if (rows < 0 || n < 0 || n % 8 != 0) return AWQ_EINVAL;
+  if (rows == 0 || n == 0) return AWQ_OK;
+  if (!q || !packed) return AWQ_ENULL;
+  if (!aligned16(q) || !aligned16(packed)) return AWQ_EALIGN;
+  awq_status st = check_arch();
+  if (st != AWQ_OK) return st;
+  return from_cuda(launch_pack(q, rows, n, reinterpret_cast<uint32_t*>(packed), (cudaStream_t)stream));
+}
+
+awq_status awq_unpack(const int32_t* packed, int64_t rows, int64_t n, uint8_t* q, awq_stream_t stream) {
+  if (rows < 0 || n < 0 || n % 8 != 0) return AWQ_EINVAL;
+  if (rows == 0 || n == 0) return AWQ_OK;
+  if (!q || !packed) return AWQ_ENULL;
+  if (!aligned16(q) || !aligned16(packed)) return AWQ_EALIGN;
+  awq_status st = check_arch();
+  if (st != AWQ_OK) return st;
+  return from_cuda(launch_unpack(reinterpret_cast<const uint32_t*>(packed), rows, n, q, (cudaStream_t)stream));
+}
+
+awq_status awq_dequant(const int32_t* qweight, const int32_t* qzeros, const uint16_t* scales, int64_t K,
+                       int64_t N, int32_t group_size, uint16_t* w, awq_stream_t stream) {
+  if (group_size != 32 && group_size != 64 && group_size != 128 && group_size != 256) return AWQ_EINVAL;
+  if (K < 0 || N < 0 || K % group_size != 0 || N % 8 != 0) return AWQ_EINVAL;
+  if (K == 0 || N == 0) return AWQ_OK;
+  if (!qweight || !scales || !w) return AWQ_ENULL;
+  if (!aligned16(qweight) || !aligned16(scales) || !aligned16(w) || (qzeros && !aligned16(qzeros)))
+    return AWQ_EALIGN;
+  awq_status st = check_arch();
+  if (st != AWQ_OK) return st;
+  return from_cuda(launch_dequant(reinterpret_cast<const uint32_t*>(qweight),
+                                  reinterpret_cast<const uint32_t*>(qzeros), scales, K, N, group_size, w,
+                                  (cudaStream_t)stream));
+}
+
+static bool gemv_shape_ok(int64_t M, int64_t K, int64_t N, int32_t group_size, int32_t split_k) {
+  return M >= 0 && M <= kGemvMaxM && K > 0 && K % kGroup == 0 && N > 0 && N % 16 == 0 && group_size == kGroup &&
+         split_k >= 0 && K <= (int64_t)1 << 30 && N <= (int64_t)1 << 30;
+}
+static bool gemm_shape_ok(int64_t M, int64_t K, int64_t N, int32_t split_k) {
+  return M >= 0 && M <= (int64_t)1 << 24 && K > 0 && K % kGroup == 0 && K <= (int64_t)1 << 30 && N > 0 &&
+         N % 32 == 0 && N <= (int64_t)1 << 30 && split_k >= 0 && M * N < ((int64_t)1 << 40);
+}
+
+size_t awq_workspace_bytes(awq_op op, int64_t M, int64_t K, int64_t N, int32_t split_k) {
+  switch (op) {
+    case AWQ_OP_GEMV:
+      if (!gemv_shape_ok(M, K, N, kGroup, split_k) || M == 0) return 0;
+      return gemv_workspace_bytes(gemv_plan(M, K, N, split_k), M, N);
+    case AWQ_OP_GEMM:
+      if (!gemm_shape_ok(M, K, N, split_k) || M == 0) return 0;
+      return gemm_workspace_bytes(gemm_plan(M, K, N, split_k, kModeZeroPoint), M, K, N, kModeZeroPoint);
+    case AWQ_OP_W4A8_GEMM:
+      if (!gemm_shape_ok(M, K, N, split_k) || M == 0) return 0;
+      return gemm_workspace_bytes(gemm_plan(M, K, N, split_k, kModeW4A8), M, K, N, kModeW4A8);
+    default:
+      return 0;
+  }
+}
+
+awq_status awq_gemv(const uint16_t* x, const int32_t* qweight, const int32_t* qzeros, const uint16_t* scales,
+                    uint16_t* y, int64_t M, int64_t K, int64_t N, int32_t group_size, int32_t split_k,
+                    void* workspace, size_t workspace_bytes, awq_stream_t stream) {
+  if (!gemv_shape_ok(M, K, N, group_size, split_k)) return AWQ_EINVAL;
+  if (M == 0) return AWQ_OK;
+  if (!x || !qweight || !scales || !y) return AWQ_ENULL;
+  if (!aligned16(x) || !aligned16(qweight) || !aligned16(scales) || !aligned16(y) || (qzeros && !aligned16(qzeros)))
+    return AWQ_EALIGN;
+  const GemvPlan plan = gemv_plan(M, K, N, split_k);
+  awq_status st = check_workspace(gemv_workspace_bytes(plan, M, N), workspace, workspace_bytes);
+  if (st != AWQ_OK) return st;
+  st = check_arch();
+  if (st != AWQ_OK) return st;
+  return from_cuda(launch_gemv(x, reinterpret_cast<const uint32_t*>(qweight), reinterpret_cast<const uint32_t*>(qzeros),
+                               scales, y, M, K, N, plan, workspace, device_error_ptr(), (cudaStream_t)stream));
+}
+
+awq_status awq_gemm(const uint16_t* x, const int32_t* qweight, const int32_t* qzeros, const uint16_t* scales,
+                    uint16_t* y, int64_t M, int64_t K, int64_t N, int32_t group_size, int32_t split_k,
+                    void* workspace, size_t workspace_bytes, awq_stream_t stream) {
+  if (!gemm_shape_ok(M, K, N, split_k) || group_size != kGroup) return AWQ_EINVAL;
+  if (M == 0) return AWQ_OK;
+  if (!x || !qweight || !scales || !y) return AWQ_ENULL;
+  if (!aligned16(x) || !aligned16(qweight) || !aligned16(scales) || !aligned16(y) || (qzeros && !aligned16(qzeros)))
+    return AWQ_EALIGN;
+  const int mode = qzeros ? kModeZeroPoint : kModeSymmetric;
+  const GemmPlan plan = gemm_plan(M, K, N, split_k, mode);
+  awq_status st = check_workspace(gemm_workspace_bytes(plan, M, K, N, mode), workspace, workspace_bytes);
+  if (st != AWQ_OK) return st;
+  st = check_arch();
+  if (st != AWQ_OK) return st;
+  int* err = device_error_ptr();
+  if (!err) return AWQ_ECUDA;
+  void* part = nullptr;
+  int* counters = nullptr;
+  if (plan.split > 1) {
+    if ((int64_t)plan.n_tiles * plan.m_tiles > kMaxCounters) return AWQ_EINVAL;
+    counters = static_cast<int*>(workspace);
+    part = static_cast<char*>(workspace) + kCounterBytes;
+  }
+  return from_cuda(launch_gemm(mode, x, reinterpret_cast<const uint32_t*>(qweight),
+                               reinterpret_cast<const uint32_t*>(qzeros), scales, nullptr, nullptr, y, nullptr, M,
+                               K, N, plan, part, counters, err, (cudaStream_t)stream));
+}
+
+awq_status w4a8_quant_act(const uint16_t* x, int8_t* xq, float* s_tok, int64_t M, int64_t K, awq_stream_t stream) {
+  if (M < 0 || K <= 0 || K % 8 != 0 || M > 0x7FFFFFFF || K > ((int64_t)1 << 30)) return AWQ_EINVAL;
+  if (M == 0) return AWQ_OK;
+  if (!x || !xq || !s_tok) return AWQ_ENULL;
+  if (!aligned16(x) || !aligned16(xq)) return AWQ_EALIGN;
+  awq_status st = check_arch();
+  if (st != AWQ_OK) return st;
+  return from_cuda(launch_quant_act(x, xq, s_tok, M, K, (cudaStream_t)stream));
+}
+
+awq_status w4a8_gemm(const int8_t* xq, const float* s_tok, const int32_t* wq, const uint16_t* s_ch, uint16_t* y,
+                     int32_t* acc_out, int64_t M, int64_t K, int64_t N, int32_t split_k, void* workspace,
+                     size_t workspace_bytes, awq_stream_t stream) {
+  if (!gemm_shape_ok(M, K, N, split_k)) return AWQ_EINVAL;
+  if (M == 0) return AWQ_OK;
+  if (!xq || !s_tok || !wq || !s_ch || !y) return AWQ_ENULL;
+  if (!aligned16(xq) || !aligned16(wq) || !aligned16(s_ch) || !aligned16(y) || (acc_out && !aligned16(acc_out)))
+    return AWQ_EALIGN;
+  const GemmPlan plan = gemm_plan(M, K, N, split_k, kModeW4A8);
+  awq_status st = check_workspace(gemm_workspace_bytes(plan, M, K, N, kModeW4A8), workspace, workspace_bytes);
+  if (st != AWQ_OK) return st;
+  st = check_arch();
+  if (st != AWQ_OK) return st;
+  int* err = device_error_ptr();
+  if (!err) return AWQ_ECUDA;
+  char* ws = static_cast<char*>(workspace);
+  uint16_t* x16 = reinterpret_cast<uint16_t*>(ws + kCounterBytes);
+  void* part = nullptr;
+  int* counters = nullptr;
+  if (plan.split > 1) {
+    if ((int64_t)plan.n_tiles * plan.m_tiles > kMaxCounters) return AWQ_EINVAL;
+    counters = reinterpret_cast<int*>(ws);
+    part = ws + kCounterBytes + align256((size_t)M * (size_t)K * 2);
+  }
+  cudaError_t e = launch_i8_to_f16(xq, x16, M * K, (cudaStream_t)stream);
+  if (e != cudaSuccess) return AWQ_ECUDA;
+  return from_cuda(launch_gemm(kModeW4A8, x16, reinterpret_cast<const uint32_t*>(wq), nullptr, nullptr, s_tok, s_ch,
+                               y, acc_out, M, K, N, plan, part, counters, err, (cudaStream_t)stream));
+}
+
+awq_status awq_last_device_error(int32_t* code) {
+  if (!code) return AWQ_ENULL;
+  *code = 0;
+  int* p = device_error_ptr();
+  if (!p) return AWQ_ECUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return AWQ_ECUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return AWQ_ECUDA;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return AWQ_ECUDA;
+  }
+  *code = v;
+  return v ? AWQ_ETIMEOUT : AWQ_OK;
+}
+
+}  // extern "C"

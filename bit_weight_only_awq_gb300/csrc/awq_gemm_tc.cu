@@ -1,0 +1,524 @@
+// Tensor-core GEMM for the AWQ linear layer (prefill, M > 8) and for W4A8.
+//
+// Source of the operation: the M > 8 branch of the AWQ dispatch snippet,
+// gemmv2_forward_cuda(inputs, qweight, scales, qzeros, group_size, split_k_iters)
+// ("Speed up AWQ 2.5x with updated kernel"), and the W4A8 GEMM of "Support W4A8
+// quantization for vllm" (int4 weights widened without a scale, per-channel scale
+// applied on the output, int32 reduction in a temporary buffer).  Kernel design:
+//
+//  * Operands are swapped so that the weights are the MMA's A operand: one CTA owns
+//    128 output columns (the MMA M dimension) and BT tokens (the MMA N dimension),
+//    D^T[n, m] accumulates in tensor memory (fp32, BT columns of 128 lanes).
+//  * A packed AWQ word holds 8 consecutive output columns of one input row, which is
+//    exactly one 16-byte chunk of an MN-major operand.  Dequant warps therefore turn
+//    each word into 8 fp16 values with shifts, one LOP3 per pair (fp16 magic 0x6400),
+//    HSUB2 of the zero and HMUL2 of the scale, and store them straight into the
+//    128-byte-swizzled MN-major layout; no transposition is needed.
+//  * TMA brings, per 64-row k-step: the activation tile (K-major, 128-byte swizzle),
+//    the packed weight tile, and the zero-point / scale rows of the step's group.
+//  * Warp roles: warp 0 issues TMA, warp 1 owns tensor memory and issues tcgen05.mma
+//    (one thread), warps 2..9 dequantize and then run the epilogue (tcgen05.ld ->
+//    fp16 / int32 -> global).  Stages are chained by mbarriers; every wait is bounded
+//    in time and records an error id instead of hanging.
+//  * split > 1: each K slice writes fp32 (W4A16) or int32 (W4A8) partials; the last
+//    CTA of an output tile (atomic ticket) sums them in slice order.
+//  * W4A8: int8 activations (converted once to fp16, exact) times int4 weights
+//    (u - 8, exact in fp16): each product is an integer of magnitude <= 1024 and each
+//    slice spans at most 16384 rows, so every fp32 partial sum is an exact integer.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+
+#include "awq_internal.h"
+
+namespace awq {
+namespace {
+
+constexpr int kBK = 64;          // input rows per k-step
+constexpr int kBN = 128;         // weight columns per CTA (MMA M)
+constexpr int kQWords = kBN / 8; // packed words per row of a stage
+constexpr int kDqWarps = 8;
+constexpr int kThreads = (2 + kDqWarps) * 32;
+constexpr int kWBytes = kBK * kBN * 2;     // dequantized tile, 16 KB
+constexpr int kQBytes = kBK * kQWords * 4; // packed tile, 4 KB
+constexpr int kZBytes = kQWords * 4;       // one zero-point row, 64 B
+constexpr int kSBytes = kBN * 2;           // one scale row, 256 B
+constexpr long long kWaitLimitNs = 2000000000LL;  // 2 s
+
+template <int BT>
+struct Cfg {
+  static constexpr int kXBytes = BT * kBK * 2;
+  static constexpr int kStageRaw = kXBytes + kWBytes + kQBytes + 128 + kSBytes;
+  static constexpr int kStageBytes = (kStageRaw + 1023) / 1024 * 1024;
+  static constexpr int kFit = (227 * 1024 - 2048) / kStageBytes;
+  static constexpr int kStages = BT >= 128 ? (kFit > 8 ? 8 : kFit) : 4;
+  static constexpr int kSmem = kStages * kStageBytes + 1024 /*align slack*/ + 1024 /*barriers*/;
+  static constexpr int kTmemCols = BT < 32 ? 32 : BT;
+  // tcgen05 instruction descriptor, kind::f16: D f32, A/B f16, A MN-major, B K-major, M=128, N=BT
+  static constexpr uint32_t kIdesc = (1u << 4) | (1u << 15) | ((uint32_t)(BT >> 3) << 17) |
+                                     ((uint32_t)(kBN >> 4) << 24);
+};
+
+// ------------------------------------------------------------------ PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ long long now_ns() {
+  long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait on an mbarrier phase.  Gives up when `abort` is raised by another
+// thread or after kWaitLimitNs; a timeout records `id` in the device error word
+// and raises `abort`.  Returns true when the phase completed.
+__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort, int* err, int id) {
+  if (mbar_try(bar, parity)) return true;
+  const long long t0 = now_ns();
+  for (uint32_t spin = 1;; ++spin) {
+    if (mbar_try(bar, parity)) return true;
+    if ((spin & 255u) == 0) {
+      if (*abort) return false;
+      if (now_ns() - t0 > kWaitLimitNs) {
+        if (err) atomicExch(err, id);
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;  // descriptor version for tcgen05
+  d |= (uint64_t)2 << 61;  // 128-byte swizzle
+  return d;
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                 "=r"(r[7])
+               : "r"(taddr)
+               : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
+  __half2 r = __hsub2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  __half2 r = __hmul2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+// pair j of a packed word: (col 2j, col 2j+1) = nibble slots (j, j+4) as fp16 1024 + code
+__device__ __forceinline__ uint32_t pair_magic(uint32_t w, int j) {
+  return ((w >> (4 * j)) & 0x000F000Fu) | 0x64006400u;
+}
+
+// ------------------------------------------------------------------ kernel
+template <int BT, int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_q,
+            const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_s,
+            __half* __restrict__ y, int32_t* __restrict__ acc_out, const float* __restrict__ s_tok,
+            const __half* __restrict__ s_ch, void* __restrict__ part, int* __restrict__ counters,
+            int* __restrict__ err, int M, int N, int K, int ksteps_per_split) {
+  using C = Cfg<BT>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
+  // bars: full[S], wready[S], empty[S], accf
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * C::kStages + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* last_flag = reinterpret_cast<int*>(tmem_slot + 2);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int n0 = blockIdx.x * kBN;
+  const int m0 = blockIdx.y * BT;
+  const int total_steps = K / kBK;
+  const int step0 = blockIdx.z * ksteps_per_split;
+  const int nsteps = min(ksteps_per_split, total_steps - step0);
+
+  auto full_bar = [&](int s) { return smem_u32(bars + s); };
+  auto wready_bar = [&](int s) { return smem_u32(bars + C::kStages + s); };
+  auto empty_bar = [&](int s) { return smem_u32(bars + 2 * C::kStages + s); };
+  const uint32_t accf_bar = smem_u32(bars + 3 * C::kStages);
+  auto stage_base = [&](int s) { return smem + s * C::kStageBytes; };
+  // stage layout: X (BT x 64 fp16, SW128) | W (64 x 128 fp16, MN-major SW128) | Q | Z | S
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(wready_bar(s), kDqWarps);
+      mbar_init(empty_bar(s), 1);
+    }
+    mbar_init(accf_bar, 1);
+    *abort_flag = 0;
+    *last_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"((uint32_t)C::kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint32_t tx = C::kXBytes + kQBytes + (MODE == kModeZeroPoint ? kZBytes : 0) +
+                          (MODE != kModeW4A8 ? kSBytes : 0);
+      int last_it[8];
+      for (int s = 0; s < 8; ++s) last_it[s] = -1;
+      for (int it = 0; it < nsteps; ++it) {
+        const int st = it % C::kStages;
+        const uint32_t ph = (uint32_t)(it / C::kStages) & 1u;
+        if (!wait_bounded(empty_bar(st), ph ^ 1u, abort_flag, err, 101)) break;
+        const int kb = (step0 + it) * kBK;
+        const int grp = kb / kGroup;
+        uint8_t* sb = stage_base(st);
+        mbar_arrive_tx(full_bar(st), tx);
+        tma_load_2d(smem_u32(sb), &tm_x, kb, m0, full_bar(st));
+        tma_load_2d(smem_u32(sb + C::kXBytes + kWBytes), &tm_q, n0 / 8, kb, full_bar(st));
+        if (MODE == kModeZeroPoint)
+          tma_load_2d(smem_u32(sb + C::kXBytes + kWBytes + kQBytes), &tm_z, n0 / 8, grp, full_bar(st));
+        if (MODE != kModeW4A8)
+          tma_load_2d(smem_u32(sb + C::kXBytes + kWBytes + kQBytes + 128), &tm_s, n0, grp, full_bar(st));
+        last_it[st] = it;
+      }
+      // never leave the CTA with copies in flight
+      for (int s = 0; s < C::kStages; ++s)
+        if (last_it[s] >= 0) {
+          volatile int no_abort = 0;
+          wait_bounded(full_bar(s), (uint32_t)(last_it[s] / C::kStages) & 1u, &no_abort, err, 102);
+        }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      bool ok = true;
+      for (int it = 0; it < nsteps && ok; ++it) {
+        const int st = it % C::kStages;
+        const uint32_t ph = (uint32_t)(it / C::kStages) & 1u;
+        ok = wait_bounded(full_bar(st), ph, abort_flag, err, 201) &&
+             wait_bounded(wready_bar(st), ph, abort_flag, err, 202);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t xs = smem_u32(stage_base(st));
+        const uint32_t ws = xs + C::kXBytes;
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk) {
+          // A: weights, MN-major; 64-column atoms 1024 B apart (LBO), 8-row k groups 2048 B apart (SBO)
+          const uint64_t ad = smem_desc_sw128(ws + kk * 2 * 2048, 1024, 2048);
+          // B: activations, K-major; 16 k = 32 B inside the 128-byte swizzle row, 8-row groups 1024 B apart
+          const uint64_t bd = smem_desc_sw128(xs + kk * 32, 16, 1024);
+          mma_f16(tmem, ad, bd, C::kIdesc, (it > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(empty_bar(st));
+      }
+      mma_commit(accf_bar);  // arrives once every issued mma has completed
+      volatile int no_abort = 0;
+      wait_bounded(accf_bar, 0, &no_abort, err, 203);
+    }
+  } else {
+    // ------------------------------------------------ dequant warps
+    const int d = threadIdx.x - 64;  // 0..255
+    const int c = d & 15;            // packed word column within the tile
+    const int r0 = d >> 4;           // first of the thread's 4 rows (r0 + 16 j)
+    for (int it = 0; it < nsteps; ++it) {
+      const int st = it % C::kStages;
+      const uint32_t ph = (uint32_t)(it / C::kStages) & 1u;
+      if (!wait_bounded(full_bar(st), ph, abort_flag, err, 301)) break;
+      if (!wait_bounded(empty_bar(st), ph ^ 1u, abort_flag, err, 302)) break;
+      uint8_t* sb = stage_base(st);
+      const uint32_t* qs = reinterpret_cast<const uint32_t*>(sb + C::kXBytes + kWBytes);
+      uint8_t* wt = sb + C::kXBytes;
+      uint32_t zp[4], sp[4];
+      if (MODE != kModeW4A8) {
+        const uint32_t zword =
+            MODE == kModeZeroPoint ? reinterpret_cast<const uint32_t*>(sb + C::kXBytes + kWBytes + kQBytes)[c]
+                                   : 0x88888888u;
+        const uint4 sv = reinterpret_cast<const uint4*>(sb + C::kXBytes + kWBytes + kQBytes + 128)[c];
+        sp[0] = sv.x; sp[1] = sv.y; sp[2] = sv.z; sp[3] = sv.w;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) zp[j] = pair_magic(zword, j);
+      }
+#pragma unroll
+      for (int jr = 0; jr < 4; ++jr) {
+        const int r = r0 + 16 * jr;
+        const uint32_t w = qs[r * kQWords + c];
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t h = pair_magic(w, j);
+          o[j] = (MODE == kModeW4A8) ? hsub2(h, 0x64086408u) /* u - 8, exact */
+                                     : hmul2(hsub2(h, zp[j]), sp[j]);
+        }
+        const uint32_t off = (uint32_t)((r >> 3) * 2048 + (c >> 3) * 1024 + (r & 7) * 128 + (((c & 7) ^ (r & 7)) << 4));
+        *reinterpret_cast<uint4*>(wt + off) = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(wready_bar(st));
+    }
+
+    // ------------------------------------------------ epilogue (same 8 warps)
+    const bool have = wait_bounded(accf_bar, 0, abort_flag, err, 401);
+    tc_fence_after();
+    const int lq = warp & 3;                 // TMEM lane quarter this warp may access
+    const int half = (warp - 2) >> 2;        // which half of the BT token columns
+    const int nl = lq * 32 + lane;           // TMEM lane = weight column in the tile
+    const int n = n0 + nl;
+    const bool n_ok = n < N;
+    const int split = gridDim.z;
+    constexpr int kHalf = BT / 2;
+    float sch = 0.f;
+    if (MODE == kModeW4A8 && n_ok) sch = __half2float(s_ch[n]);
+    if (have) {
+#pragma unroll 1
+      for (int cb = half * kHalf; cb < (half + 1) * kHalf; cb += 8) {
+        float v[8];
+        tmem_ld8(tmem + ((uint32_t)(lq * 32) << 16) + (uint32_t)cb, v);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int m = m0 + cb + j;
+          if (!n_ok || m >= M) continue;
+          const size_t o = (size_t)m * N + n;
+          if (MODE == kModeW4A8) {
+            const int a = __float2int_rn(v[j]);  // exact integer
+            if (split == 1) {
+              if (acc_out) acc_out[o] = a;
+              y[o] = __float2half_rn(__fmul_rn(__fmul_rn((float)a, s_tok[m]), sch));
+            } else {
+              reinterpret_cast<int32_t*>(part)[(size_t)blockIdx.z * M * N + o] = a;
+            }
+          } else {
+            if (split == 1) y[o] = __float2half_rn(v[j]);
+            else reinterpret_cast<float*>(part)[(size_t)blockIdx.z * M * N + o] = v[j];
+          }
+        }
+      }
+    }
+    if (split > 1) {
+      __threadfence();
+      asm volatile("bar.sync 1, %0;" ::"r"(kDqWarps * 32) : "memory");
+      if (d == 0) {
+        const int ctr = blockIdx.y * gridDim.x + blockIdx.x;
+        *last_flag = (atomicAdd(counters + ctr, 1) == split - 1);
+      }
+      asm volatile("bar.sync 1, %0;" ::"r"(kDqWarps * 32) : "memory");
+      if (*last_flag) {
+        __threadfence();
+        for (int cb = half * kHalf; cb < (half + 1) * kHalf; ++cb) {
+          const int m = m0 + cb;
+          if (!n_ok || m >= M) continue;
+          const size_t o = (size_t)m * N + n;
+          if (MODE == kModeW4A8) {
+            int a = 0;
+            for (int sp = 0; sp < split; ++sp) a += __ldcg(reinterpret_cast<const int32_t*>(part) + (size_t)sp * M * N + o);
+            if (acc_out) acc_out[o] = a;
+            y[o] = __float2half_rn(__fmul_rn(__fmul_rn((float)a, s_tok[m]), sch));
+          } else {
+            float a = 0.f;
+            for (int sp = 0; sp < split; ++sp) a += __ldcg(reinterpret_cast<const float*>(part) + (size_t)sp * M * N + o);
+            y[o] = __float2half_rn(a);
+          }
+        }
+        if (d == 0) atomicExch(counters + blockIdx.y * gridDim.x + blockIdx.x, 0);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"((uint32_t)C::kTmemCols)
+                 : "memory");
+  }
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+bool make_map_2d(CUtensorMap* map, CUtensorMapDataType dt, int elem_bytes, const void* base, uint64_t inner,
+                 uint64_t outer, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner * (uint64_t)elem_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BT, int MODE>
+cudaError_t launch_t(const uint16_t* x16, const uint32_t* qw, const uint32_t* qz, const uint16_t* sc,
+                     const float* s_tok, const uint16_t* s_ch, uint16_t* y, int32_t* acc_out, int64_t M,
+                     int64_t K, int64_t N, const GemmPlan& p, void* part, int* counters, int* err,
+                     cudaStream_t s) {
+  using C = Cfg<BT>;
+  CUtensorMap tx, tq, tz, ts;
+  const uint64_t nw = (uint64_t)N / 8, ng = (uint64_t)K / kGroup;
+  bool ok = make_map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x16, (uint64_t)K, (uint64_t)M, kBK, BT,
+                        CU_TENSOR_MAP_SWIZZLE_128B) &&
+            make_map_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, qw, nw, (uint64_t)K, kQWords, kBK,
+                        CU_TENSOR_MAP_SWIZZLE_NONE);
+  // zero-point and scale maps: dummies (the weight map) when the mode does not read them
+  ok = ok && make_map_2d(&tz, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, qz ? (const void*)qz : (const void*)qw, nw,
+                         qz ? ng : (uint64_t)K, kQWords, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
+  ok = ok && (MODE == kModeW4A8
+                  ? make_map_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, qw, nw, (uint64_t)K, kQWords, 1,
+                                CU_TENSOR_MAP_SWIZZLE_NONE)
+                  : make_map_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, sc, (uint64_t)N, ng, kBN, 1,
+                                CU_TENSOR_MAP_SWIZZLE_NONE));
+  if (!ok) return cudaErrorInvalidValue;
+  auto kern = gemm_kernel<BT, MODE>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.n_tiles, p.m_tiles, p.split);
+  kern<<<grid, kThreads, C::kSmem, s>>>(tx, tq, tz, ts, reinterpret_cast<__half*>(y), acc_out, s_tok,
+                                       reinterpret_cast<const __half*>(s_ch), part, counters, err, (int)M,
+                                       (int)N, (int)K, p.ksteps);
+  return cudaGetLastError();
+}
+
+template <int MODE>
+cudaError_t launch_mode(const uint16_t* x16, const uint32_t* qw, const uint32_t* qz, const uint16_t* sc,
+                        const float* s_tok, const uint16_t* s_ch, uint16_t* y, int32_t* acc_out, int64_t M,
+                        int64_t K, int64_t N, const GemmPlan& p, void* part, int* counters, int* err,
+                        cudaStream_t s) {
+  switch (p.bt) {
+    case 16: return launch_t<16, MODE>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters, err, s);
+    case 32: return launch_t<32, MODE>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters, err, s);
+    case 64: return launch_t<64, MODE>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters, err, s);
+    case 128: return launch_t<128, MODE>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters, err, s);
+    case 256: return launch_t<256, MODE>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters, err, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+GemmPlan gemm_plan(int64_t M, int64_t K, int64_t N, int split_k, int mode) {
+  GemmPlan p;
+  p.bt = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
+  p.n_tiles = (int)((N + kBN - 1) / kBN);
+  p.m_tiles = (int)((M + p.bt - 1) / p.bt);
+  const int total = (int)(K / kBK);
+  int split = split_k;
+  if (split <= 0) {
+    // fill the 152 SMs: largest split (<= 8, >= 8 k-steps per slice) whose CTA count stays <= one wave,
+    // if the unsplit grid is under one wave
+    const int tiles = p.n_tiles * p.m_tiles;
+    split = 1;
+    if (tiles < 152 && tiles <= kMaxCounters)
+      for (int sp = 2; sp <= 8; ++sp)
+        if (tiles * sp <= 152 && total / sp >= 8) split = sp;
+  }
+  if (mode == kModeW4A8) {
+    const int min_split = (int)((K + kW4A8MaxKSlice - 1) / kW4A8MaxKSlice);
+    if (split < min_split) split = min_split;
+  }
+  if (split > total) split = total;
+  if (split < 1) split = 1;
+  p.ksteps = (total + split - 1) / split;
+  p.split = (total + p.ksteps - 1) / p.ksteps;
+  return p;
+}
+
+// Workspace: [tile counters, kCounterBytes] [W4A8: fp16 copy of the codes] [split partials]
+size_t gemm_workspace_bytes(const GemmPlan& p, int64_t M, int64_t K, int64_t N, int mode) {
+  const size_t x16 = mode == kModeW4A8 ? align256((size_t)M * (size_t)K * 2) : 0;
+  const size_t part = p.split > 1 ? align256((size_t)p.split * (size_t)M * (size_t)N * 4) : 0;
+  if (x16 == 0 && part == 0) return 0;
+  return kCounterBytes + x16 + part;
+}
+
+cudaError_t launch_gemm(int mode, const uint16_t* x16, const uint32_t* qw, const uint32_t* qz, const uint16_t* sc,
+                        const float* s_tok, const uint16_t* s_ch, uint16_t* y, int32_t* acc_out, int64_t M,
+                        int64_t K, int64_t N, const GemmPlan& p, void* part, int* counters, int* err,
+                        cudaStream_t s) {
+  switch (mode) {
+    case kModeZeroPoint:
+      return launch_mode<kModeZeroPoint>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters, err, s);
+    case kModeSymmetric:
+      return launch_mode<kModeSymmetric>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters, err, s);
+    case kModeW4A8:
+      return launch_mode<kModeW4A8>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters, err, s);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace awq

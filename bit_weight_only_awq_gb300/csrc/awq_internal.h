@@ -1,0 +1,75 @@
+// Private declarations shared by the translation units of libawq.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace awq {
+
+// Order map of the older AWQ format: nibble slot i holds logical column
+// order_map(i), map = [0, 2, 4, 6, 1, 3, 5, 7].
+// Source: "Speed up AWQ 2.5x with updated kernel", casper-hansen's format differences.
+__host__ __device__ constexpr int order_map(int slot) { return 2 * (slot & 3) + (slot >> 2); }
+// Inverse: logical column j lives in nibble slot slot_of_col(j) = [0, 4, 1, 5, 2, 6, 3, 7][j].
+__host__ __device__ constexpr int slot_of_col(int col) { return (col >> 1) + 4 * (col & 1); }
+static_assert(order_map(0) == 0 && order_map(1) == 2 && order_map(3) == 6 && order_map(4) == 1 &&
+                  order_map(7) == 7 && slot_of_col(order_map(5)) == 5 && slot_of_col(1) == 4,
+              "AWQ order map");
+
+constexpr int kGroup = 128;          // GPU path group size (input channels per scale)
+constexpr int kGemvMaxM = 8;         // decode path handles up to 8 tokens
+constexpr int kW4A8MaxKSlice = 16384;  // exact-integer bound of an fp32 tensor-core sum
+
+// Workspace layout shared by every split-K call: a fixed 64 KB block of tile
+// counters at offset 0 (so that a zeroed workspace stays valid across calls of
+// any shape: each call returns its counters to zero), then call-specific data.
+constexpr size_t kCounterBytes = 65536;
+constexpr int kMaxCounters = (int)(kCounterBytes / sizeof(int));
+inline size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
+
+// Device error word (one per device, inside the library): kernels record the id
+// of a bounded wait that expired; the host reads and clears it.
+int* device_error_ptr();  // nullptr if the symbol address could not be obtained
+
+// ---- elementwise kernels (awq_elementwise.cu)
+cudaError_t launch_pack(const uint8_t* q, int64_t rows, int64_t n, uint32_t* packed, cudaStream_t s);
+cudaError_t launch_unpack(const uint32_t* packed, int64_t rows, int64_t n, uint8_t* q, cudaStream_t s);
+cudaError_t launch_dequant(const uint32_t* qw, const uint32_t* qz, const uint16_t* scales, int64_t K,
+                           int64_t N, int group, uint16_t* w, cudaStream_t s);
+
+// ---- decode GEMV (awq_gemv.cu)
+struct GemvPlan {
+  int split;            // K slices (grid.y)
+  int groups_per_split; // 128-row groups per slice
+  int tiles;            // 128-column tiles (grid.x)
+};
+GemvPlan gemv_plan(int64_t M, int64_t K, int64_t N, int split_k);
+size_t gemv_workspace_bytes(const GemvPlan& p, int64_t M, int64_t N);
+cudaError_t launch_gemv(const uint16_t* x, const uint32_t* qw, const uint32_t* qz, const uint16_t* sc,
+                        uint16_t* y, int64_t M, int64_t K, int64_t N, const GemvPlan& p, void* ws,
+                        int* err, cudaStream_t s);
+
+// ---- tensor-core GEMM (awq_gemm_tc.cu)
+enum GemmMode { kModeZeroPoint = 0, kModeSymmetric = 1, kModeW4A8 = 2 };
+struct GemmPlan {
+  int bt;        // token tile (MMA N): 16, 32, 64, 128 or 256
+  int split;     // K slices (grid.z)
+  int ksteps;    // 64-row k-steps per slice
+  int n_tiles;   // 128-column weight tiles (grid.x)
+  int m_tiles;   // token tiles (grid.y)
+};
+GemmPlan gemm_plan(int64_t M, int64_t K, int64_t N, int split_k, int mode);
+size_t gemm_workspace_bytes(const GemmPlan& p, int64_t M, int64_t K, int64_t N, int mode);
+// x16: fp16 activations [M, K] (for W4A8 the fp16 copy of the int8 codes).
+cudaError_t launch_gemm(int mode, const uint16_t* x16, const uint32_t* qw, const uint32_t* qz,
+                        const uint16_t* sc, const float* s_tok, const uint16_t* s_ch, uint16_t* y,
+                        int32_t* acc_out, int64_t M, int64_t K, int64_t N, const GemmPlan& p,
+                        void* ws_partials, int* counters, int* err, cudaStream_t s);
+
+// ---- W4A8 activation kernels (w4a8_act.cu)
+cudaError_t launch_quant_act(const uint16_t* x, int8_t* xq, float* s_tok, int64_t M, int64_t K,
+                             cudaStream_t s);
+cudaError_t launch_i8_to_f16(const int8_t* xq, uint16_t* x16, int64_t count, cudaStream_t s);
+
+}  // namespace awq

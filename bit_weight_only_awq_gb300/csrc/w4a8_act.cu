@@ -1,0 +1,101 @@
+// W4A8 activation kernels: per-token dynamic int8 quantization and the exact int8 -> fp16
+// widening that feeds the fp16 tensor path.
+//
+// Source: "Support W4A8 quantization for vllm" (vLLM pull request #5218): the dynamic_quant
+// function of brisker's consistency script (scale = absmax of the fp16 row / 127 computed in
+// fp16, widened to float; codes = round(x / scale) clamped to [-128, 127]) and HandH1998's
+// note that this per-token scale is computed online.
+#include <cuda_fp16.h>
+
+#include "awq_internal.h"
+
+namespace awq {
+namespace {
+
+constexpr int kQThreads = 256;
+
+// One CTA per token row: pass 1 finds absmax, pass 2 writes the codes (second read hits L2).
+__global__ void __launch_bounds__(kQThreads)
+quant_act_kernel(const __half* __restrict__ x, int8_t* __restrict__ xq, float* __restrict__ s_tok, int K) {
+  __shared__ uint32_t warp_max[kQThreads / 32];
+  __shared__ float s_shared;
+  const int64_t row = blockIdx.x;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + row * (int64_t)K);
+  const int nvec = K / 8;
+
+  uint32_t mx = 0;  // |x| as fp16 bits: integer order equals magnitude order for finite values
+  for (int i = threadIdx.x; i < nvec; i += kQThreads) {
+    const uint4 v = __ldg(xr + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      mx = max(mx, w[j] & 0x7FFFu);
+      mx = max(mx, (w[j] >> 16) & 0x7FFFu);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+  if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = mx;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t m = 0;
+    for (int w = 0; w < kQThreads / 32; ++w) m = max(m, warp_max[w]);
+    const float absmax = __half2float(__ushort_as_half((unsigned short)m));
+    // fp16 division of the page's script: fp32 quotient rounded once to fp16, then widened
+    const float s = __half2float(__float2half_rn(__fdiv_rn(absmax, 127.0f)));
+    s_shared = s;
+    s_tok[row] = s;
+  }
+  __syncthreads();
+  const float s = s_shared;
+  uint2* qr = reinterpret_cast<uint2*>(xq + row * (int64_t)K);
+  for (int i = threadIdx.x; i < nvec; i += kQThreads) {
+    const uint4 v = __ldg(xr + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t out[2] = {0, 0};
+    if (s > 0.f) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float xv = __half2float(__ushort_as_half((unsigned short)(w[j >> 1] >> (16 * (j & 1)))));
+        float qv = rintf(__fdiv_rn(xv, s));
+        qv = fminf(fmaxf(qv, -128.f), 127.f);
+        out[j >> 2] |= ((uint32_t)(int)qv & 0xFFu) << (8 * (j & 3));
+      }
+    }
+    qr[i] = make_uint2(out[0], out[1]);
+  }
+}
+
+__global__ void i8_to_f16_kernel(const int8_t* __restrict__ xq, __half* __restrict__ out, int64_t nvec) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < nvec; i += (int64_t)gridDim.x * blockDim.x) {
+    const uint2 v = __ldg(reinterpret_cast<const uint2*>(xq) + i);
+    uint32_t o[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      const uint32_t w = p < 2 ? v.x : v.y;
+      const int a = (int)(int8_t)((w >> (16 * (p & 1))) & 0xFF);
+      const int b = (int)(int8_t)((w >> (16 * (p & 1) + 8)) & 0xFF);
+      o[p] = (uint32_t)__half_as_ushort(__int2half_rn(a)) | ((uint32_t)__half_as_ushort(__int2half_rn(b)) << 16);
+    }
+    reinterpret_cast<uint4*>(out)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_quant_act(const uint16_t* x, int8_t* xq, float* s_tok, int64_t M, int64_t K, cudaStream_t s) {
+  if (M == 0) return cudaSuccess;
+  quant_act_kernel<<<(unsigned)M, kQThreads, 0, s>>>(reinterpret_cast<const __half*>(x), xq, s_tok, (int)K);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_i8_to_f16(const int8_t* xq, uint16_t* x16, int64_t count, cudaStream_t s) {
+  const int64_t nvec = count / 8;
+  if (nvec == 0) return cudaSuccess;
+  int64_t blocks = (nvec + 255) / 256;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  i8_to_f16_kernel<<<(unsigned)blocks, 256, 0, s>>>(xq, reinterpret_cast<__half*>(x16), nvec);
+  return cudaGetLastError();
+}
+
+}  // namespace awq

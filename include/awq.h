@@ -1,0 +1,178 @@
+/*
+ * awq.h -- C ABI of libawq, a GB300 (sm_103a) implementation of the group-wise
+ * INT4 weight-only quantized linear layer (AWQ W4A16) and its W4A8 variant.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every pointer argument is a DEVICE pointer on the current CUDA device,
+ *    unless the comment says otherwise.  The caller owns every buffer; the
+ *    library allocates nothing (scratch space is the caller's `workspace`).
+ *  - fp16 values travel as raw IEEE binary16 bits in uint16_t.
+ *  - Matrices are dense and row-major.  M = tokens, K = input features
+ *    (reduction), N = output features, group_size = input channels per
+ *    quantization group (128 on the GPU path).
+ *  - Every call is asynchronous on `stream` (NULL = the legacy default
+ *    stream).  Argument checks run on the host before anything is launched;
+ *    a failing check returns a negative status and launches nothing.  No
+ *    C++ exception crosses this boundary.
+ *  - Packing ("older" AWQ format): a packed int32 word c of a row holds the
+ *    4-bit codes of logical columns 8c..8c+7; nibble slot i (bits 4i..4i+3)
+ *    holds column 8c + map[i] with map = [0, 2, 4, 6, 1, 3, 5, 7].
+ *    Source: "Speed up AWQ 2.5x with updated kernel" (vLLM pull request),
+ *    casper-hansen's list of format differences between the older and the
+ *    new AWQ format.
+ *  - Pointers to matrices must be 16-byte aligned (AWQ_EALIGN otherwise).
+ */
+#ifndef AWQ_H_
+#define AWQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream; NULL selects the legacy default stream. */
+typedef struct CUstream_st *awq_stream_t;
+
+typedef enum {
+  AWQ_OK = 0,
+  AWQ_EINVAL = -1,      /* a size or shape argument is out of range */
+  AWQ_EALIGN = -2,      /* a matrix pointer is not 16-byte aligned */
+  AWQ_EARCH = -3,       /* the current device is not a compute-capability 10.3 GPU */
+  AWQ_ECUDA = -4,       /* a CUDA runtime call or a kernel launch failed */
+  AWQ_ETIMEOUT = -5,    /* a bounded device-side wait expired (awq_last_device_error) */
+  AWQ_EWORKSPACE = -6,  /* workspace NULL or smaller than awq_workspace_bytes() */
+  AWQ_ENULL = -7        /* a required pointer is NULL */
+} awq_status;
+
+/* Operation selector for awq_workspace_bytes(). */
+typedef enum { AWQ_OP_GEMV = 0, AWQ_OP_GEMM = 1, AWQ_OP_W4A8_GEMM = 2 } awq_op;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *awq_status_string(awq_status status);
+
+/*
+ * awq_pack -- pack 4-bit codes into AWQ int32 words.
+ * q: uint8 [rows, n] codes (values above 15 are clamped to 15);
+ * packed: int32 [rows, n/8].  n % 8 == 0, rows >= 0.
+ * Source: the older-format order map ("Speed up AWQ 2.5x with updated
+ * kernel", casper-hansen's format differences); the clamp follows the packer
+ * fix reported in "Support W4A8 quantization for vllm" (HandH1998's reply to
+ * brisker about the missing clamp in the per-channel pack).
+ */
+awq_status awq_pack(const uint8_t *q, int64_t rows, int64_t n, int32_t *packed,
+                    awq_stream_t stream);
+
+/* awq_unpack -- inverse of awq_pack: packed int32 [rows, n/8] -> uint8 codes [rows, n]. */
+awq_status awq_unpack(const int32_t *packed, int64_t rows, int64_t n, uint8_t *q,
+                      awq_stream_t stream);
+
+/*
+ * awq_dequant -- W[k, n] = fp16_RN((q[k, n] - z[k / g, n]) * s[k / g, n]).
+ * qweight int32 [K, N/8]; qzeros int32 [K/g, N/8] or NULL for the symmetric
+ * variant (z = 8); scales fp16 [K/g, N]; w fp16 [K, N] (output).
+ * K % group_size == 0, N % 8 == 0, group_size in {32, 64, 128, 256}.
+ * The result is bit-identical to the correctly rounded product.
+ * Source: the qweight / scales / qzeros / group_size operands of the AWQ
+ * kernels ("Speed up AWQ 2.5x with updated kernel", dispatch snippet);
+ * symmetric variant: "Marlin symmetric quantization and inference".
+ */
+awq_status awq_dequant(const int32_t *qweight, const int32_t *qzeros, const uint16_t *scales,
+                       int64_t K, int64_t N, int32_t group_size, uint16_t *w,
+                       awq_stream_t stream);
+
+/*
+ * awq_workspace_bytes -- bytes of caller-owned workspace that awq_gemv,
+ * awq_gemm or w4a8_gemm need for the given shape and split_k (0 = the
+ * library's automatic choice, which this function resolves the same way the
+ * compute call does).  Returns 0 when no workspace is needed.
+ *
+ * Workspace contract: before its FIRST use the workspace must be zero-filled
+ * (cudaMemsetAsync); every call that completes leaves its tile counters at
+ * zero again, so consecutive calls on one stream can reuse it without
+ * re-zeroing.  Calls that may run concurrently need separate workspaces.
+ * After AWQ_ETIMEOUT, zero the workspace again before reusing it.
+ */
+size_t awq_workspace_bytes(awq_op op, int64_t M, int64_t K, int64_t N, int32_t split_k);
+
+/*
+ * awq_gemv -- y = x * W for M <= 8 tokens (decode), W dequantized on the fly.
+ * x fp16 [M, K]; qweight int32 [K, N/8]; qzeros int32 [K/128, N/8] or NULL
+ * (symmetric, z = 8); scales fp16 [K/128, N]; y fp16 [M, N] (output).
+ * 1 <= M <= 8, K % 128 == 0, N % 16 == 0, group_size == 128.
+ * split_k: number of K slices reduced in fp32 (0 = automatic); the fp16
+ * output is rounded once from the fp32 sum.  Needs a workspace when the
+ * resolved split_k exceeds 1.
+ * Source: the M <= 8 branch of the dispatch snippet, gemv_forward_cuda(inputs,
+ * qweight, scales, qzeros, group_size) ("Speed up AWQ 2.5x with updated kernel").
+ */
+awq_status awq_gemv(const uint16_t *x, const int32_t *qweight, const int32_t *qzeros,
+                    const uint16_t *scales, uint16_t *y, int64_t M, int64_t K, int64_t N,
+                    int32_t group_size, int32_t split_k, void *workspace,
+                    size_t workspace_bytes, awq_stream_t stream);
+
+/*
+ * awq_gemm -- y = x * W on the tensor cores (tcgen05, fp16 x fp16 -> fp32 in
+ * tensor memory) for any M >= 1 (intended for M > 8: prefill).
+ * Same operands and layouts as awq_gemv; K % 128 == 0, N % 32 == 0,
+ * group_size == 128.  split_k: K slices reduced in fp32 (0 = automatic).
+ * Source: the M > 8 branch of the dispatch snippet, gemmv2_forward_cuda(
+ * inputs, qweight, scales, qzeros, group_size, split_k_iters) ("Speed up AWQ
+ * 2.5x with updated kernel").
+ */
+awq_status awq_gemm(const uint16_t *x, const int32_t *qweight, const int32_t *qzeros,
+                    const uint16_t *scales, uint16_t *y, int64_t M, int64_t K, int64_t N,
+                    int32_t group_size, int32_t split_k, void *workspace,
+                    size_t workspace_bytes, awq_stream_t stream);
+
+/*
+ * w4a8_quant_act -- per-token dynamic int8 quantization of activations.
+ * x fp16 [M, K]; xq int8 [M, K] (output); s_tok fp32 [M] (output).
+ * s_tok[m] = fp32(fp16_RN(absmax_k |x[m, k]| / 127)) computed in fp32,
+ * xq = clamp(rint(x / s_tok), -128, 127); an all-zero row gives s = 0, xq = 0.
+ * M >= 1, K % 8 == 0.
+ * Source: "Support W4A8 quantization for vllm", the dynamic_quant function of
+ * brisker's consistency script and HandH1998's note that s1 is the dynamic
+ * per-token scale computed online.
+ */
+awq_status w4a8_quant_act(const uint16_t *x, int8_t *xq, float *s_tok, int64_t M, int64_t K,
+                          awq_stream_t stream);
+
+/*
+ * w4a8_gemm -- W4A8 product with exact int32 accumulation.
+ * xq int8 [M, K]; s_tok fp32 [M]; wq int32 [K, N/8] holding u = q + 8 for
+ * signed int4 weights q in [-8, 7], AWQ packing; s_ch fp16 [N] per-output-
+ * channel scales; y fp16 [M, N] (output); acc_out int32 [M, N] (optional
+ * output of the exact accumulator, NULL to skip).
+ * acc[m, n] = sum_k xq[m, k] * q[k, n] (exact), y = fp16_RN((fp32(acc) *
+ * s_tok[m]) * fp32(s_ch[n])).  K % 128 == 0, N % 32 == 0.
+ * Always needs a workspace (it holds an fp16 copy of xq for the fp16 tensor
+ * path; every int8 and int4 value and every product is exact in fp16/fp32).
+ * split_k: K slices reduced in int32 (0 = automatic; each slice spans at most
+ * 16384 inputs so its fp32 tensor-core sum stays an exact integer).
+ * Source: "Support W4A8 quantization for vllm": marlin_qqq_gemm(a, b_q_weight,
+ * s1, s2, s3, workspace, size_m, size_n, size_k) in tlrmchlsmth's review;
+ * HandH1998's per-channel dequantization (int4 to int8, channel scale on the
+ * output); alexm's note that the global reduce works on int32 elements in a
+ * temporary buffer C.
+ */
+awq_status w4a8_gemm(const int8_t *xq, const float *s_tok, const int32_t *wq,
+                     const uint16_t *s_ch, uint16_t *y, int32_t *acc_out, int64_t M, int64_t K,
+                     int64_t N, int32_t split_k, void *workspace, size_t workspace_bytes,
+                     awq_stream_t stream);
+
+/*
+ * awq_last_device_error -- reads and clears the device-side error word of the
+ * current device (synchronous: waits for the device).  *code receives 0 when
+ * no bounded wait expired since the last read, else the id of the wait that
+ * gave up.  Returns AWQ_ETIMEOUT when *code != 0.
+ */
+awq_status awq_last_device_error(int32_t *code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* AWQ_H_ */

@@ -1,0 +1,120 @@
+"""Host-side checks of the C ABI (no GPU needed, no compute call is made).
+
+* the library builds and exports every function include/awq.h declares;
+* argument checks reject bad shapes, NULL and misaligned pointers and short
+  workspaces before anything touches the GPU;
+* workspace sizing follows the documented layout.
+"""
+
+import ctypes
+import re
+import subprocess
+
+import pytest
+
+from bit_weight_only_awq_gb300 import build as awq_build
+
+
+@pytest.fixture(scope="module")
+def awq():
+    awq_build.build()
+    from bit_weight_only_awq_gb300 import awq as mod
+    return mod
+
+
+EINVAL, EALIGN, EWORKSPACE, ENULL = -1, -2, -6, -7
+FAKE = 1 << 40          # an aligned address that is never dereferenced (checks run first)
+FAKE_MISALIGNED = FAKE + 4
+
+
+def test_header_declares_the_boundary(awq):
+    names = awq.header_functions()
+    for want in ("awq_pack", "awq_unpack", "awq_dequant", "awq_gemv", "awq_gemm", "awq_workspace_bytes",
+                 "w4a8_quant_act", "w4a8_gemm", "awq_status_string", "awq_last_device_error"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(awq):
+    out = subprocess.run(["nm", "-D", "--defined-only", awq._LIB_PATH], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(re.findall(r" T (\w+)$", out, re.M))
+    for name in awq.header_functions():
+        assert name in exported, name
+        assert getattr(awq.lib, name) is not None
+
+
+def test_status_strings(awq):
+    for code, name in awq.STATUS.items():
+        assert awq.lib.awq_status_string(code).decode().startswith(name)
+
+
+def _gemv(awq, M=1, K=4096, N=4096, g=128, split=0, x=FAKE, qw=FAKE, qz=FAKE, sc=FAKE, y=FAKE, ws=None, wsb=0):
+    return awq.lib.awq_gemv(x, qw, qz, sc, y, M, K, N, g, split, ws, wsb, None)
+
+
+def test_gemv_rejects_bad_shapes_before_launch(awq):
+    assert _gemv(awq, M=9) == EINVAL
+    assert _gemv(awq, M=-1) == EINVAL
+    assert _gemv(awq, K=100) == EINVAL
+    assert _gemv(awq, N=24) == EINVAL
+    assert _gemv(awq, g=64) == EINVAL
+    assert _gemv(awq, split=-2) == EINVAL
+
+
+def test_gemv_rejects_null_and_misaligned(awq):
+    assert _gemv(awq, x=None) == ENULL
+    assert _gemv(awq, y=None) == ENULL
+    assert _gemv(awq, qw=FAKE_MISALIGNED) == EALIGN
+    assert _gemv(awq, sc=FAKE_MISALIGNED) == EALIGN
+
+
+def test_gemv_requires_workspace_when_split(awq):
+    need = awq.awq_workspace_bytes(awq.OP_GEMV, 4, 4096, 4096, 4)
+    assert need > 0
+    assert _gemv(awq, M=4, split=4) == EWORKSPACE
+    assert _gemv(awq, M=4, split=4, ws=FAKE, wsb=need - 1) == EWORKSPACE
+    assert _gemv(awq, M=4, split=4, ws=FAKE + 16, wsb=need) == EALIGN   # workspace wants 256-byte alignment
+
+
+def test_empty_batch_is_a_noop(awq):
+    assert _gemv(awq, M=0, x=None, y=None) == 0
+    assert awq.lib.awq_gemm(None, None, None, None, None, 0, 4096, 4096, 128, 0, None, 0, None) == 0
+    assert awq.lib.awq_pack(None, 0, 64, None, None) == 0
+
+
+def test_gemm_and_w4a8_argument_checks(awq):
+    f = awq.lib.awq_gemm
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 256, 4096, 4112, 128, 0, None, 0, None) == EINVAL   # N % 32
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 256, 4000, 4096, 128, 0, None, 0, None) == EINVAL   # K % 128
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 256, 4096, 4096, 32, 0, None, 0, None) == EINVAL    # group size
+    g = awq.lib.w4a8_gemm
+    assert g(FAKE, FAKE, FAKE, FAKE, FAKE, None, 4, 21760, 8192, 0, None, 0, None) == EWORKSPACE
+    assert g(None, FAKE, FAKE, FAKE, FAKE, None, 4, 21760, 8192, 0, None, 0, None) == ENULL
+    q = awq.lib.w4a8_quant_act
+    assert q(FAKE, FAKE, FAKE, 4, 100, None) == EINVAL
+    assert q(FAKE, FAKE_MISALIGNED, FAKE, 4, 128, None) == EALIGN
+    assert awq.lib.awq_dequant(FAKE, None, FAKE, 128, 64, 96, FAKE, None) == EINVAL
+    assert awq.lib.awq_unpack(FAKE, 4, 12, FAKE, None) == EINVAL
+
+
+def test_workspace_layout(awq):
+    counters = 65536
+    # GEMV: counters block + split x M x N fp32 partials (256-byte rounded)
+    assert awq.awq_workspace_bytes(awq.OP_GEMV, 8, 4096, 4096, 1) == 0
+    assert awq.awq_workspace_bytes(awq.OP_GEMV, 8, 4096, 4096, 4) == counters + 4 * 8 * 4096 * 4
+    # W4A8 at K = 21760 must split K into slices of at most 16384 rows: at least 2 slices
+    ws = awq.awq_workspace_bytes(awq.OP_W4A8_GEMM, 4096, 21760, 8192, 0)
+    x16 = 4096 * 21760 * 2
+    assert ws >= counters + x16 + 2 * 4096 * 8192 * 4
+    # a forced single slice is raised to the minimum
+    assert awq.awq_workspace_bytes(awq.OP_W4A8_GEMM, 16, 21760, 8192, 1) == counters + 16 * 21760 * 2 + 2 * 16 * 8192 * 4
+    # small-K W4A8 without split still needs the fp16 copy of the codes
+    assert awq.awq_workspace_bytes(awq.OP_W4A8_GEMM, 4096, 4096, 8192, 1) == counters + 4096 * 4096 * 2
+    # invalid shapes need nothing (the compute call reports the error)
+    assert awq.awq_workspace_bytes(awq.OP_GEMM, 16, 100, 4096, 0) == 0
+
+
+def test_binding_has_no_fallback(awq):
+    src = open(awq.__file__).read()
+    assert "oracle" not in src
+    assert "numpy" not in src

@@ -1,0 +1,233 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the same seeded inputs.
+
+Bars (written here, derived in the design doc):
+* packing, unpacking, dequantized weights, W4A8 codes / scales / int32 accumulators
+  and W4A8 fp16 outputs: bit-exact;
+* W4A16 fp16 outputs (GEMV, GEMM): max |y_gpu - y_oracle| <= 2e-3 * rms(y_oracle),
+  with y_oracle the unrounded float64 product of the oracle's fp16 weights.
+Small cases cover several tiles and ragged tails; full workload shapes are checked
+on seeded column / row samples that the oracle computes one by one.
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+from bit_weight_only_awq_gb300 import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-3
+
+
+@pytest.fixture(scope="module")
+def awq():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from bit_weight_only_awq_gb300 import build as awq_build
+    awq_build.build()
+    from bit_weight_only_awq_gb300 import awq as mod
+    return mod
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def host(t):
+    torch.cuda.synchronize()
+    return t.cpu().numpy()
+
+
+def assert_within_tol(y_gpu16, ref64, what=""):
+    y = y_gpu16.astype(np.float64)
+    rms = np.sqrt(np.mean(ref64 ** 2))
+    err = np.max(np.abs(y - ref64))
+    assert np.all(np.isfinite(y)), what
+    assert err <= TOL * rms, f"{what}: max err {err:.3e} > {TOL} * rms {rms:.3e}"
+
+
+def oracle_columns(p, word_cols):
+    """Oracle output restricted to the output columns of the given packed word columns."""
+    qw = p["qweight"][:, word_cols]
+    qz = None if p["qzeros"] is None else p["qzeros"][:, word_cols]
+    cols = (8 * np.asarray(word_cols)[:, None] + np.arange(8)[None, :]).ravel()
+    sc = p["scales"][:, cols]
+    return oracle.awq_linear(p["x"], qw, qz, sc, p["group_size"]), cols
+
+
+def sample_word_cols(nw, seed, count=48):
+    rng = np.random.default_rng(seed)
+    pick = set(rng.choice(nw, size=min(count, nw), replace=False).tolist()) | {0, nw - 1}
+    return np.array(sorted(pick))
+
+
+def run_w4a16(awq, fn, p, split_k=0):
+    x = dev(p["x"])
+    qw = dev(p["qweight"])
+    qz = None if p["qzeros"] is None else dev(p["qzeros"])
+    sc = dev(p["scales"])
+    return host(fn(x, qw, qz, sc, 128, split_k=split_k))
+
+
+# ---------------------------------------------------------------- packing / dequant
+@pytest.mark.parametrize("rows,n", [(37, 200), (1, 8), (256, 4096)])
+def test_pack_unpack_bitexact(awq, rows, n):
+    codes = synth.random_codes(rows, n, seed=rows + n, high=32)      # includes codes that must clamp
+    got = host(awq.awq_pack(dev(codes)))
+    assert np.array_equal(got, oracle.pack(codes))
+    words = synth.random_words(np.random.default_rng(rows), rows, n // 8)
+    assert np.array_equal(host(awq.awq_unpack(dev(words))), oracle.unpack(words))
+
+
+@pytest.mark.parametrize("symmetric", [False, True])
+@pytest.mark.parametrize("K,N,g", [(512, 512, 128), (384, 264, 128), (256, 64, 64)])
+def test_dequant_bitexact(awq, K, N, g, symmetric):
+    p = synth.awq_problem(1, K, N, seed=K + N, group_size=g, symmetric=symmetric)
+    got = host(awq.awq_dequant(dev(p["qweight"]), None if symmetric else dev(p["qzeros"]), dev(p["scales"]), g))
+    want = oracle.dequant(p["qweight"], p["qzeros"], p["scales"], g)
+    assert np.array_equal(got.view(np.uint16), want.view(np.uint16))
+
+
+def test_dequant_bitexact_tiny_and_subnormal_scales(awq):
+    p = synth.awq_problem(1, 256, 256, seed=5)
+    rng = np.random.default_rng(6)
+    bits = rng.integers(0x0001, 0x2000, size=p["scales"].shape, dtype=np.int64).astype(np.uint16)
+    scales = bits.view(np.float16)
+    got = host(awq.awq_dequant(dev(p["qweight"]), dev(p["qzeros"]), dev(scales), 128))
+    want = oracle.dequant(p["qweight"], p["qzeros"], scales, 128)
+    assert np.array_equal(got.view(np.uint16), want.view(np.uint16))
+
+
+# ---------------------------------------------------------------- GEMV (M <= 8)
+def test_gemv_tiny_config(awq):
+    p = synth.awq_problem(1, 512, 512, seed=0)
+    y = run_w4a16(awq, awq.awq_gemv, p)
+    assert_within_tol(y, oracle.awq_linear(p["x"], p["qweight"], p["qzeros"], p["scales"], 128), "tiny")
+
+
+@pytest.mark.parametrize("symmetric", [False, True])
+@pytest.mark.parametrize("split_k", [1, 3, 0])
+@pytest.mark.parametrize("M", [1, 2, 3, 5, 8])
+def test_gemv_small_ragged(awq, M, split_k, symmetric):
+    # N = 400: 50 packed words, 4 column tiles with a ragged last tile; K = 1280: 10 groups
+    p = synth.awq_problem(M, 1280, 400, seed=100 + M, symmetric=symmetric)
+    y = run_w4a16(awq, awq.awq_gemv, p, split_k)
+    ref = oracle.awq_linear(p["x"], p["qweight"], p["qzeros"], p["scales"], 128)
+    assert_within_tol(y, ref, f"gemv M={M} split={split_k} sym={symmetric}")
+
+
+@pytest.mark.parametrize("M", [1, 8])
+@pytest.mark.parametrize("name,K,N", synth.LLAMA2_7B_DECODE)
+def test_gemv_llama2_shapes_sampled(awq, name, K, N, M):
+    p = synth.awq_problem(M, K, N, seed=1000 + K + N + M)
+    y = run_w4a16(awq, awq.awq_gemv, p)
+    wc = sample_word_cols(N // 8, seed=K + N)
+    ref, cols = oracle_columns(p, wc)
+    assert_within_tol(y[:, cols], ref, f"gemv {name} M={M}")
+
+
+def test_gemv_repeatable_with_workspace_reuse(awq):
+    p = synth.awq_problem(4, 4096, 4096, seed=77)
+    y1 = run_w4a16(awq, awq.awq_gemv, p, 8)
+    y2 = run_w4a16(awq, awq.awq_gemv, p, 8)
+    assert np.array_equal(y1.view(np.uint16), y2.view(np.uint16))
+
+
+# ---------------------------------------------------------------- GEMM (tensor cores)
+@pytest.mark.parametrize("symmetric", [False, True])
+@pytest.mark.parametrize("M", [1, 9, 16, 40, 64, 100, 128, 200, 256, 300])
+def test_gemm_small_ragged(awq, M, symmetric):
+    # N = 416: 4 weight tiles, last one ragged; K = 640: 10 k-steps, 5 groups
+    p = synth.awq_problem(M, 640, 416, seed=200 + M, symmetric=symmetric)
+    y = run_w4a16(awq, awq.awq_gemm, p, 1)
+    ref = oracle.awq_linear(p["x"], p["qweight"], p["qzeros"], p["scales"], 128)
+    assert_within_tol(y, ref, f"gemm M={M} sym={symmetric}")
+
+
+@pytest.mark.parametrize("split_k", [2, 3, 0])
+def test_gemm_split_k(awq, split_k):
+    p = synth.awq_problem(70, 1024, 256, seed=300 + split_k)
+    y = run_w4a16(awq, awq.awq_gemm, p, split_k)
+    ref = oracle.awq_linear(p["x"], p["qweight"], p["qzeros"], p["scales"], 128)
+    assert_within_tol(y, ref, f"gemm split={split_k}")
+
+
+@pytest.mark.parametrize("M", [256, 1024])
+@pytest.mark.parametrize("name,K,N", synth.MISTRAL_7B_PREFILL)
+def test_gemm_mistral_shapes_sampled(awq, name, K, N, M):
+    p = synth.awq_problem(M, K, N, seed=2000 + K + N + M)
+    y = run_w4a16(awq, awq.awq_gemm, p)
+    wc = sample_word_cols(N // 8, seed=K + N, count=24)
+    ref, cols = oracle_columns(p, wc)
+    assert_within_tol(y[:, cols], ref, f"gemm {name} M={M}")
+
+
+def test_gemm_largest_prefill_sampled_rows(awq):
+    K, N, M = 4096, 28672, 8192
+    p = synth.awq_problem(M, K, N, seed=2999)
+    y = run_w4a16(awq, awq.awq_gemm, p)
+    rows = np.array(sorted(set(np.random.default_rng(1).choice(M, 40, replace=False).tolist()) | {0, M - 1}))
+    wc = sample_word_cols(N // 8, seed=3, count=16)
+    sub = dict(p, x=p["x"][rows])
+    ref, cols = oracle_columns(sub, wc)
+    assert_within_tol(y[np.ix_(rows, cols)], ref, "gemm gate_up M=8192")
+
+
+@pytest.mark.parametrize("M", [1, 8])
+def test_gemm_and_gemv_agree_at_small_m(awq, M):
+    p = synth.awq_problem(M, 4096, 6144, seed=400 + M, symmetric=(M == 8))
+    yv = run_w4a16(awq, awq.awq_gemv, p).astype(np.float64)
+    yg = run_w4a16(awq, awq.awq_gemm, p).astype(np.float64)
+    ref = oracle.awq_linear(p["x"], p["qweight"], p["qzeros"], p["scales"], 128)
+    assert_within_tol(yv, ref, "gemv")
+    assert_within_tol(yg, ref, "gemm")
+
+
+# ---------------------------------------------------------------- W4A8
+@pytest.mark.parametrize("M,K", [(1, 21760), (5, 1024), (64, 21760)])
+def test_quant_act_bitexact(awq, M, K):
+    x = synth.activations(np.random.default_rng(M + K), M, K)
+    if M > 2:
+        x[2] = 0                      # an all-zero token row
+    xq, s = awq.w4a8_quant_act(dev(x))
+    want_q, want_s = oracle.quant_act(x)
+    assert np.array_equal(host(s).view(np.uint32), want_s.view(np.uint32))
+    assert np.array_equal(host(xq), want_q)
+
+
+def _w4a8_run(awq, p, split_k=0, with_acc=True):
+    x = dev(p["x"])
+    xq, s = awq.w4a8_quant_act(x)
+    M, K = p["x"].shape
+    N = p["wq"].shape[1] * 8
+    acc = torch.empty((M, N), dtype=torch.int32, device="cuda") if with_acc else None
+    y = awq.w4a8_gemm(xq, s, dev(p["wq"]), dev(p["s_ch"]), split_k=split_k, acc_out=acc)
+    return host(xq), host(s), host(y), (host(acc) if with_acc else None)
+
+
+@pytest.mark.parametrize("split_k", [1, 2, 0])
+def test_w4a8_small_bitexact(awq, split_k):
+    p = synth.w4a8_problem(5, 1024, 288, seed=500 + split_k)
+    xq, s, y, acc = _w4a8_run(awq, p, split_k)
+    want_y, want_acc = oracle.w4a8_linear(xq, s, p["wq"], p["s_ch"])
+    assert np.array_equal(acc, want_acc)
+    assert np.array_equal(y.view(np.uint16), want_y.view(np.uint16))
+
+
+@pytest.mark.parametrize("M", [1, 16, 64, 256])
+def test_w4a8_config_sampled_bitexact(awq, M):
+    K, N = synth.W4A8_SHAPE
+    p = synth.w4a8_problem(M, K, N, seed=600 + M)
+    xq, s, y, acc = _w4a8_run(awq, p)
+    wc = sample_word_cols(N // 8, seed=M, count=12)
+    cols = (8 * wc[:, None] + np.arange(8)[None, :]).ravel()
+    want_y, want_acc = oracle.w4a8_linear(xq, s, p["wq"][:, wc], p["s_ch"][cols])
+    assert np.array_equal(acc[:, cols], want_acc)
+    assert np.array_equal(y[:, cols].view(np.uint16), want_y.view(np.uint16))
+
+
+def test_no_device_timeouts_recorded(awq):
+    torch.cuda.synchronize()
+    assert awq.awq_last_device_error() == 0
