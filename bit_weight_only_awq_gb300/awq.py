@@ -40,6 +40,7 @@ _SIGS = {
     "awq_workspace_bytes": (_sz, [_i32, _i64, _i64, _i64, _i32]),
     "awq_gemv": (_i32, [_p, _p, _p, _p, _p, _i64, _i64, _i64, _i32, _i32, _p, _sz, _p]),
     "awq_gemm": (_i32, [_p, _p, _p, _p, _p, _i64, _i64, _i64, _i32, _i32, _p, _sz, _p]),
+    "awq_gemv_noalloc": (_i32, [_p, _p, _p, _p, _p, _i64, _i64, _i64, _i32, _i32, _p]),
     "w4a8_quant_act": (_i32, [_p, _p, _p, _i64, _i64, _p]),
     "w4a8_gemm": (_i32, [_p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _i32, _p, _sz, _p]),
     "awq_last_device_error": (_i32, [ctypes.POINTER(_i32)]),
@@ -142,6 +143,21 @@ def _gemm_like(name, op, x, qweight, qzeros, scales, group_size, split_k, out, w
 def awq_gemv(x, qweight, qzeros, scales, group_size: int = GROUP_SIZE, split_k: int = 0, out=None,
              workspace=None, stream=None) -> torch.Tensor:
     return _gemm_like("awq_gemv", OP_GEMV, x, qweight, qzeros, scales, group_size, split_k, out, workspace, stream)
+
+
+def awq_gemv_noalloc(x, qweight, qzeros, scales, group_size: int = GROUP_SIZE, split_k: int = 0, out=None,
+                     stream=None) -> torch.Tensor:
+    """awq_gemv without a caller workspace: the library's fixed per-device scratch array is used.
+
+    The output tensor is the only memory this wrapper allocates (pass `out` to allocate nothing).
+    """
+    M, K = x.shape
+    N = qweight.shape[1] * 8
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    _check("awq_gemv_noalloc", lib.awq_gemv_noalloc(_ptr(x), _ptr(qweight), _ptr(qzeros), _ptr(scales), _ptr(out),
+                                                    M, K, N, group_size, split_k, _stream(stream)))
+    return out
 
 
 def awq_gemm(x, qweight, qzeros, scales, group_size: int = GROUP_SIZE, split_k: int = 0, out=None,

@@ -114,6 +114,29 @@ awq_status awq_gemv(const uint16_t *x, const int32_t *qweight, const int32_t *qz
                     size_t workspace_bytes, awq_stream_t stream);
 
 /*
+ * awq_gemv_noalloc -- awq_gemv for callers that cannot allocate device memory.
+ * The pages have no counterpart to this entry point; it exists for callers such as a
+ * plugin inside an inference runtime that owns all device memory and gives the plugin
+ * no allocator, or a serving loop that forbids allocation after start-up (cudaMalloc
+ * may synchronize the device).  Same arguments, results and checks as awq_gemv, minus
+ * the workspace: the split-K scratch lives in a fixed 8 MiB array inside the library
+ * on every GPU that loads it, held until the process exits.  The call allocates
+ * nothing (no cudaMalloc / cudaFree, no allocating library routine).
+ *  - The first call on each device resolves the array's device address
+ *    (cudaGetSymbolAddress with that device current); make that first call before
+ *    any stream capture.
+ *  - Automatic split (split_k = 0) shrinks the split until its scratch fits 8 MiB;
+ *    an explicit split_k whose scratch (64 KB of tickets + split * M * N * 4 bytes)
+ *    exceeds 8 MiB is rejected with AWQ_EWORKSPACE.
+ *  - Every call shares the array and clears the tickets it needs on `stream` before
+ *    its kernel; calls whose kernels overlap on the GPU (other streams, other host
+ *    threads) race on the array and must be serialized by the caller.
+ */
+awq_status awq_gemv_noalloc(const uint16_t *x, const int32_t *qweight, const int32_t *qzeros,
+                            const uint16_t *scales, uint16_t *y, int64_t M, int64_t K, int64_t N,
+                            int32_t group_size, int32_t split_k, awq_stream_t stream);
+
+/*
  * awq_gemm -- y = x * W on the tensor cores (tcgen05, fp16 x fp16 -> fp32 in
  * tensor memory) for any M >= 1 (intended for M > 8: prefill).
  * Same operands and layouts as awq_gemv; K % 128 == 0, N % 32 == 0,
