@@ -49,7 +49,8 @@ def build(verbose_ptxas: bool = False, force: bool = False) -> str:
     """Compile every translation unit and link libawq.so; returns the library path."""
     os.makedirs(BUILD_DIR, exist_ok=True)
     srcs_mtime = max(os.path.getmtime(os.path.join(CSRC, s)) for s in SOURCES)
-    hdrs = [os.path.join(CSRC, "awq_internal.h"), os.path.join(ROOT, "include", "awq.h")]
+    hdrs = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
+    hdrs.append(os.path.join(ROOT, "include", "awq.h"))
     srcs_mtime = max([srcs_mtime] + [os.path.getmtime(h) for h in hdrs])
     if not force and os.path.exists(LIB_PATH) and os.path.getmtime(LIB_PATH) >= srcs_mtime:
         return LIB_PATH

@@ -113,7 +113,7 @@ awq_status awq_dequant(const int32_t* qweight, const int32_t* qzeros, const uint
 }
 
 static bool gemv_shape_ok(int64_t M, int64_t K, int64_t N, int32_t group_size, int32_t split_k) {
-  return M >= 0 && M <= kGemvMaxM && K > 0 && K % kGroup == 0 && N > 0 && N % 16 == 0 && group_size == kGroup &&
+  return M >= 0 && M <= kGemvMaxM && K > 0 && K % kGroup == 0 && N > 0 && N % 32 == 0 && group_size == kGroup &&
          split_k >= 0 && K <= (int64_t)1 << 30 && N <= (int64_t)1 << 30;
 }
 static bool gemm_shape_ok(int64_t M, int64_t K, int64_t N, int32_t split_k) {

@@ -39,10 +39,24 @@ cudaError_t launch_dequant(const uint32_t* qw, const uint32_t* qz, const uint16_
                            int64_t N, int group, uint16_t* w, cudaStream_t s);
 
 // ---- decode GEMV (awq_gemv.cu)
+constexpr int kNumSMs = 152;  // GB300
+
+// Work partition of the decode GEMV: units are (128-column tile, 128-row group) pairs in
+// tile-major order; CTA p of P owns units [unit_begin(p), unit_begin(p + 1)).
+__host__ __device__ inline int64_t unit_begin(int64_t p, int64_t units, int64_t ctas) {
+  return p * units / ctas;
+}
+// The CTA whose range contains unit u.
+__host__ __device__ inline int64_t cta_of_unit(int64_t u, int64_t units, int64_t ctas) {
+  return ((u + 1) * ctas + units - 1) / units - 1;
+}
+
 struct GemvPlan {
-  int split;            // K slices (grid.y)
-  int groups_per_split; // 128-row groups per slice
-  int tiles;            // 128-column tiles (grid.x)
+  int tiles;   // 128-column tiles
+  int groups;  // 128-row groups (K / 128)
+  int ctas;    // grid size P
+  int maxc;    // most CTAs contributing to one tile (1 = no cross-CTA reduction)
+  int split;   // effective K split (ceil(ctas / tiles)), the knob callers pass as split_k
 };
 GemvPlan gemv_plan(int64_t M, int64_t K, int64_t N, int split_k);
 size_t gemv_workspace_bytes(const GemvPlan& p, int64_t M, int64_t N);

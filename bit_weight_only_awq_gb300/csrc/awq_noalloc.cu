@@ -52,7 +52,7 @@ using namespace awq;
 extern "C" awq_status awq_gemv_noalloc(const uint16_t* x, const int32_t* qweight, const int32_t* qzeros,
                                        const uint16_t* scales, uint16_t* y, int64_t M, int64_t K, int64_t N,
                                        int32_t group_size, int32_t split_k, awq_stream_t stream) {
-  if (M < 0 || M > kGemvMaxM || K <= 0 || K % kGroup != 0 || K > ((int64_t)1 << 30) || N <= 0 || N % 16 != 0 ||
+  if (M < 0 || M > kGemvMaxM || K <= 0 || K % kGroup != 0 || K > ((int64_t)1 << 30) || N <= 0 || N % 32 != 0 ||
       N > ((int64_t)1 << 30) || group_size != kGroup || split_k < 0)
     return AWQ_EINVAL;
   if (M == 0) return AWQ_OK;
@@ -78,7 +78,7 @@ extern "C" awq_status awq_gemv_noalloc(const uint16_t* x, const int32_t* qweight
   if (major != 10 || minor != 3) return AWQ_EARCH;
 
   void* scratch = nullptr;
-  if (plan.split > 1) {
+  if (gemv_workspace_bytes(plan, M, N) > 0) {
     scratch = scratch_address();
     if (!scratch) return AWQ_ECUDA;
     // The split-K tickets at the start of the array must read zero when the kernel starts; the

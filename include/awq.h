@@ -101,10 +101,12 @@ size_t awq_workspace_bytes(awq_op op, int64_t M, int64_t K, int64_t N, int32_t s
  * awq_gemv -- y = x * W for M <= 8 tokens (decode), W dequantized on the fly.
  * x fp16 [M, K]; qweight int32 [K, N/8]; qzeros int32 [K/128, N/8] or NULL
  * (symmetric, z = 8); scales fp16 [K/128, N]; y fp16 [M, N] (output).
- * 1 <= M <= 8, K % 128 == 0, N % 16 == 0, group_size == 128.
- * split_k: number of K slices reduced in fp32 (0 = automatic); the fp16
- * output is rounded once from the fp32 sum.  Needs a workspace when the
- * resolved split_k exceeds 1.
+ * 1 <= M <= 8 (0 = no-op), K % 128 == 0, N % 32 == 0, group_size == 128.
+ * split_k: number of K slices per 128-column tile, reduced in fp32 (0 =
+ * automatic: a persistent grid of two CTAs per SM, each owning an equal share
+ * of the (tile, 128-row group) units); the fp16 output is rounded once from
+ * the fp32 sum.  Needs a workspace when a tile is shared by several CTAs
+ * (awq_workspace_bytes() > 0).
  * Source: the M <= 8 branch of the dispatch snippet, gemv_forward_cuda(inputs,
  * qweight, scales, qzeros, group_size) ("Speed up AWQ 2.5x with updated kernel").
  */

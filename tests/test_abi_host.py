@@ -57,6 +57,7 @@ def test_gemv_rejects_bad_shapes_before_launch(awq):
     assert _gemv(awq, M=-1) == EINVAL
     assert _gemv(awq, K=100) == EINVAL
     assert _gemv(awq, N=24) == EINVAL
+    assert _gemv(awq, N=48) == EINVAL           # the TMA row stride needs N % 32 == 0
     assert _gemv(awq, g=64) == EINVAL
     assert _gemv(awq, split=-2) == EINVAL
 

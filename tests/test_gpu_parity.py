@@ -111,8 +111,8 @@ def test_gemv_tiny_config(awq):
 @pytest.mark.parametrize("split_k", [1, 3, 0])
 @pytest.mark.parametrize("M", [1, 2, 3, 5, 8])
 def test_gemv_small_ragged(awq, M, split_k, symmetric):
-    # N = 400: 50 packed words, 4 column tiles with a ragged last tile; K = 1280: 10 groups
-    p = synth.awq_problem(M, 1280, 400, seed=100 + M, symmetric=symmetric)
+    # N = 416: 52 packed words, 4 column tiles with a ragged last tile; K = 1280: 10 groups
+    p = synth.awq_problem(M, 1280, 416, seed=100 + M, symmetric=symmetric)
     y = run_w4a16(awq, awq.awq_gemv, p, split_k)
     ref = oracle.awq_linear(p["x"], p["qweight"], p["qzeros"], p["scales"], 128)
     assert_within_tol(y, ref, f"gemv M={M} split={split_k} sym={symmetric}")
