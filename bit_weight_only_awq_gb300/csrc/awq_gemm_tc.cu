@@ -53,7 +53,8 @@ struct Cfg {
   static constexpr int kFit = (227 * 1024 - 2048) / kStageBytes;
   static constexpr int kStages = BT >= 128 ? (kFit > 8 ? 8 : kFit) : 4;
   static constexpr int kSmem = kStages * kStageBytes + 1024 /*align slack*/ + 1024 /*barriers*/;
-  static constexpr int kTmemCols = BT < 32 ? 32 : BT;
+  static constexpr int kTmemCols1 = BT < 32 ? 32 : BT;  // one accumulator
+  static constexpr int kTmemCols2 = 2 * BT < 32 ? 32 : 2 * BT;  // two (W4A8: one per exact K chunk)
   // tcgen05 instruction descriptor, kind::f16: D f32, A/B f16, A MN-major, B K-major, M=128, N=BT
   static constexpr uint32_t kIdesc = (1u << 4) | (1u << 15) | ((uint32_t)(BT >> 3) << 17) |
                                      ((uint32_t)(kBN >> 4) << 24);
@@ -120,8 +121,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_s,
             __half* __restrict__ y, int32_t* __restrict__ acc_out, const float* __restrict__ s_tok,
             const __half* __restrict__ s_ch, void* __restrict__ part, int* __restrict__ counters,
-            int* __restrict__ err, int M, int N, int K, int ksteps_per_split) {
+            int* __restrict__ err, int M, int N, int K, int ksteps_per_split, int chunk_steps) {
   using C = Cfg<BT>;
+  // W4A8 keeps one TMEM accumulator per chunk of at most chunk_steps k-steps (16384 rows), each an
+  // exact integer in fp32; W4A16 uses one accumulator for its whole K slice.
+  constexpr int kTmemCols = MODE == kModeW4A8 ? C::kTmemCols2 : C::kTmemCols1;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
@@ -159,7 +163,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                 "r"((uint32_t)C::kTmemCols)
+                 "r"((uint32_t)kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -217,7 +221,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
           const uint64_t ad = smem_desc_sw128(ws + kk * 2 * 2048, 1024, 2048);
           // B: activations, K-major; 16 k = 32 B inside the 128-byte swizzle row, 8-row groups 1024 B apart
           const uint64_t bd = smem_desc_sw128(xs + kk * 32, 16, 1024);
-          mma_f16(tmem, ad, bd, C::kIdesc, (it > 0 || kk > 0) ? 1u : 0u);
+          const int chunk = MODE == kModeW4A8 ? it / chunk_steps : 0;
+          const int within = MODE == kModeW4A8 ? it - chunk * chunk_steps : it;
+          mma_f16(tmem + (uint32_t)(chunk * BT), ad, bd, C::kIdesc, (within > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(empty_bar(st));
       }
@@ -260,7 +266,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                                      : hmul2(hsub2(h, zp[j]), sp[j]);
         }
         const uint32_t off = (uint32_t)((r >> 3) * 2048 + (c >> 3) * 1024 + (r & 7) * 128 + (((c & 7) ^ (r & 7)) << 4));
-        *reinterpret_cast<uint4*>(wt + off) = make_uint4(o[0], o[1], o[2], o[3]);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(smem_u32(wt + off)), "r"(o[0]), "r"(o[1]),
+                     "r"(o[2]), "r"(o[3])
+                     : "memory");
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
@@ -284,13 +292,24 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
       for (int cb = half * kHalf; cb < (half + 1) * kHalf; cb += 8) {
         float v[8];
         tmem_ld8(tmem + ((uint32_t)(lq * 32) << 16) + (uint32_t)cb, v);
+        int vi[8];
+        if (MODE == kModeW4A8) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) vi[j] = __float2int_rn(v[j]);  // exact integers
+          if (nsteps > chunk_steps) {
+            float v2[8];
+            tmem_ld8(tmem + ((uint32_t)(lq * 32) << 16) + (uint32_t)(BT + cb), v2);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) vi[j] += __float2int_rn(v2[j]);
+          }
+        }
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const int m = m0 + cb + j;
           if (!n_ok || m >= M) continue;
           const size_t o = (size_t)m * N + n;
           if (MODE == kModeW4A8) {
-            const int a = __float2int_rn(v[j]);  // exact integer
+            const int a = vi[j];
             if (split == 1) {
               if (acc_out) acc_out[o] = a;
               y[o] = __float2half_rn(__fmul_rn(__fmul_rn((float)a, s_tok[m]), sch));
@@ -338,7 +357,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"((uint32_t)C::kTmemCols)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"((uint32_t)kTmemCols)
                  : "memory");
   }
 }
@@ -396,7 +415,7 @@ cudaError_t launch_t(const uint16_t* x16, const uint32_t* qw, const uint32_t* qz
   dim3 grid(p.n_tiles, p.m_tiles, p.split);
   kern<<<grid, kThreads, C::kSmem, s>>>(tx, tq, tz, ts, reinterpret_cast<__half*>(y), acc_out, s_tok,
                                        reinterpret_cast<const __half*>(s_ch), part, counters, err, (int)M,
-                                       (int)N, (int)K, p.ksteps);
+                                       (int)N, (int)K, p.ksteps, kW4A8MaxKSlice / kBK);
   return cudaGetLastError();
 }
 
@@ -422,6 +441,11 @@ GemmPlan gemm_plan(int64_t M, int64_t K, int64_t N, int split_k, int mode) {
   p.bt = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
   p.n_tiles = (int)((N + kBN - 1) / kBN);
   p.m_tiles = (int)((M + p.bt - 1) / p.bt);
+  // under one wave of 152 SMs: narrower token tiles (down to 64) before splitting K
+  while (p.bt > 64 && (int64_t)p.n_tiles * p.m_tiles < 114) {
+    p.bt /= 2;
+    p.m_tiles = (int)((M + p.bt - 1) / p.bt);
+  }
   const int total = (int)(K / kBK);
   int split = split_k;
   if (split <= 0) {
@@ -434,7 +458,8 @@ GemmPlan gemm_plan(int64_t M, int64_t K, int64_t N, int split_k, int mode) {
         if (tiles * sp <= 152 && total / sp >= 8) split = sp;
   }
   if (mode == kModeW4A8) {
-    const int min_split = (int)((K + kW4A8MaxKSlice - 1) / kW4A8MaxKSlice);
+    // two exact accumulators per CTA: each K slice spans at most 2 x 16384 rows
+    const int min_split = (int)((K + 2 * kW4A8MaxKSlice - 1) / (2 * kW4A8MaxKSlice));
     if (split < min_split) split = min_split;
   }
   if (split > total) split = total;

@@ -175,8 +175,10 @@ awq_status w4a8_quant_act(const uint16_t *x, int8_t *xq, float *s_tok, int64_t M
  * s_tok[m]) * fp32(s_ch[n])).  K % 128 == 0, N % 32 == 0.
  * Always needs a workspace (it holds an fp16 copy of xq for the fp16 tensor
  * path; every int8 and int4 value and every product is exact in fp16/fp32).
- * split_k: K slices reduced in int32 (0 = automatic; each slice spans at most
- * 16384 inputs so its fp32 tensor-core sum stays an exact integer).
+ * split_k: K slices reduced in int32 across CTAs (0 = automatic).  Inside a
+ * CTA every 16384 inputs get their own fp32 tensor-memory accumulator (two at
+ * most), so each fp32 sum is an exact integer; K beyond 32768 per slice is
+ * split across CTAs.
  * Source: "Support W4A8 quantization for vllm": marlin_qqq_gemm(a, b_q_weight,
  * s1, s2, s3, workspace, size_m, size_n, size_k) in tlrmchlsmth's review;
  * HandH1998's per-channel dequantization (int4 to int8, channel scale on the

@@ -103,12 +103,13 @@ def test_workspace_layout(awq):
     # GEMV: counters block + split x M x N fp32 partials (256-byte rounded)
     assert awq.awq_workspace_bytes(awq.OP_GEMV, 8, 4096, 4096, 1) == 0
     assert awq.awq_workspace_bytes(awq.OP_GEMV, 8, 4096, 4096, 4) == counters + 4 * 8 * 4096 * 4
-    # W4A8 at K = 21760 must split K into slices of at most 16384 rows: at least 2 slices
-    ws = awq.awq_workspace_bytes(awq.OP_W4A8_GEMM, 4096, 21760, 8192, 0)
+    # W4A8 at K = 21760: two exact accumulators per CTA (16384 rows each) cover K without a split
     x16 = 4096 * 21760 * 2
-    assert ws >= counters + x16 + 2 * 4096 * 8192 * 4
-    # a forced single slice is raised to the minimum
-    assert awq.awq_workspace_bytes(awq.OP_W4A8_GEMM, 16, 21760, 8192, 1) == counters + 16 * 21760 * 2 + 2 * 16 * 8192 * 4
+    assert awq.awq_workspace_bytes(awq.OP_W4A8_GEMM, 4096, 21760, 8192, 0) == counters + x16
+    assert awq.awq_workspace_bytes(awq.OP_W4A8_GEMM, 16, 21760, 8192, 1) == counters + 16 * 21760 * 2
+    # K beyond 2 x 16384 rows forces a K split across CTAs with int32 partials
+    assert awq.awq_workspace_bytes(awq.OP_W4A8_GEMM, 4096, 40960, 8192, 1) == \
+        counters + 4096 * 40960 * 2 + 2 * 4096 * 8192 * 4
     # small-K W4A8 without split still needs the fp16 copy of the codes
     assert awq.awq_workspace_bytes(awq.OP_W4A8_GEMM, 4096, 4096, 8192, 1) == counters + 4096 * 4096 * 2
     # invalid shapes need nothing (the compute call reports the error)
