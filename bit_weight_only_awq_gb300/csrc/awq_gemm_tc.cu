@@ -14,12 +14,20 @@
 //    each word into 8 fp16 values with shifts, one LOP3 per pair (fp16 magic 0x6400),
 //    HSUB2 of the zero and HMUL2 of the scale, and store them straight into the
 //    128-byte-swizzled MN-major layout; no transposition is needed.
-//  * TMA brings, per 64-row k-step: the activation tile (K-major, 128-byte swizzle),
-//    the packed weight tile, and the zero-point / scale rows of the step's group.
-//  * Warp roles: warp 0 issues TMA, warp 1 owns tensor memory and issues tcgen05.mma
-//    (one thread), warps 2..9 dequantize and then run the epilogue (tcgen05.ld ->
-//    fp16 / int32 -> global).  Stages are chained by mbarriers; every wait is bounded
-//    in time and records an error id instead of hanging.
+//  * Three shared-memory rings per 64-row k-step, each sized for its own lifetime:
+//    packed weights with the group's zero-point / scale rows (TMA, 8 deep, 4.4 KB each:
+//    consumed by the dequant warps, so it can run far ahead of DRAM latency), the
+//    dequantized fp16 weight tile (3 deep, written by the dequant warps, read by the
+//    MMA), and the activation tile (TMA, K-major 128-byte swizzle, as deep as shared
+//    memory allows; its slot is held only from the copy to the MMA that reads it).
+//    Measured on GB300: with one ring for everything, a slot stayed busy from the copy
+//    through dequantization to the MMA (~1.7 us) and four slots capped the tensor
+//    pipe at ~45 %.
+//  * Warp roles: warp 0 copies activations, warp 2 copies packed weights (TMA), warp 1
+//    owns tensor memory and issues tcgen05.mma (one thread), warps 3..18 dequantize in
+//    two groups of eight that take alternate k-steps, and the first group then runs the
+//    epilogue (tcgen05.ld -> fp16 / int32 -> global).  Rings are chained by mbarriers;
+//    every wait is bounded in time and records an error id instead of hanging.
 //  * split > 1: each K slice writes fp32 (W4A16) or int32 (W4A8) partials; the last
 //    CTA of an output tile (atomic ticket) sums them in slice order.
 //  * W4A8: int8 activations (converted once to fp16, exact) times int4 weights
@@ -38,26 +46,32 @@ namespace {
 constexpr int kBK = 64;          // input rows per k-step
 constexpr int kBN = 128;         // weight columns per CTA (MMA M)
 constexpr int kQWords = kBN / 8; // packed words per row of a stage
-constexpr int kDqWarps = 8;
-constexpr int kThreads = (2 + kDqWarps) * 32;
+constexpr int kDqGroupWarps = 8;              // one group dequantizes one stage (256 threads)
+constexpr int kDqGroups = 2;                  // groups alternate stages to overlap their latency
+constexpr int kDqWarps = kDqGroupWarps * kDqGroups;
+constexpr int kThreads = (3 + kDqWarps) * 32;   // x producer, MMA, q producer, dequant
 constexpr int kWBytes = kBK * kBN * 2;     // dequantized tile, 16 KB
 constexpr int kQBytes = kBK * kQWords * 4; // packed tile, 4 KB
 constexpr int kZBytes = kQWords * 4;       // one zero-point row, 64 B
 constexpr int kSBytes = kBN * 2;           // one scale row, 256 B
+constexpr int kQStage = kQBytes + 128 + kSBytes;  // packed tile | zero row (padded) | scale row
+constexpr int kQStages = 8;
+constexpr int kWStages = 3;
 
 template <int BT>
 struct Cfg {
   static constexpr int kXBytes = BT * kBK * 2;
-  static constexpr int kStageRaw = kXBytes + kWBytes + kQBytes + 128 + kSBytes;
-  static constexpr int kStageBytes = (kStageRaw + 1023) / 1024 * 1024;
-  static constexpr int kFit = (227 * 1024 - 2048) / kStageBytes;
-  static constexpr int kStages = BT >= 128 ? (kFit > 8 ? 8 : kFit) : 4;
-  static constexpr int kSmem = kStages * kStageBytes + 1024 /*align slack*/ + 1024 /*barriers*/;
+  static constexpr int kFixed = kWStages * kWBytes + kQStages * kQStage + 2048;
+  static constexpr int kFit = (227 * 1024 - kFixed) / kXBytes;
+  static constexpr int kXStages = kFit > 8 ? 8 : kFit;
+  static constexpr int kSmem = kXStages * kXBytes + kFixed + 1024;
   static constexpr int kTmemCols1 = BT < 32 ? 32 : BT;  // one accumulator
   static constexpr int kTmemCols2 = 2 * BT < 32 ? 32 : 2 * BT;  // two (W4A8: one per exact K chunk)
   // tcgen05 instruction descriptor, kind::f16: D f32, A/B f16, A MN-major, B K-major, M=128, N=BT
   static constexpr uint32_t kIdesc = (1u << 4) | (1u << 15) | ((uint32_t)(BT >> 3) << 17) |
                                      ((uint32_t)(kBN >> 4) << 24);
+  static_assert(kXStages >= 2, "activation ring");
+  static_assert(kSmem <= 227 * 1024, "shared memory budget");
 };
 
 // ------------------------------------------------------------------ descriptors and tcgen05
@@ -126,11 +140,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
   // W4A8 keeps one TMEM accumulator per chunk of at most chunk_steps k-steps (16384 rows), each an
   // exact integer in fp32; W4A16 uses one accumulator for its whole K slice.
   constexpr int kTmemCols = MODE == kModeW4A8 ? C::kTmemCols2 : C::kTmemCols1;
+  constexpr int SX = C::kXStages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
-  // bars: full[S], wready[S], empty[S], accf
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * C::kStages + 1);
+  uint8_t* xring = smem;                                   // SX x BT*64 fp16 (1024-aligned slots)
+  uint8_t* wring = xring + SX * C::kXBytes;                // kWStages x 16 KB (1024-aligned)
+  uint8_t* qring = wring + kWStages * kWBytes;             // kQStages x kQStage (128-aligned)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(qring + kQStages * kQStage);
+  // bars: fullx[SX] emptyx[SX] fullq[Q] emptyq[Q] wready[W] wempty[W] accf
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * SX + 2 * kQStages + 2 * kWStages + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* last_flag = reinterpret_cast<int*>(tmem_slot + 2);
 
@@ -142,18 +160,26 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
   const int step0 = blockIdx.z * ksteps_per_split;
   const int nsteps = min(ksteps_per_split, total_steps - step0);
 
-  auto full_bar = [&](int s) { return smem_u32(bars + s); };
-  auto wready_bar = [&](int s) { return smem_u32(bars + C::kStages + s); };
-  auto empty_bar = [&](int s) { return smem_u32(bars + 2 * C::kStages + s); };
-  const uint32_t accf_bar = smem_u32(bars + 3 * C::kStages);
-  auto stage_base = [&](int s) { return smem + s * C::kStageBytes; };
-  // stage layout: X (BT x 64 fp16, SW128) | W (64 x 128 fp16, MN-major SW128) | Q | Z | S
+  auto fullx = [&](int s) { return smem_u32(bars + s); };
+  auto emptyx = [&](int s) { return smem_u32(bars + SX + s); };
+  auto fullq = [&](int s) { return smem_u32(bars + 2 * SX + s); };
+  auto emptyq = [&](int s) { return smem_u32(bars + 2 * SX + kQStages + s); };
+  auto wready = [&](int s) { return smem_u32(bars + 2 * SX + 2 * kQStages + s); };
+  auto wempty = [&](int s) { return smem_u32(bars + 2 * SX + 2 * kQStages + kWStages + s); };
+  const uint32_t accf_bar = smem_u32(bars + 2 * SX + 2 * kQStages + 2 * kWStages);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(full_bar(s), 1);
-      mbar_init(wready_bar(s), kDqWarps);
-      mbar_init(empty_bar(s), 1);
+    for (int s = 0; s < SX; ++s) {
+      mbar_init(fullx(s), 1);
+      mbar_init(emptyx(s), 1);
+    }
+    for (int s = 0; s < kQStages; ++s) {
+      mbar_init(fullq(s), 1);
+      mbar_init(emptyq(s), kDqGroupWarps);
+    }
+    for (int s = 0; s < kWStages; ++s) {
+      mbar_init(wready(s), kDqGroupWarps);
+      mbar_init(wempty(s), 1);
     }
     mbar_init(accf_bar, 1);
     *abort_flag = 0;
@@ -172,96 +198,100 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    // ------------------------------------------------ TMA producer
+  if (warp == 0 || warp == 2) {
+    // ------------------------------------------------ TMA producers: activations (warp 0), weights (warp 2)
     if (lane == 0) {
-      const uint32_t tx = C::kXBytes + kQBytes + (MODE == kModeZeroPoint ? kZBytes : 0) +
-                          (MODE != kModeW4A8 ? kSBytes : 0);
-      int last_it[8];
-      for (int s = 0; s < 8; ++s) last_it[s] = -1;
-      for (int it = 0; it < nsteps; ++it) {
-        const int st = it % C::kStages;
-        const uint32_t ph = (uint32_t)(it / C::kStages) & 1u;
-        if (!wait_bounded(empty_bar(st), ph ^ 1u, abort_flag, err, 101)) break;
+      const bool is_x = warp == 0;
+      const int S = is_x ? SX : kQStages;
+      const uint32_t tx = is_x ? (uint32_t)C::kXBytes
+                               : (uint32_t)(kQBytes + (MODE == kModeZeroPoint ? kZBytes : 0) +
+                                            (MODE != kModeW4A8 ? kSBytes : 0));
+      int issued = 0;
+      for (int it = 0; it < nsteps; ++it, ++issued) {
+        const int st = it % S;
+        const uint32_t ph = (uint32_t)(it / S) & 1u;
+        if (!wait_bounded(is_x ? emptyx(st) : emptyq(st), ph ^ 1u, abort_flag, err, is_x ? 101 : 102)) break;
         const int kb = (step0 + it) * kBK;
-        const int grp = kb / kGroup;
-        uint8_t* sb = stage_base(st);
-        mbar_arrive_tx(full_bar(st), tx);
-        tma_load_2d(smem_u32(sb), &tm_x, kb, m0, full_bar(st));
-        tma_load_2d(smem_u32(sb + C::kXBytes + kWBytes), &tm_q, n0 / 8, kb, full_bar(st));
-        if (MODE == kModeZeroPoint)
-          tma_load_2d(smem_u32(sb + C::kXBytes + kWBytes + kQBytes), &tm_z, n0 / 8, grp, full_bar(st));
-        if (MODE != kModeW4A8)
-          tma_load_2d(smem_u32(sb + C::kXBytes + kWBytes + kQBytes + 128), &tm_s, n0, grp, full_bar(st));
-        last_it[st] = it;
+        if (is_x) {
+          mbar_arrive_tx(fullx(st), tx);
+          tma_load_2d(smem_u32(xring + st * C::kXBytes), &tm_x, kb, m0, fullx(st));
+        } else {
+          const int grp = kb / kGroup;
+          uint8_t* qb = qring + st * kQStage;
+          mbar_arrive_tx(fullq(st), tx);
+          tma_load_2d(smem_u32(qb), &tm_q, n0 / 8, kb, fullq(st));
+          if (MODE == kModeZeroPoint) tma_load_2d(smem_u32(qb + kQBytes), &tm_z, n0 / 8, grp, fullq(st));
+          if (MODE != kModeW4A8) tma_load_2d(smem_u32(qb + kQBytes + 128), &tm_s, n0, grp, fullq(st));
+        }
       }
       // never leave the CTA with copies in flight
-      for (int s = 0; s < C::kStages; ++s)
-        if (last_it[s] >= 0) {
-          volatile int no_abort = 0;
-          wait_bounded(full_bar(s), (uint32_t)(last_it[s] / C::kStages) & 1u, &no_abort, err, 102);
-        }
+      volatile int no_abort = 0;
+      for (int j = issued - S < 0 ? 0 : issued - S; j < issued; ++j)
+        wait_bounded(is_x ? fullx(j % S) : fullq(j % S), (uint32_t)(j / S) & 1u, &no_abort, err, 103);
     }
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer
     if (lane == 0) {
       bool ok = true;
       for (int it = 0; it < nsteps && ok; ++it) {
-        const int st = it % C::kStages;
-        const uint32_t ph = (uint32_t)(it / C::kStages) & 1u;
-        ok = wait_bounded(full_bar(st), ph, abort_flag, err, 201) &&
-             wait_bounded(wready_bar(st), ph, abort_flag, err, 202);
+        const int xs = it % SX, ws = it % kWStages;
+        ok = wait_bounded(fullx(xs), (uint32_t)(it / SX) & 1u, abort_flag, err, 201) &&
+             wait_bounded(wready(ws), (uint32_t)(it / kWStages) & 1u, abort_flag, err, 202);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t xs = smem_u32(stage_base(st));
-        const uint32_t ws = xs + C::kXBytes;
+        const uint32_t xa = smem_u32(xring + xs * C::kXBytes);
+        const uint32_t wa = smem_u32(wring + ws * kWBytes);
+        const int chunk = MODE == kModeW4A8 ? it / chunk_steps : 0;
+        const int within = MODE == kModeW4A8 ? it - chunk * chunk_steps : it;
 #pragma unroll
         for (int kk = 0; kk < kBK / 16; ++kk) {
           // A: weights, MN-major; 64-column atoms 1024 B apart (LBO), 8-row k groups 2048 B apart (SBO)
-          const uint64_t ad = smem_desc_sw128(ws + kk * 2 * 2048, 1024, 2048);
+          const uint64_t ad = smem_desc_sw128(wa + kk * 2 * 2048, 1024, 2048);
           // B: activations, K-major; 16 k = 32 B inside the 128-byte swizzle row, 8-row groups 1024 B apart
-          const uint64_t bd = smem_desc_sw128(xs + kk * 32, 16, 1024);
-          const int chunk = MODE == kModeW4A8 ? it / chunk_steps : 0;
-          const int within = MODE == kModeW4A8 ? it - chunk * chunk_steps : it;
+          const uint64_t bd = smem_desc_sw128(xa + kk * 32, 16, 1024);
           mma_f16(tmem + (uint32_t)(chunk * BT), ad, bd, C::kIdesc, (within > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(empty_bar(st));
+        mma_commit(emptyx(xs));  // both arrive once these mmas have read their operands
+        mma_commit(wempty(ws));
       }
       mma_commit(accf_bar);  // arrives once every issued mma has completed
       volatile int no_abort = 0;
       wait_bounded(accf_bar, 0, &no_abort, err, 203);
     }
   } else {
-    // ------------------------------------------------ dequant warps
-    const int d = threadIdx.x - 64;  // 0..255
+    // ------------------------------------------------ dequant warps (two groups, alternate k-steps)
+    const int group = (threadIdx.x - 96) / (kDqGroupWarps * 32);
+    const int d = (threadIdx.x - 96) % (kDqGroupWarps * 32);  // 0..255 within the group
     const int c = d & 15;            // packed word column within the tile
     const int r0 = d >> 4;           // first of the thread's 4 rows (r0 + 16 j)
-    for (int it = 0; it < nsteps; ++it) {
-      const int st = it % C::kStages;
-      const uint32_t ph = (uint32_t)(it / C::kStages) & 1u;
-      if (!wait_bounded(full_bar(st), ph, abort_flag, err, 301)) break;
-      if (!wait_bounded(empty_bar(st), ph ^ 1u, abort_flag, err, 302)) break;
-      uint8_t* sb = stage_base(st);
-      const uint32_t* qs = reinterpret_cast<const uint32_t*>(sb + C::kXBytes + kWBytes);
-      uint8_t* wt = sb + C::kXBytes;
+    for (int it = group; it < nsteps; it += kDqGroups) {
+      const int qs = it % kQStages, ws = it % kWStages;
+      if (!wait_bounded(fullq(qs), (uint32_t)(it / kQStages) & 1u, abort_flag, err, 301)) break;
+      if (!wait_bounded(wempty(ws), ((uint32_t)(it / kWStages) & 1u) ^ 1u, abort_flag, err, 302)) break;
+      const uint8_t* qb = qring + qs * kQStage;
+      const uint32_t* qw = reinterpret_cast<const uint32_t*>(qb);
+      uint8_t* wt = wring + ws * kWBytes;
       uint32_t zp[4], sp[4];
       if (MODE != kModeW4A8) {
-        const uint32_t zword =
-            MODE == kModeZeroPoint ? reinterpret_cast<const uint32_t*>(sb + C::kXBytes + kWBytes + kQBytes)[c]
-                                   : 0x88888888u;
-        const uint4 sv = reinterpret_cast<const uint4*>(sb + C::kXBytes + kWBytes + kQBytes + 128)[c];
+        const uint32_t zword = MODE == kModeZeroPoint ? reinterpret_cast<const uint32_t*>(qb + kQBytes)[c]
+                                                      : 0x88888888u;
+        const uint4 sv = reinterpret_cast<const uint4*>(qb + kQBytes + 128)[c];
         sp[0] = sv.x; sp[1] = sv.y; sp[2] = sv.z; sp[3] = sv.w;
 #pragma unroll
         for (int j = 0; j < 4; ++j) zp[j] = pair_magic(zword, j);
       }
+      uint32_t words[4];
+#pragma unroll
+      for (int jr = 0; jr < 4; ++jr) words[jr] = qw[(r0 + 16 * jr) * kQWords + c];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(emptyq(qs));  // packed words are in registers: the slot can refill
 #pragma unroll
       for (int jr = 0; jr < 4; ++jr) {
         const int r = r0 + 16 * jr;
-        const uint32_t w = qs[r * kQWords + c];
         uint32_t o[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const uint32_t h = pair_magic(w, j);
+          const uint32_t h = pair_magic(words[jr], j);
           o[j] = (MODE == kModeW4A8) ? hsub2(h, 0x64086408u) /* u - 8, exact */
                                      : hmul2(hsub2(h, zp[j]), sp[j]);
         }
@@ -272,14 +302,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
-      if (lane == 0) mbar_arrive(wready_bar(st));
+      if (lane == 0) mbar_arrive(wready(ws));
     }
 
-    // ------------------------------------------------ epilogue (same 8 warps)
+    // ------------------------------------------------ epilogue (first dequant group)
+    if (group == 0) {
     const bool have = wait_bounded(accf_bar, 0, abort_flag, err, 401);
     tc_fence_after();
     const int lq = warp & 3;                 // TMEM lane quarter this warp may access
-    const int half = (warp - 2) >> 2;        // which half of the BT token columns
+    const int half = (warp - 3) >> 2;        // which half of the BT token columns
     const int nl = lq * 32 + lane;           // TMEM lane = weight column in the tile
     const int n = n0 + nl;
     const bool n_ok = n < N;
@@ -325,12 +356,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     }
     if (split > 1) {
       __threadfence();
-      asm volatile("bar.sync 1, %0;" ::"r"(kDqWarps * 32) : "memory");
+      asm volatile("bar.sync 1, %0;" ::"r"(kDqGroupWarps * 32) : "memory");
       if (d == 0) {
         const int ctr = blockIdx.y * gridDim.x + blockIdx.x;
         *last_flag = (atomicAdd(counters + ctr, 1) == split - 1);
       }
-      asm volatile("bar.sync 1, %0;" ::"r"(kDqWarps * 32) : "memory");
+      asm volatile("bar.sync 1, %0;" ::"r"(kDqGroupWarps * 32) : "memory");
       if (*last_flag) {
         __threadfence();
         for (int cb = half * kHalf; cb < (half + 1) * kHalf; ++cb) {
@@ -352,7 +383,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
       }
     }
   }
-
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
