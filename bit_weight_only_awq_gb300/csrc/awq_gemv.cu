@@ -4,24 +4,28 @@
 // gemv_forward_cuda(inputs, qweight, scales, qzeros, group_size) ("Speed up AWQ
 // 2.5x with updated kernel").  The kernel design is this library's own:
 //
-//  * HBM-bound: every packed word is read exactly once.  Measured on GB300, a TMA
-//    stream only approaches the copy bandwidth with 256-byte-or-longer runs per row and
-//    ~200 KB in flight per SM (loaded DRAM latency is several microseconds), and a decode
-//    GEMV of a 7B-model layer moves only 8-47 MB, so per-call latency (first bytes, the
-//    cross-CTA reduction, the launch) matters as much as the streaming rate.  The kernel
-//    therefore uses at most half of an SM: one persistent CTA per SM per call, a
-//    producer warp streaming 16 KB stages (64 rows x 512 columns of packed words as two
-//    128-byte-swizzled TMA boxes, plus the group's zero-point / scale rows and the 64
-//    activations of every token) through a 5-deep ring, and 8 consumer warps (one
-//    64-column slice each) that copy their share of a stage into registers and release
-//    the slot at once.  The other half of every SM takes the next call's CTA, which
-//    programmatic dependent launch starts early: it streams its weights while this call
-//    finishes, so consecutive calls overlap their latencies.
+//  * HBM-bound: every packed word is read exactly once.  Measured on GB300 with this
+//    kernel's access pattern (512-column tiles walked down K, 256-byte runs per row), a
+//    TMA stream reaches ~6.1 TB/s with 32 KB stages but only ~5.4 TB/s with 16 KB ones,
+//    whatever the ring depth; and a decode GEMV of a 7B-model layer moves only 8-47 MB,
+//    so per-call latency (first bytes, the cross-CTA reduction, the launch) matters as
+//    much as the streaming rate.  The kernel therefore uses at most half of an SM: one
+//    persistent CTA per SM per call, a producer warp streaming 36 KB stages (one whole
+//    quantization group: 128 rows x 512 columns of packed words as four
+//    128-byte-swizzled TMA boxes, the group's zero-point / scale rows and the 128
+//    activations of every token) through a 3-deep ring, and 8 consumer warps (one
+//    64-column slice each) that copy their share of a stage into registers 64 rows at a
+//    time and release the slot after the last copy.  The other half of every SM takes the
+//    next call's CTA, which programmatic dependent launch starts early: it streams its
+//    weights while this call finishes, so consecutive calls overlap their latencies.
 //  * Persistent, evenly balanced grid: the (512-column tile, 64-row block) units are cut
-//    into equal contiguous ranges, one per SM.  A tile finished by one CTA is written
-//    directly; a tile shared by several CTAs leaves one fp32 partial per CTA in the
-//    workspace and the last of them (atomic ticket) sums the partials in contributor
-//    order and rounds once to fp16, so results are bit-reproducible.
+//    into equal contiguous ranges, one per SM; a CTA's units are grouped into stages of
+//    one quantization group (or a lone 64-row block at a range edge).  A tile finished by
+//    one CTA is written directly; a tile shared by several CTAs leaves one fp32 partial per
+//    CTA in the workspace.  The tickets are taken only after the CTA's last unit, so no
+//    CTA stalls mid-range on a fence; the last contributor of a tile (atomic ticket) sums
+//    the partials in contributor order and rounds once to fp16, so results are
+//    bit-reproducible.
 //  * Programmatic dependent launch: the GEMV starts streaming its weights before waiting
 //    for the previous kernel, and touches activations, outputs and the workspace only
 //    after that wait.
@@ -49,14 +53,18 @@ namespace {
 constexpr int kConsumers = 8;                  // consumer warps, one 64-column slice of the tile each
 constexpr int kThreads = (kConsumers + 1) * 32;
 constexpr int kCtasPerSm = 2;                  // this call's CTA and the next call's
-constexpr int kStages = 5;
-constexpr int kRows = 64;                      // rows per stage (half a quantization group)
+constexpr int kStages = 3;
+constexpr int kRows = 64;                      // rows per unit (a TMA box, half a quantization group)
 constexpr int kTileWords = 64;                 // packed words per tile row = 512 output columns
 constexpr int kTileCols = kTileWords * 8;
 constexpr int kBoxWords = 32;                  // one 128-byte-swizzled TMA box is 32 words wide
 constexpr int kBoxBytes = kRows * kBoxWords * 4;   // 8 KB
-constexpr int kQBytes = kRows * kTileWords * 4;    // 16 KB (two boxes)
-constexpr int kXBytes = kGemvMaxM * kRows * 2;     // 1 KB (one 128B-swizzled box, 8 tokens x 64)
+constexpr int kUnitsPerStage = 2;              // 64-row units per stage: 2 = one quantization group
+constexpr int kUnitQBytes = kRows * kTileWords * 4;  // 16 KB of packed words per unit
+constexpr int kColStride = kUnitsPerStage * kBoxBytes;  // box (column half c, unit h) at c * kColStride + h * 8 KB
+constexpr int kQBytes = kUnitsPerStage * kUnitQBytes;
+constexpr int kXBoxBytes = kGemvMaxM * kRows * 2;  // 1 KB (one 128B-swizzled box, 8 tokens x 64)
+constexpr int kXBytes = kUnitsPerStage * kXBoxBytes;
 constexpr int kZBytes = kTileWords * 4;            // 256 B
 constexpr int kSBytes = kTileCols * 2;             // 1 KB
 constexpr int kXOff = kQBytes;
@@ -64,7 +72,7 @@ constexpr int kZOff = kXOff + kXBytes;
 constexpr int kSOff = kZOff + kZBytes;
 constexpr int kStageBytes = ((kSOff + kSBytes) + 1023) / 1024 * 1024;
 constexpr int kSmemBytes = kStages * kStageBytes + 256 + 1024;
-static_assert(kSmemBytes * kCtasPerSm <= 227 * 1024, "shared memory budget: two CTAs per SM");
+static_assert(kSmemBytes * kCtasPerSm <= 227 * 1024 - 2048, "shared memory budget: two CTAs per SM");
 static_assert(kTileWords == kConsumers * 8, "one 8-word slice per consumer warp");
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
@@ -113,10 +121,10 @@ __device__ __forceinline__ void consumers_sync() {  // the consumer warps only (
   asm volatile("bar.sync 1, %0;" ::"r"(kConsumers * 32) : "memory");
 }
 
-// 32-bit word `word` (0..63) of packed row `row` in the stage tile: two 128-byte-swizzled
-// boxes of 32 words x 64 rows.
+// 32-bit word `word` (0..63) of packed row `row` (0..127) in the stage tile: 128-byte-swizzled
+// boxes of 32 words x 64 rows, column half c = word / 32 at c * 16 KB, rows 64..127 8 KB further.
 __device__ __forceinline__ uint32_t q_offset(int row, int word) {
-  return (uint32_t)((word >> 5) * kBoxBytes + row * 128 + (((((word & 31) >> 2) ^ (row & 7))) << 4) +
+  return (uint32_t)((word >> 5) * kColStride + row * 128 + (((((word & 31) >> 2) ^ (row & 7))) << 4) +
                     (word & 3) * 4);
 }
 // Activation pair (k, k+1), k even (0..62), of token g in the 128-byte-swizzled 1 KB box.
@@ -145,16 +153,13 @@ __device__ __forceinline__ LaneOffsets lane_offsets(int word, int g, int t) {
 struct StageRegs {
   uint32_t r[4][4];  // [16-row step][rows 2t, 2t+1, 2t+8, 2t+9]
   uint32_t b[4][2];  // [16-row step][activation pairs k = 2t, 2t+8]
-  uint32_t zword;
-  uint4 sv;
 };
 
-__device__ __forceinline__ void load_stage(const uint8_t* sb, bool has_z, int word, const LaneOffsets& lo,
-                                           StageRegs& sr) {
-  sr.zword = has_z ? reinterpret_cast<const uint32_t*>(sb + kZOff)[word] : 0x88888888u;
-  sr.sv = reinterpret_cast<const uint4*>(sb + kSOff)[word];
-  const uint8_t* q0 = sb + lo.q[0];
-  const uint8_t* q1 = sb + lo.q[1];
+// 64-row unit `hh` (0, 1) of the stage at `sb`
+__device__ __forceinline__ void load_stage(const uint8_t* sb, int hh, const LaneOffsets& lo, StageRegs& sr) {
+  const uint8_t* q0 = sb + hh * kBoxBytes + lo.q[0];
+  const uint8_t* q1 = sb + hh * kBoxBytes + lo.q[1];
+  const uint8_t* xb = sb + hh * kXBoxBytes;
 #pragma unroll
   for (int it = 0; it < 4; ++it) {
     const int base = 16 * it;  // (base + 2t + c) & 7 == (2t + c) & 7
@@ -163,43 +168,129 @@ __device__ __forceinline__ void load_stage(const uint8_t* sb, bool has_z, int wo
     sr.r[it][2] = *reinterpret_cast<const uint32_t*>(q0 + (base + 8) * 128);
     sr.r[it][3] = *reinterpret_cast<const uint32_t*>(q1 + (base + 8) * 128);
     // k + 8 is the neighbouring 16-byte chunk: physical chunk ^ 1, address ^ 16
-    sr.b[it][0] = *reinterpret_cast<const uint32_t*>(sb + lo.x[it]);
-    sr.b[it][1] = *reinterpret_cast<const uint32_t*>(sb + (lo.x[it] ^ 16u));
+    sr.b[it][0] = *reinterpret_cast<const uint32_t*>(xb + lo.x[it]);
+    sr.b[it][1] = *reinterpret_cast<const uint32_t*>(xb + (lo.x[it] ^ 16u));
   }
 }
 
-// acc += W^T x over the 64 rows held in `sr` (this lane's packed word column, 8 tokens).
-__device__ __forceinline__ void compute_stage(const StageRegs& sr, float (&acc)[4][4]) {
+// Zero-point / scale constants of this lane's packed word for one quantization group:
+// zlo / zhi = 1024 + z and 1024 + 16 z of slots 2b / 2b + 1 (both halves), slo / shi = s and s / 16.
+struct GroupConsts {
   uint32_t zlo[4], zhi[4], slo[4], shi[4];
+};
+
+__device__ __forceinline__ void group_consts(uint32_t zword, const uint4& sv, GroupConsts& c) {
 #pragma unroll
   for (int b = 0; b < 4; ++b) {
-    const uint32_t zb = prmt(sr.zword, sr.zword, byte_sel(b));
-    zlo[b] = magic<0x000F000Fu>(zb);  // 1024 + z(slot 2b)
-    zhi[b] = magic<0x00F000F0u>(zb);  // 1024 + 16 z(slot 2b+1)
-    slo[b] = bcast_half(sr.sv, order_map(2 * b));
-    shi[b] = hmul2(bcast_half(sr.sv, order_map(2 * b + 1)), 0x2C002C00u);  // s / 16
+    const uint32_t zb = prmt(zword, zword, byte_sel(b));
+    c.zlo[b] = magic<0x000F000Fu>(zb);  // 1024 + z(slot 2b)
+    c.zhi[b] = magic<0x00F000F0u>(zb);  // 1024 + 16 z(slot 2b+1)
+    c.slo[b] = bcast_half(sv, order_map(2 * b));
+    c.shi[b] = hmul2(bcast_half(sv, order_map(2 * b + 1)), 0x2C002C00u);  // s / 16, exact
   }
+}
+
+// acc += W^T x over the 64 rows held in `sr` (this lane's packed word column, 8 tokens).  Each
+// 16-row step is written as phases over its four independent byte positions (PRMT, LOP3, HSUB2,
+// HMUL2, mma) so that no instruction waits on the one issued just before it.
+__device__ __forceinline__ void compute_stage(const StageRegs& sr, const GroupConsts& c, float (&acc)[4][4]) {
 #pragma unroll
   for (int it = 0; it < 4; ++it) {
+    uint32_t p01[4], p23[4], a[4][4];
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
-      const uint32_t p01 = prmt(sr.r[it][0], sr.r[it][1], byte_sel(b));
-      const uint32_t p23 = prmt(sr.r[it][2], sr.r[it][3], byte_sel(b));
-      const uint32_t a0 = hmul2(hsub2(magic<0x000F000Fu>(p01), zlo[b]), slo[b]);
-      const uint32_t a1 = hmul2(hsub2(magic<0x00F000F0u>(p01), zhi[b]), shi[b]);
-      const uint32_t a2 = hmul2(hsub2(magic<0x000F000Fu>(p23), zlo[b]), slo[b]);
-      const uint32_t a3 = hmul2(hsub2(magic<0x00F000F0u>(p23), zhi[b]), shi[b]);
-      mma16816(acc[b], a0, a1, a2, a3, sr.b[it][0], sr.b[it][1]);
+      p01[b] = prmt(sr.r[it][0], sr.r[it][1], byte_sel(b));
+      p23[b] = prmt(sr.r[it][2], sr.r[it][3], byte_sel(b));
+    }
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      a[b][0] = magic<0x000F000Fu>(p01[b]);
+      a[b][1] = magic<0x00F000F0u>(p01[b]);
+      a[b][2] = magic<0x000F000Fu>(p23[b]);
+      a[b][3] = magic<0x00F000F0u>(p23[b]);
+    }
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      a[b][0] = hsub2(a[b][0], c.zlo[b]);
+      a[b][1] = hsub2(a[b][1], c.zhi[b]);
+      a[b][2] = hsub2(a[b][2], c.zlo[b]);
+      a[b][3] = hsub2(a[b][3], c.zhi[b]);
+    }
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      a[b][0] = hmul2(a[b][0], c.slo[b]);
+      a[b][1] = hmul2(a[b][1], c.shi[b]);
+      a[b][2] = hmul2(a[b][2], c.slo[b]);
+      a[b][3] = hmul2(a[b][3], c.shi[b]);
+    }
+#pragma unroll
+    for (int b = 0; b < 4; ++b) mma16816(acc[b], a[b][0], a[b][1], a[b][2], a[b][3], sr.b[it][0], sr.b[it][1]);
+  }
+}
+
+// Stages of a CTA's unit range: a stage is a whole quantization group (two 64-row units) when the
+// range holds both halves of it, else a lone unit.  Every role walks the same sequence.
+struct StageWalk {
+  int u, u1, RB;
+  __device__ __forceinline__ StageWalk(int u0_, int u1_, int RB_) : u(u0_), u1(u1_), RB(RB_) {}
+  // units of the stage starting at u: 2 if u is group-aligned and u + 1 is in the range and tile
+  __device__ __forceinline__ int units_here() const {
+    const int rb = u % RB;
+    return (kUnitsPerStage == 2 && (rb & 1) == 0 && u + 1 < u1 && rb + 1 < RB) ? 2 : 1;
+  }
+};
+
+// Sum of the tile's partials in contributor order, rounded once to fp16 (run by the last contributor).
+__device__ __forceinline__ void reduce_tile(const float* __restrict__ part, __half* __restrict__ y, int tile,
+                                            int nt, int maxc, int M, int N, int tid, int nthreads) {
+  const float4* base = reinterpret_cast<const float4*>(part + (size_t)tile * maxc * kGemvMaxM * kTileCols);
+  constexpr int kQuads = kTileCols / 4;
+  constexpr size_t kSlotQuads = (size_t)kGemvMaxM * kQuads;
+  // two quads per thread and eight contributors per step: sixteen 16-byte loads in flight
+  for (int q0 = tid; q0 < M * kQuads; q0 += 2 * nthreads) {
+    const int q1 = q0 + nthreads;
+    const bool has1 = q1 < M * kQuads;
+    float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0;
+    for (int j0 = 0; j0 < nt; j0 += 8) {
+      float4 v0[8], v1[8];
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+        const bool in = j0 + jj < nt;
+        v0[jj] = in ? __ldcg(base + (size_t)(j0 + jj) * kSlotQuads + q0) : make_float4(0.f, 0.f, 0.f, 0.f);
+        v1[jj] = (in && has1) ? __ldcg(base + (size_t)(j0 + jj) * kSlotQuads + q1) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+        s0.x += v0[jj].x; s0.y += v0[jj].y; s0.z += v0[jj].z; s0.w += v0[jj].w;
+        s1.x += v1[jj].x; s1.y += v1[jj].y; s1.z += v1[jj].z; s1.w += v1[jj].w;
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int q = k ? q1 : q0;
+      if (k && !has1) break;
+      const float4 sv = k ? s1 : s0;
+      const int m = q / kQuads;
+      const int n = tile * kTileCols + (q - m * kQuads) * 4;
+      if (n < N) {  // N % 32 == 0: all four outputs are in range
+        __half2* dst = reinterpret_cast<__half2*>(y + (size_t)m * N + n);
+        dst[0] = __floats2half2_rn(sv.x, sv.y);
+        dst[1] = __floats2half2_rn(sv.z, sv.w);
+      }
     }
   }
 }
 
-__global__ void __launch_bounds__(kThreads, kCtasPerSm)
+// Register cap that still lets two CTAs share an SM (a launch-bounds hint made the compiler stop at 96
+// and spill).
+constexpr int kMaxRegs = (65536 / (kThreads * kCtasPerSm)) / 8 * 8;
+
+__global__ void __maxnreg__(kMaxRegs)
 gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_x,
             const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_s, int has_z,
             __half* __restrict__ y, float* __restrict__ part, int* __restrict__ counters, int* __restrict__ err,
             int M, int N, int RB, int tiles, int maxc) {
-  // RB = K / 64 row blocks per tile; unit u = (tile u / RB, row block u % RB)
+  // RB = K / 64 row blocks per tile; unit u = (tile u / RB, row block u % RB); units < 2^31 (host check)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
@@ -208,11 +299,11 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int64_t units = (int64_t)tiles * RB;
-  const int64_t P = gridDim.x;
-  const int64_t p = blockIdx.x;
-  const int64_t u0 = unit_begin(p, units, P);
-  const int64_t u1 = unit_begin(p + 1, units, P);
+  const int units = tiles * RB;
+  const int P = gridDim.x;
+  const int p = blockIdx.x;
+  const int u0 = (int)unit_begin(p, units, P);
+  const int u1 = (int)unit_begin(p + 1, units, P);
   auto full_bar = [&](int s) { return smem_u32(bars + s); };
   auto empty_bar = [&](int s) { return smem_u32(bars + kStages + s); };
 
@@ -233,41 +324,54 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
   if (warp == kConsumers) {
     // ------------------------------------------------ TMA producer
     if (lane == 0) {
-      const uint32_t tx = kQBytes + kXBytes + (has_z ? kZBytes : 0) + kSBytes;
-      auto issue_weights = [&](int st, int64_t u) {
-        const int tile = (int)(u / RB);
-        const int rb = (int)(u - (int64_t)tile * RB);
+      auto tx_bytes = [&](int nh) {
+        return (uint32_t)(nh * (kUnitQBytes + kXBoxBytes) + (has_z ? kZBytes : 0) + kSBytes);
+      };
+      auto issue_weights = [&](int st, int u, int nh) {
+        const int tile = u / RB;
+        const int rb = u - tile * RB;
         const int grp = rb / (kGroup / kRows);
         uint8_t* sb = smem + st * kStageBytes;
+        for (int hh = 0; hh < nh; ++hh)
 #pragma unroll
-        for (int bx = 0; bx < kTileWords / kBoxWords; ++bx)
-          tma_load_2d(smem_u32(sb + bx * kBoxBytes), &tm_q, tile * kTileWords + bx * kBoxWords, rb * kRows,
-                      full_bar(st));
+          for (int bx = 0; bx < kTileWords / kBoxWords; ++bx)
+            tma_load_2d(smem_u32(sb + bx * kColStride + hh * kBoxBytes), &tm_q, tile * kTileWords + bx * kBoxWords,
+                        (rb + hh) * kRows, full_bar(st));
         if (has_z) tma_load_2d(smem_u32(sb + kZOff), &tm_z, tile * kTileWords, grp, full_bar(st));
         // scales viewed as int32 pairs: 512 columns = one 256-pair box
         tma_load_2d(smem_u32(sb + kSOff), &tm_s, tile * (kTileCols / 2), grp, full_bar(st));
       };
-      auto issue_x = [&](int st, int64_t u) {
-        const int rb = (int)(u % RB);
-        tma_load_2d(smem_u32(smem + st * kStageBytes + kXOff), &tm_x, rb * kRows, 0, full_bar(st));
+      auto issue_x = [&](int st, int u, int nh) {
+        const int rb = u % RB;
+        for (int hh = 0; hh < nh; ++hh)
+          tma_load_2d(smem_u32(smem + st * kStageBytes + kXOff + hh * kXBoxBytes), &tm_x, (rb + hh) * kRows, 0,
+                      full_bar(st));
       };
-      const int64_t n = u1 - u0;
-      const int pre = (int)(n < kStages ? n : kStages);
-      // weights of the first stages stream before the wait on the previous kernel
-      for (int i = 0; i < pre; ++i) {
-        mbar_arrive_tx(full_bar(i), tx);
-        issue_weights(i, u0 + i);
+      // the first stages' weights stream before the wait on the previous kernel
+      StageWalk w(u0, u1, RB);
+      int pre = 0;
+      int pre_u[kStages], pre_nh[kStages];
+      while (pre < kStages && w.u < u1) {
+        const int nh = w.units_here();
+        mbar_arrive_tx(full_bar(pre), tx_bytes(nh));
+        issue_weights(pre, w.u, nh);
+        pre_u[pre] = w.u;
+        pre_nh[pre] = nh;
+        ++pre;
+        w.u += nh;
       }
       asm volatile("griddepcontrol.wait;" ::: "memory");
-      for (int i = 0; i < pre; ++i) issue_x(i, u0 + i);
+      for (int i = 0; i < pre; ++i) issue_x(i, pre_u[i], pre_nh[i]);
       int issued = pre;
-      for (int64_t u = u0 + pre; u < u1; ++u, ++issued) {
+      for (; w.u < u1; ++issued) {
         const int st = issued % kStages;
         const uint32_t ph = (uint32_t)(issued / kStages) & 1u;
         if (!wait_bounded(empty_bar(st), ph ^ 1u, abort_flag, err, 501)) break;
-        mbar_arrive_tx(full_bar(st), tx);
-        issue_weights(st, u);
-        issue_x(st, u);
+        const int nh = w.units_here();
+        mbar_arrive_tx(full_bar(st), tx_bytes(nh));
+        issue_weights(st, w.u, nh);
+        issue_x(st, w.u, nh);
+        w.u += nh;
       }
       // never leave the CTA with copies in flight: the last stages issued must have landed
       volatile int no_abort = 0;
@@ -281,24 +385,42 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     const int word = warp * 8 + g;    // this lane's packed word column in the tile
     const LaneOffsets lo = lane_offsets(word, g, t);
     bool waited = false;
-    int64_t i = 0;                    // stage counter, identical to the producer's
-    for (int64_t seg = u0; seg < u1;) {
-      const int tile = (int)(seg / RB);
-      const int64_t seg_end = min(u1, (int64_t)(tile + 1) * RB);
+    bool shared_tiles = false;        // any tile of this range also computed by another CTA
+    GroupConsts gc;                   // zero / scale constants of the current group (cached_grp)
+    int cached_grp = -1;
+    int i = 0;                        // stage counter, identical to the producer's
+    StageWalk w(u0, u1, RB);
+    while (w.u < u1) {
+      const int tile = w.u / RB;
+      const int seg_end = min(u1, (tile + 1) * RB);
       float acc[4][4];
 #pragma unroll
       for (int b = 0; b < 4; ++b)
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[b][e] = 0.f;
-      for (int64_t u = seg; u < seg_end; ++u, ++i) {
-        const int st = (int)(i % kStages);
+      cached_grp = -1;  // a new tile: other columns
+      for (; w.u < seg_end; ++i) {
+        const int nh = w.units_here();
+        w.u += nh;
+        const int st = i % kStages;
         const uint32_t ph = (uint32_t)(i / kStages) & 1u;
-        StageRegs sr;
+        const uint8_t* sb = smem + st * kStageBytes;
+        const int grp = (w.u - nh - tile * RB) / (kGroup / kRows);
         const bool ok = wait_bounded(full_bar(st), ph, abort_flag, err, 503);
-        if (ok) load_stage(smem + st * kStageBytes, has_z != 0, word, lo, sr);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(empty_bar(st));  // slot free before the arithmetic
-        if (ok) compute_stage(sr, acc);
+        if (ok && grp != cached_grp) {  // a stage never spans two groups
+          const uint32_t zword = has_z ? reinterpret_cast<const uint32_t*>(sb + kZOff)[word] : 0x88888888u;
+          group_consts(zword, reinterpret_cast<const uint4*>(sb + kSOff)[word], gc);
+          cached_grp = grp;
+        }
+        for (int hh = 0; hh < nh; ++hh) {
+          StageRegs sr;
+          if (ok) load_stage(sb, hh, lo, sr);
+          if (hh == nh - 1) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty_bar(st));  // slot free before the last unit's arithmetic
+          }
+          if (ok) compute_stage(sr, gc, acc);
+        }
       }
 
       // ---- flush: this warp owns its 64 columns; CTAs sharing the tile meet in the workspace
@@ -306,11 +428,10 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         asm volatile("griddepcontrol.wait;" ::: "memory");  // outputs and workspace of the previous kernel
         waited = true;
       }
-      const int64_t pf = cta_of_unit((int64_t)tile * RB, units, P);
-      const int64_t pl = cta_of_unit((int64_t)(tile + 1) * RB - 1, units, P);
-      const int nt = (int)(pl - pf + 1);
+      const int pf = (int)cta_of_unit(tile * RB, units, P);
+      const int pl = (int)cta_of_unit((tile + 1) * RB - 1, units, P);
       // D fragment: acc[b][0/1] = (column lo of byte b, tokens 2t / 2t+1), acc[b][2/3] = column hi
-      if (nt == 1) {
+      if (pf == pl) {
 #pragma unroll
         for (int b = 0; b < 4; ++b)
 #pragma unroll
@@ -328,42 +449,28 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             const int m = 2 * t + (e & 1);
             if (m < M) slot[m * kTileCols + word * 8 + order_map(2 * b + (e >> 1))] = acc[b][e];
           }
-        __threadfence();
-        consumers_sync();
+        shared_tiles = true;
+      }
+    }
+
+    // ---- tickets of the shared tiles, after the whole range: one fence for all partials
+    if (shared_tiles) {
+      __threadfence();
+      consumers_sync();
+      for (int tile = u0 / RB; tile <= (u1 - 1) / RB; ++tile) {
+        const int pf = (int)cta_of_unit(tile * RB, units, P);
+        const int pl = (int)cta_of_unit((tile + 1) * RB - 1, units, P);
+        if (pf == pl) continue;
+        const int nt = pl - pf + 1;
         if (threadIdx.x == 0) *last_flag = (atomicAdd(counters + tile, 1) == nt - 1);
         consumers_sync();
         if (*last_flag) {
           __threadfence();
-          // contributor-ordered sum, eight partials in flight per step
-          const float4* base = reinterpret_cast<const float4*>(part + (size_t)tile * maxc * kGemvMaxM * kTileCols);
-          constexpr int kQuads = kTileCols / 4;
-          constexpr size_t kSlotQuads = (size_t)kGemvMaxM * kQuads;
-          for (int q = threadIdx.x; q < M * kQuads; q += kConsumers * 32) {
-            float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int j0 = 0; j0 < nt; j0 += 8) {
-              float4 v[8];
-#pragma unroll
-              for (int jj = 0; jj < 8; ++jj)
-                v[jj] = (j0 + jj < nt) ? __ldcg(base + (size_t)(j0 + jj) * kSlotQuads + q)
-                                       : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-              for (int jj = 0; jj < 8; ++jj) {
-                s.x += v[jj].x; s.y += v[jj].y; s.z += v[jj].z; s.w += v[jj].w;
-              }
-            }
-            const int m = q / kQuads;
-            const int n = tile * kTileCols + (q - m * kQuads) * 4;
-            if (n < N) {  // N % 32 == 0: all four outputs are in range
-              __half2* dst = reinterpret_cast<__half2*>(y + (size_t)m * N + n);
-              dst[0] = __floats2half2_rn(s.x, s.y);
-              dst[1] = __floats2half2_rn(s.z, s.w);
-            }
-          }
+          reduce_tile(part, y, tile, nt, maxc, M, N, threadIdx.x, kConsumers * 32);
           if (threadIdx.x == 0) atomicExch(counters + tile, 0);  // leave the ticket at zero for the next call
         }
         consumers_sync();  // last_flag is reused by the next tile
       }
-      seg = seg_end;
     }
   }
   __syncthreads();
@@ -427,6 +534,8 @@ size_t gemv_workspace_bytes(const GemvPlan& p, int64_t M, int64_t N) {
 cudaError_t launch_gemv(const uint16_t* x, const uint32_t* qw, const uint32_t* qz, const uint16_t* sc,
                         uint16_t* y, int64_t M, int64_t K, int64_t N, const GemvPlan& p, void* ws,
                         int* err, cudaStream_t s) {
+  // the kernel counts (tile, 64-row block) units in 32 bits; any tensor that fits a GPU stays far below
+  if ((int64_t)p.tiles * p.groups >= ((int64_t)1 << 31)) return cudaErrorInvalidValue;
   float* part = nullptr;
   int* counters = nullptr;
   if (p.maxc > 1) {
