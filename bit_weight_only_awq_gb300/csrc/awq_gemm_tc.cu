@@ -44,34 +44,38 @@ namespace awq {
 namespace {
 
 constexpr int kBK = 64;          // input rows per k-step
-constexpr int kBN = 128;         // weight columns per CTA (MMA M)
-constexpr int kQWords = kBN / 8; // packed words per row of a stage
+constexpr int kBN = 128;         // weight columns per MMA (M) = per M-block
 constexpr int kDqGroupWarps = 8;              // one group dequantizes one stage (256 threads)
 constexpr int kDqGroups = 2;                  // groups alternate stages to overlap their latency
 constexpr int kDqWarps = kDqGroupWarps * kDqGroups;
 constexpr int kThreads = (3 + kDqWarps) * 32;   // x producer, MMA, q producer, dequant
-constexpr int kWBytes = kBK * kBN * 2;     // dequantized tile, 16 KB
-constexpr int kQBytes = kBK * kQWords * 4; // packed tile, 4 KB
-constexpr int kZBytes = kQWords * 4;       // one zero-point row, 64 B
-constexpr int kSBytes = kBN * 2;           // one scale row, 256 B
-constexpr int kQStage = kQBytes + 128 + kSBytes;  // packed tile | zero row (padded) | scale row
-constexpr int kQStages = 8;
-constexpr int kWStages = 3;
+constexpr int kWBlockBytes = kBK * kBN * 2;     // dequantized tile of one M-block, 16 KB
 
-template <int BT>
+// NB M-blocks of 128 weight columns share every activation tile: with NB = 2 a CTA owns 256 columns
+// and the activation bytes per flop halve (the ring that feeds them was the measured limit at NB = 1).
+template <int BT, int NB, int MODE>
 struct Cfg {
+  static constexpr int kQWords = NB * kBN / 8;          // packed words per row of a stage
+  static constexpr int kQBytes = kBK * kQWords * 4;     // packed tile, 4 KB per M-block
+  static constexpr int kZBytes = kQWords * 4;           // one zero-point row
+  static constexpr int kSBytes = NB * kBN * 2;          // one scale row
+  static constexpr int kQStage = kQBytes + 128 + kSBytes;  // packed tile | zero row (padded) | scale row
+  static constexpr int kWBytes = NB * kWBlockBytes;
+  static constexpr int kQStages = NB == 1 ? 8 : 4;
+  static constexpr int kWStages = NB == 1 ? 3 : 2;
   static constexpr int kXBytes = BT * kBK * 2;
   static constexpr int kFixed = kWStages * kWBytes + kQStages * kQStage + 2048;
-  static constexpr int kFit = (227 * 1024 - kFixed) / kXBytes;
+  static constexpr int kFit = (227 * 1024 - 1024 - kFixed) / kXBytes;
   static constexpr int kXStages = kFit > 8 ? 8 : kFit;
   static constexpr int kSmem = kXStages * kXBytes + kFixed + 1024;
-  static constexpr int kTmemCols1 = BT < 32 ? 32 : BT;  // one accumulator
-  static constexpr int kTmemCols2 = 2 * BT < 32 ? 32 : 2 * BT;  // two (W4A8: one per exact K chunk)
+  static constexpr int kAccs = MODE == kModeW4A8 ? 2 : 1;  // W4A8: one accumulator per exact K chunk
+  static constexpr int kTmemCols = NB * kAccs * BT < 32 ? 32 : NB * kAccs * BT;
   // tcgen05 instruction descriptor, kind::f16: D f32, A/B f16, A MN-major, B K-major, M=128, N=BT
   static constexpr uint32_t kIdesc = (1u << 4) | (1u << 15) | ((uint32_t)(BT >> 3) << 17) |
                                      ((uint32_t)(kBN >> 4) << 24);
   static_assert(kXStages >= 2, "activation ring");
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
+  static_assert(kTmemCols <= 512, "tensor memory");
 };
 
 // ------------------------------------------------------------------ tcgen05 mma (A, B from shared memory)
@@ -97,17 +101,24 @@ __device__ __forceinline__ uint32_t pair_magic(uint32_t w, int j) {
 }
 
 // ------------------------------------------------------------------ kernel
-template <int BT, int MODE>
+template <int BT, int NB, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_q,
             const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_s,
             __half* __restrict__ y, int32_t* __restrict__ acc_out, const float* __restrict__ s_tok,
             const __half* __restrict__ s_ch, void* __restrict__ part, int* __restrict__ counters,
             int* __restrict__ err, int M, int N, int K, int ksteps_per_split, int chunk_steps) {
-  using C = Cfg<BT>;
-  // W4A8 keeps one TMEM accumulator per chunk of at most chunk_steps k-steps (16384 rows), each an
-  // exact integer in fp32; W4A16 uses one accumulator for its whole K slice.
-  constexpr int kTmemCols = MODE == kModeW4A8 ? C::kTmemCols2 : C::kTmemCols1;
+  using C = Cfg<BT, NB, MODE>;
+  // Accumulators in tensor memory: M-block b of K chunk c at column (c * NB + b) * BT.  W4A8 keeps one
+  // per chunk of at most chunk_steps k-steps (16384 rows), each an exact integer in fp32; W4A16 uses
+  // one per M-block for its whole K slice.
+  constexpr int kTmemCols = C::kTmemCols;
+  constexpr int kQStages = C::kQStages;
+  constexpr int kWStages = C::kWStages;
+  constexpr int kQStage = C::kQStage;
+  constexpr int kQBytes = C::kQBytes;
+  constexpr int kQWords = C::kQWords;
+  constexpr int kWBytes = C::kWBytes;
   constexpr int SX = C::kXStages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -122,7 +133,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * kBN;
+  const int n0 = blockIdx.x * (NB * kBN);
   const int m0 = blockIdx.y * BT;
   const int total_steps = K / kBK;
   const int step0 = blockIdx.z * ksteps_per_split;
@@ -172,8 +183,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
       const bool is_x = warp == 0;
       const int S = is_x ? SX : kQStages;
       const uint32_t tx = is_x ? (uint32_t)C::kXBytes
-                               : (uint32_t)(kQBytes + (MODE == kModeZeroPoint ? kZBytes : 0) +
-                                            (MODE != kModeW4A8 ? kSBytes : 0));
+                               : (uint32_t)(kQBytes + (MODE == kModeZeroPoint ? C::kZBytes : 0) +
+                                            (MODE != kModeW4A8 ? C::kSBytes : 0));
       int issued = 0;
       for (int it = 0; it < nsteps; ++it, ++issued) {
         const int st = it % S;
@@ -213,11 +224,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         const int within = MODE == kModeW4A8 ? it - chunk * chunk_steps : it;
 #pragma unroll
         for (int kk = 0; kk < kBK / 16; ++kk) {
-          // A: weights, MN-major; 64-column atoms 1024 B apart (LBO), 8-row k groups 2048 B apart (SBO)
-          const uint64_t ad = smem_desc_sw128(wa + kk * 2 * 2048, 1024, 2048);
           // B: activations, K-major; 16 k = 32 B inside the 128-byte swizzle row, 8-row groups 1024 B apart
           const uint64_t bd = smem_desc_sw128(xa + kk * 32, 16, 1024);
-          mma_f16(tmem + (uint32_t)(chunk * BT), ad, bd, C::kIdesc, (within > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+          for (int b = 0; b < NB; ++b) {
+            // A: weights of M-block b, MN-major; 64-column atoms 1024 B apart (LBO), 8-row k groups 2048 B apart (SBO)
+            const uint64_t ad = smem_desc_sw128(wa + b * kWBlockBytes + kk * 2 * 2048, 1024, 2048);
+            mma_f16(tmem + (uint32_t)((chunk * NB + b) * BT), ad, bd, C::kIdesc, (within > 0 || kk > 0) ? 1u : 0u);
+          }
         }
         mma_commit(emptyx(xs));  // both arrive once these mmas have read their operands
         mma_commit(wempty(ws));
@@ -230,8 +244,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     // ------------------------------------------------ dequant warps (two groups, alternate k-steps)
     const int group = (threadIdx.x - 96) / (kDqGroupWarps * 32);
     const int d = (threadIdx.x - 96) % (kDqGroupWarps * 32);  // 0..255 within the group
-    const int c = d & 15;            // packed word column within the tile
-    const int r0 = d >> 4;           // first of the thread's 4 rows (r0 + 16 j)
+    constexpr int kRowsPerPass = kDqGroupWarps * 32 / kQWords;  // 16 (NB = 1) or 8 (NB = 2)
+    constexpr int kPasses = kBK / kRowsPerPass;                   // rows per thread: 4 NB
+    const int c = d % kQWords;       // packed word column within the tile (M-block c / 16)
+    const int r0 = d / kQWords;      // first of the thread's rows (r0 + kRowsPerPass j)
+    const int cw = c & 15;           // word column within its M-block
+    const uint32_t blk_off = (uint32_t)((c >> 4) * kWBlockBytes);
     for (int it = group; it < nsteps; it += kDqGroups) {
       const int qs = it % kQStages, ws = it % kWStages;
       if (!wait_bounded(fullq(qs), (uint32_t)(it / kQStages) & 1u, abort_flag, err, 301)) break;
@@ -248,14 +266,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
 #pragma unroll
         for (int j = 0; j < 4; ++j) zp[j] = pair_magic(zword, j);
       }
-      uint32_t words[4];
+      uint32_t words[kPasses];
 #pragma unroll
-      for (int jr = 0; jr < 4; ++jr) words[jr] = qw[(r0 + 16 * jr) * kQWords + c];
+      for (int jr = 0; jr < kPasses; ++jr) words[jr] = qw[(r0 + kRowsPerPass * jr) * kQWords + c];
       __syncwarp();
       if (lane == 0) mbar_arrive(emptyq(qs));  // packed words are in registers: the slot can refill
 #pragma unroll
-      for (int jr = 0; jr < 4; ++jr) {
-        const int r = r0 + 16 * jr;
+      for (int jr = 0; jr < kPasses; ++jr) {
+        const int r = r0 + kRowsPerPass * jr;
         uint32_t o[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -263,7 +281,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
           o[j] = (MODE == kModeW4A8) ? hsub2(h, 0x64086408u) /* u - 8, exact */
                                      : hmul2(hsub2(h, zp[j]), sp[j]);
         }
-        const uint32_t off = (uint32_t)((r >> 3) * 2048 + (c >> 3) * 1024 + (r & 7) * 128 + (((c & 7) ^ (r & 7)) << 4));
+        const uint32_t off =
+            blk_off + (uint32_t)((r >> 3) * 2048 + (cw >> 3) * 1024 + (r & 7) * 128 + (((cw & 7) ^ (r & 7)) << 4));
         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(smem_u32(wt + off)), "r"(o[0]), "r"(o[1]),
                      "r"(o[2]), "r"(o[3])
                      : "memory");
@@ -273,14 +292,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
       if (lane == 0) mbar_arrive(wready(ws));
     }
 
-    // ------------------------------------------------ epilogue (first dequant group)
-    if (group == 0) {
+    // ------------------------------------------------ epilogue (dequant group b reads M-block b)
+    if (group < NB) {
     const bool have = wait_bounded(accf_bar, 0, abort_flag, err, 401);
     tc_fence_after();
     const int lq = warp & 3;                 // TMEM lane quarter this warp may access
-    const int half = (warp - 3) >> 2;        // which half of the BT token columns
-    const int nl = lq * 32 + lane;           // TMEM lane = weight column in the tile
-    const int n = n0 + nl;
+    const int half = ((warp - 3) & 7) >> 2;  // which half of the BT token columns
+    const int nl = lq * 32 + lane;           // TMEM lane = weight column in the M-block
+    const int n = n0 + group * kBN + nl;
+    const uint32_t dcol = (uint32_t)(group * BT);  // this M-block's accumulator
     const bool n_ok = n < N;
     const int split = gridDim.z;
     constexpr int kHalf = BT / 2;
@@ -290,14 +310,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
 #pragma unroll 1
       for (int cb = half * kHalf; cb < (half + 1) * kHalf; cb += 8) {
         float v[8];
-        tmem_ld8(tmem + ((uint32_t)(lq * 32) << 16) + (uint32_t)cb, v);
+        tmem_ld8(tmem + ((uint32_t)(lq * 32) << 16) + dcol + (uint32_t)cb, v);
         int vi[8];
         if (MODE == kModeW4A8) {
 #pragma unroll
           for (int j = 0; j < 8; ++j) vi[j] = __float2int_rn(v[j]);  // exact integers
           if (nsteps > chunk_steps) {
             float v2[8];
-            tmem_ld8(tmem + ((uint32_t)(lq * 32) << 16) + (uint32_t)(BT + cb), v2);
+            tmem_ld8(tmem + ((uint32_t)(lq * 32) << 16) + dcol + (uint32_t)(NB * BT + cb), v2);
 #pragma unroll
             for (int j = 0; j < 8; ++j) vi[j] += __float2int_rn(v2[j]);
           }
@@ -324,12 +344,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     }
     if (split > 1) {
       __threadfence();
-      asm volatile("bar.sync 1, %0;" ::"r"(kDqGroupWarps * 32) : "memory");
-      if (d == 0) {
+      asm volatile("bar.sync 1, %0;" ::"r"(NB * kDqGroupWarps * 32) : "memory");  // the epilogue groups
+      if (group == 0 && d == 0) {
         const int ctr = blockIdx.y * gridDim.x + blockIdx.x;
         *last_flag = (atomicAdd(counters + ctr, 1) == split - 1);
       }
-      asm volatile("bar.sync 1, %0;" ::"r"(kDqGroupWarps * 32) : "memory");
+      asm volatile("bar.sync 1, %0;" ::"r"(NB * kDqGroupWarps * 32) : "memory");
       if (*last_flag) {
         __threadfence();
         for (int cb = half * kHalf; cb < (half + 1) * kHalf; ++cb) {
@@ -347,7 +367,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             y[o] = __float2half_rn(a);
           }
         }
-        if (d == 0) atomicExch(counters + blockIdx.y * gridDim.x + blockIdx.x, 0);
+        if (group == 0 && d == 0) atomicExch(counters + blockIdx.y * gridDim.x + blockIdx.x, 0);
       }
     }
   }
@@ -387,12 +407,13 @@ bool make_map_2d(CUtensorMap* map, CUtensorMapDataType dt, int elem_bytes, const
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BT, int MODE>
+template <int BT, int NB, int MODE>
 cudaError_t launch_t(const uint16_t* x16, const uint32_t* qw, const uint32_t* qz, const uint16_t* sc,
                      const float* s_tok, const uint16_t* s_ch, uint16_t* y, int32_t* acc_out, int64_t M,
                      int64_t K, int64_t N, const GemmPlan& p, void* part, int* counters, int* err,
                      cudaStream_t s) {
-  using C = Cfg<BT>;
+  using C = Cfg<BT, NB, MODE>;
+  constexpr int kQWords = C::kQWords;
   CUtensorMap tx, tq, tz, ts;
   const uint64_t nw = (uint64_t)N / 8, ng = (uint64_t)K / kGroup;
   bool ok = make_map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x16, (uint64_t)K, (uint64_t)M, kBK, BT,
@@ -405,10 +426,10 @@ cudaError_t launch_t(const uint16_t* x16, const uint32_t* qw, const uint32_t* qz
   ok = ok && (MODE == kModeW4A8
                   ? make_map_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, qw, nw, (uint64_t)K, kQWords, 1,
                                 CU_TENSOR_MAP_SWIZZLE_NONE)
-                  : make_map_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, sc, (uint64_t)N, ng, kBN, 1,
+                  : make_map_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, sc, (uint64_t)N, ng, NB * kBN, 1,
                                 CU_TENSOR_MAP_SWIZZLE_NONE));
   if (!ok) return cudaErrorInvalidValue;
-  auto kern = gemm_kernel<BT, MODE>;
+  auto kern = gemm_kernel<BT, NB, MODE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   dim3 grid(p.n_tiles, p.m_tiles, p.split);
@@ -423,12 +444,22 @@ cudaError_t launch_mode(const uint16_t* x16, const uint32_t* qw, const uint32_t*
                         const float* s_tok, const uint16_t* s_ch, uint16_t* y, int32_t* acc_out, int64_t M,
                         int64_t K, int64_t N, const GemmPlan& p, void* part, int* counters, int* err,
                         cudaStream_t s) {
+  if constexpr (MODE != kModeW4A8) {
+    if (p.nb == 2) {
+      switch (p.bt) {
+        case 128: return launch_t<128, 2, MODE>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters, err, s);
+        case 256: return launch_t<256, 2, MODE>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters, err, s);
+        default: return cudaErrorInvalidValue;
+      }
+    }
+  }
+  if (p.nb != 1) return cudaErrorInvalidValue;
   switch (p.bt) {
-    case 16: return launch_t<16, MODE>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters, err, s);
-    case 32: return launch_t<32, MODE>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters, err, s);
-    case 64: return launch_t<64, MODE>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters, err, s);
-    case 128: return launch_t<128, MODE>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters, err, s);
-    case 256: return launch_t<256, MODE>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters, err, s);
+    case 16: return launch_t<16, 1, MODE>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters, err, s);
+    case 32: return launch_t<32, 1, MODE>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters, err, s);
+    case 64: return launch_t<64, 1, MODE>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters, err, s);
+    case 128: return launch_t<128, 1, MODE>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters, err, s);
+    case 256: return launch_t<256, 1, MODE>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters, err, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -437,14 +468,27 @@ cudaError_t launch_mode(const uint16_t* x16, const uint32_t* qw, const uint32_t*
 
 GemmPlan gemm_plan(int64_t M, int64_t K, int64_t N, int split_k, int mode) {
   GemmPlan p;
-  p.bt = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
-  p.n_tiles = (int)((N + kBN - 1) / kBN);
-  p.m_tiles = (int)((M + p.bt - 1) / p.bt);
-  // under one wave of 152 SMs: narrower token tiles (down to 64) before splitting K
-  while (p.bt > 64 && (int64_t)p.n_tiles * p.m_tiles < 114) {
-    p.bt /= 2;
-    p.m_tiles = (int)((M + p.bt - 1) / p.bt);
+  const int bt0 = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
+  auto tiles = [&](int bt, int nb) {
+    return ((N + (int64_t)nb * kBN - 1) / ((int64_t)nb * kBN)) * ((M + bt - 1) / bt);
+  };
+  // 128 weight columns per CTA; under one wave of 152 SMs, narrower token tiles (down to 64) before
+  // splitting K
+  p.nb = 1;
+  p.bt = bt0;
+  while (p.bt > 64 && tiles(p.bt, 1) < 114) p.bt /= 2;
+  // W4A16 with >= 128-token tiles: 256 weight columns per CTA (two M-blocks on one activation tile)
+  // whenever that still fills about a wave
+  if (mode != kModeW4A8 && bt0 >= 128) {
+    int bt = bt0;
+    while (bt > 128 && tiles(bt, 2) < 114) bt /= 2;
+    if (tiles(bt, 2) >= 114) {
+      p.nb = 2;
+      p.bt = bt;
+    }
   }
+  p.n_tiles = (int)((N + (int64_t)p.nb * kBN - 1) / ((int64_t)p.nb * kBN));
+  p.m_tiles = (int)((M + p.bt - 1) / p.bt);
   const int total = (int)(K / kBK);
   int split = split_k;
   if (split <= 0) {

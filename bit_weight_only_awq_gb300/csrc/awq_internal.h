@@ -70,7 +70,8 @@ struct GemmPlan {
   int bt;        // token tile (MMA N): 16, 32, 64, 128 or 256
   int split;     // K slices (grid.z)
   int ksteps;    // 64-row k-steps per slice
-  int n_tiles;   // 128-column weight tiles (grid.x)
+  int nb;        // 128-column M-blocks per CTA (1, or 2 for W4A16 with >= 128-token tiles)
+  int n_tiles;   // (128 nb)-column weight tiles (grid.x)
   int m_tiles;   // token tiles (grid.y)
 };
 GemmPlan gemm_plan(int64_t M, int64_t K, int64_t N, int split_k, int mode);

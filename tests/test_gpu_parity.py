@@ -164,6 +164,18 @@ def test_gemm_mistral_shapes_sampled(awq, name, K, N, M):
     assert_within_tol(y[:, cols], ref, f"gemm {name} M={M}")
 
 
+@pytest.mark.parametrize("split_k", [1, 2])
+def test_gemm_two_mblock_tiles_ragged_tail(awq, split_k):
+    # M = 512, N = 14624: 58 tiles of 256 columns x 2 token tiles, the plan's two-M-block CTAs; the
+    # last tile holds 32 real columns, the rest of it lies beyond N
+    M, K, N = 512, 1024, 14624
+    p = synth.awq_problem(M, K, N, seed=3100 + split_k)
+    y = run_w4a16(awq, awq.awq_gemm, p, split_k)
+    wc = np.array(sorted(set(sample_word_cols(N // 8, seed=31, count=24).tolist()) | set(range(N // 8 - 4, N // 8))))
+    ref, cols = oracle_columns(p, wc)
+    assert_within_tol(y[:, cols], ref, f"gemm two M-blocks split={split_k}")
+
+
 def test_gemm_largest_prefill_sampled_rows(awq):
     K, N, M = 4096, 28672, 8192
     p = synth.awq_problem(M, K, N, seed=2999)
