@@ -63,22 +63,39 @@ struct Cfg {
   static constexpr int kWBytes = NB * kWBlockBytes;
   static constexpr int kQStages = NB == 1 ? 8 : 4;
   static constexpr int kWStages = NB == 1 ? 3 : 2;
-  static constexpr int kXBytes = BT * kBK * 2;
+  // With 256-token tiles the activation tile of a k-step arrives as two 32-k halves (64-byte swizzle),
+  // each in its own ring slot and released as soon as the two k16 mmas that read it are done: the ring
+  // is bound by (copy latency + hold time) per slot, and half-size slots hold for half as long
+  // (measured +5 % at 256 tokens; smaller tiles lose more to the per-copy cost than they gain).
+  static constexpr int kXK = BT >= 256 ? 32 : 64;
+  static constexpr int kXSub = kBK / kXK;
+  static constexpr int kXSlotBytes = BT * kXK * 2;
   static constexpr int kFixed = kWStages * kWBytes + kQStages * kQStage + 2048;
-  static constexpr int kFit = (227 * 1024 - 1024 - kFixed) / kXBytes;
-  static constexpr int kXStages = kFit > 8 ? 8 : kFit;
-  static constexpr int kSmem = kXStages * kXBytes + kFixed + 1024;
+  static constexpr int kFit = (227 * 1024 - 1024 - kFixed) / kXSlotBytes;
+  static constexpr int kXStages = kFit > 16 ? 16 : kFit;   // slots
+  static constexpr int kSmem = kXStages * kXSlotBytes + kFixed + 1024;
   static constexpr int kAccs = MODE == kModeW4A8 ? 2 : 1;  // W4A8: one accumulator per exact K chunk
   static constexpr int kTmemCols = NB * kAccs * BT < 32 ? 32 : NB * kAccs * BT;
   // tcgen05 instruction descriptor, kind::f16: D f32, A/B f16, A MN-major, B K-major, M=128, N=BT
   static constexpr uint32_t kIdesc = (1u << 4) | (1u << 15) | ((uint32_t)(BT >> 3) << 17) |
                                      ((uint32_t)(kBN >> 4) << 24);
-  static_assert(kXStages >= 2, "activation ring");
+  static_assert(kXStages >= 2 * kXSub, "activation ring");
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
   static_assert(kTmemCols <= 512, "tensor memory");
 };
 
 // ------------------------------------------------------------------ tcgen05 mma (A, B from shared memory)
+// Shared-memory descriptor of a K-major operand with 64-byte swizzle: rows of 64 bytes, 8-row groups
+// 512 bytes apart (layout type 4).
+__device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)(16 >> 4) << 16;
+  d |= (uint64_t)(512 >> 4) << 32;
+  d |= (uint64_t)1 << 46;  // descriptor version for tcgen05
+  d |= (uint64_t)4 << 61;  // 64-byte swizzle
+  return d;
+}
 __device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                         uint32_t accumulate) {
   asm volatile(
@@ -122,8 +139,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
   constexpr int SX = C::kXStages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  uint8_t* xring = smem;                                   // SX x BT*64 fp16 (1024-aligned slots)
-  uint8_t* wring = xring + SX * C::kXBytes;                // kWStages x 16 KB (1024-aligned)
+  uint8_t* xring = smem;                                   // SX slots of BT x 32 fp16 (1024-aligned)
+  uint8_t* wring = xring + SX * C::kXSlotBytes;            // kWStages x NB x 16 KB (1024-aligned)
   uint8_t* qring = wring + kWStages * kWBytes;             // kQStages x kQStage (128-aligned)
   uint64_t* bars = reinterpret_cast<uint64_t*>(qring + kQStages * kQStage);
   // bars: fullx[SX] emptyx[SX] fullq[Q] emptyq[Q] wready[W] wempty[W] accf
@@ -182,19 +199,20 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     if (lane == 0) {
       const bool is_x = warp == 0;
       const int S = is_x ? SX : kQStages;
-      const uint32_t tx = is_x ? (uint32_t)C::kXBytes
+      const uint32_t tx = is_x ? (uint32_t)C::kXSlotBytes
                                : (uint32_t)(kQBytes + (MODE == kModeZeroPoint ? C::kZBytes : 0) +
                                             (MODE != kModeW4A8 ? C::kSBytes : 0));
+      const int units = is_x ? nsteps * C::kXSub : nsteps;  // x: (k-step, 32-k half) slots
       int issued = 0;
-      for (int it = 0; it < nsteps; ++it, ++issued) {
-        const int st = it % S;
-        const uint32_t ph = (uint32_t)(it / S) & 1u;
+      for (int j = 0; j < units; ++j, ++issued) {
+        const int st = j % S;
+        const uint32_t ph = (uint32_t)(j / S) & 1u;
         if (!wait_bounded(is_x ? emptyx(st) : emptyq(st), ph ^ 1u, abort_flag, err, is_x ? 101 : 102)) break;
-        const int kb = (step0 + it) * kBK;
         if (is_x) {
           mbar_arrive_tx(fullx(st), tx);
-          tma_load_2d(smem_u32(xring + st * C::kXBytes), &tm_x, kb, m0, fullx(st));
+          tma_load_2d(smem_u32(xring + st * C::kXSlotBytes), &tm_x, step0 * kBK + j * C::kXK, m0, fullx(st));
         } else {
+          const int kb = (step0 + j) * kBK;
           const int grp = kb / kGroup;
           uint8_t* qb = qring + st * kQStage;
           mbar_arrive_tx(fullq(st), tx);
@@ -213,28 +231,34 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     if (lane == 0) {
       bool ok = true;
       for (int it = 0; it < nsteps && ok; ++it) {
-        const int xs = it % SX, ws = it % kWStages;
-        ok = wait_bounded(fullx(xs), (uint32_t)(it / SX) & 1u, abort_flag, err, 201) &&
-             wait_bounded(wready(ws), (uint32_t)(it / kWStages) & 1u, abort_flag, err, 202);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t xa = smem_u32(xring + xs * C::kXBytes);
+        const int ws = it % kWStages;
+        ok = wait_bounded(wready(ws), (uint32_t)(it / kWStages) & 1u, abort_flag, err, 202);
         const uint32_t wa = smem_u32(wring + ws * kWBytes);
         const int chunk = MODE == kModeW4A8 ? it / chunk_steps : 0;
         const int within = MODE == kModeW4A8 ? it - chunk * chunk_steps : it;
+        for (int h = 0; h < C::kXSub && ok; ++h) {
+          const int j = it * C::kXSub + h;
+          const int xs = j % SX;
+          ok = wait_bounded(fullx(xs), (uint32_t)(j / SX) & 1u, abort_flag, err, 201);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t xa = smem_u32(xring + xs * C::kXSlotBytes);
 #pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk) {
-          // B: activations, K-major; 16 k = 32 B inside the 128-byte swizzle row, 8-row groups 1024 B apart
-          const uint64_t bd = smem_desc_sw128(xa + kk * 32, 16, 1024);
+          for (int k2 = 0; k2 < C::kXK / 16; ++k2) {
+            const int kk = h * (C::kXK / 16) + k2;
+            // B: activations, K-major; 16 k = 32 B inside the 64- or 128-byte swizzle row, 8-row groups
+            // 512 or 1024 B apart
+            const uint64_t bd = C::kXK == 32 ? smem_desc_sw64(xa + k2 * 32) : smem_desc_sw128(xa + k2 * 32, 16, 1024);
 #pragma unroll
-          for (int b = 0; b < NB; ++b) {
-            // A: weights of M-block b, MN-major; 64-column atoms 1024 B apart (LBO), 8-row k groups 2048 B apart (SBO)
-            const uint64_t ad = smem_desc_sw128(wa + b * kWBlockBytes + kk * 2 * 2048, 1024, 2048);
-            mma_f16(tmem + (uint32_t)((chunk * NB + b) * BT), ad, bd, C::kIdesc, (within > 0 || kk > 0) ? 1u : 0u);
+            for (int b = 0; b < NB; ++b) {
+              // A: weights of M-block b, MN-major; 64-column atoms 1024 B apart (LBO), 8-row k groups 2048 B apart (SBO)
+              const uint64_t ad = smem_desc_sw128(wa + b * kWBlockBytes + kk * 2 * 2048, 1024, 2048);
+              mma_f16(tmem + (uint32_t)((chunk * NB + b) * BT), ad, bd, C::kIdesc, (within > 0 || kk > 0) ? 1u : 0u);
+            }
           }
+          mma_commit(emptyx(xs));  // this half of the activation tile is free once its mmas have read it
         }
-        mma_commit(emptyx(xs));  // both arrive once these mmas have read their operands
-        mma_commit(wempty(ws));
+        if (ok) mma_commit(wempty(ws));
       }
       mma_commit(accf_bar);  // arrives once every issued mma has completed
       volatile int no_abort = 0;
@@ -416,8 +440,8 @@ cudaError_t launch_t(const uint16_t* x16, const uint32_t* qw, const uint32_t* qz
   constexpr int kQWords = C::kQWords;
   CUtensorMap tx, tq, tz, ts;
   const uint64_t nw = (uint64_t)N / 8, ng = (uint64_t)K / kGroup;
-  bool ok = make_map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x16, (uint64_t)K, (uint64_t)M, kBK, BT,
-                        CU_TENSOR_MAP_SWIZZLE_128B) &&
+  bool ok = make_map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x16, (uint64_t)K, (uint64_t)M, C::kXK, BT,
+                        C::kXK == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B) &&
             make_map_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, qw, nw, (uint64_t)K, kQWords, kBK,
                         CU_TENSOR_MAP_SWIZZLE_NONE);
   // zero-point and scale maps: dummies (the weight map) when the mode does not read them
