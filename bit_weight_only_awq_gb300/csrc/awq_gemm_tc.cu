@@ -63,11 +63,12 @@ struct Cfg {
   static constexpr int kWBytes = NB * kWBlockBytes;
   static constexpr int kQStages = NB == 1 ? 8 : 4;
   static constexpr int kWStages = NB == 1 ? 3 : 2;
-  // With 256-token tiles the activation tile of a k-step arrives as two 32-k halves (64-byte swizzle),
-  // each in its own ring slot and released as soon as the two k16 mmas that read it are done: the ring
-  // is bound by (copy latency + hold time) per slot, and half-size slots hold for half as long
-  // (measured +5 % at 256 tokens; smaller tiles lose more to the per-copy cost than they gain).
-  static constexpr int kXK = BT >= 256 ? 32 : 64;
+  // With 256-token tiles and two M-blocks the activation tile of a k-step arrives as two 32-k halves
+  // (64-byte swizzle), each in its own ring slot and released as soon as the mmas that read it are
+  // done: the ring is bound by (copy latency + hold time) per slot, and half-size slots hold for half
+  // as long (measured +5 %).  With fewer mmas per slot (smaller tiles, one M-block) the per-copy cost
+  // wins (measured -10 % for one M-block at 256 tokens).
+  static constexpr int kXK = (BT >= 256 && NB == 2) ? 32 : 64;
   static constexpr int kXSub = kBK / kXK;
   static constexpr int kXSlotBytes = BT * kXK * 2;
   static constexpr int kFixed = kWStages * kWBytes + kQStages * kQStage + 2048;
