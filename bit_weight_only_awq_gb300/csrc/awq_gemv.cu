@@ -54,6 +54,10 @@ constexpr int kConsumers = 8;                  // consumer warps, one 64-column 
 constexpr int kThreads = (kConsumers + 1) * 32;
 constexpr int kCtasPerSm = 2;                  // this call's CTA and the next call's
 constexpr int kStages = 3;
+// Polling pauses: the producer's empty-slot waits and the consumers' full-slot waits share their
+// schedulers with consumer warps that have arithmetic to issue.
+constexpr uint32_t kProducerSleepNs = 1000;
+constexpr uint32_t kConsumerSleepNs = 0;
 constexpr int kRows = 64;                      // rows per unit (a TMA box, half a quantization group)
 constexpr int kTileWords = 64;                 // packed words per tile row = 512 output columns
 constexpr int kTileCols = kTileWords * 8;
@@ -230,13 +234,24 @@ __device__ __forceinline__ void compute_stage(const StageRegs& sr, const GroupCo
 
 // Stages of a CTA's unit range: a stage is a whole quantization group (two 64-row units) when the
 // range holds both halves of it, else a lone unit.  Every role walks the same sequence.
+// Tile and row block are tracked incrementally (no division per stage).
 struct StageWalk {
-  int u, u1, RB;
-  __device__ __forceinline__ StageWalk(int u0_, int u1_, int RB_) : u(u0_), u1(u1_), RB(RB_) {}
+  int u, u1, RB, tile, rb;
+  __device__ __forceinline__ StageWalk(int u0_, int u1_, int RB_) : u(u0_), u1(u1_), RB(RB_) {
+    tile = u0_ / RB_;
+    rb = u0_ - tile * RB_;
+  }
   // units of the stage starting at u: 2 if u is group-aligned and u + 1 is in the range and tile
   __device__ __forceinline__ int units_here() const {
-    const int rb = u % RB;
     return (kUnitsPerStage == 2 && (rb & 1) == 0 && u + 1 < u1 && rb + 1 < RB) ? 2 : 1;
+  }
+  __device__ __forceinline__ void advance(int nh) {
+    u += nh;
+    rb += nh;
+    if (rb == RB) {
+      rb = 0;
+      ++tile;
+    }
   }
 };
 
@@ -327,9 +342,7 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       auto tx_bytes = [&](int nh) {
         return (uint32_t)(nh * (kUnitQBytes + kXBoxBytes) + (has_z ? kZBytes : 0) + kSBytes);
       };
-      auto issue_weights = [&](int st, int u, int nh) {
-        const int tile = u / RB;
-        const int rb = u - tile * RB;
+      auto issue_weights = [&](int st, int tile, int rb, int nh) {
         const int grp = rb / (kGroup / kRows);
         uint8_t* sb = smem + st * kStageBytes;
         for (int hh = 0; hh < nh; ++hh)
@@ -341,8 +354,7 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         // scales viewed as int32 pairs: 512 columns = one 256-pair box
         tma_load_2d(smem_u32(sb + kSOff), &tm_s, tile * (kTileCols / 2), grp, full_bar(st));
       };
-      auto issue_x = [&](int st, int u, int nh) {
-        const int rb = u % RB;
+      auto issue_x = [&](int st, int rb, int nh) {
         for (int hh = 0; hh < nh; ++hh)
           tma_load_2d(smem_u32(smem + st * kStageBytes + kXOff + hh * kXBoxBytes), &tm_x, (rb + hh) * kRows, 0,
                       full_bar(st));
@@ -350,28 +362,28 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       // the first stages' weights stream before the wait on the previous kernel
       StageWalk w(u0, u1, RB);
       int pre = 0;
-      int pre_u[kStages], pre_nh[kStages];
+      int pre_rb[kStages], pre_nh[kStages];
       while (pre < kStages && w.u < u1) {
         const int nh = w.units_here();
         mbar_arrive_tx(full_bar(pre), tx_bytes(nh));
-        issue_weights(pre, w.u, nh);
-        pre_u[pre] = w.u;
+        issue_weights(pre, w.tile, w.rb, nh);
+        pre_rb[pre] = w.rb;
         pre_nh[pre] = nh;
         ++pre;
-        w.u += nh;
+        w.advance(nh);
       }
       asm volatile("griddepcontrol.wait;" ::: "memory");
-      for (int i = 0; i < pre; ++i) issue_x(i, pre_u[i], pre_nh[i]);
+      for (int i = 0; i < pre; ++i) issue_x(i, pre_rb[i], pre_nh[i]);
       int issued = pre;
       for (; w.u < u1; ++issued) {
         const int st = issued % kStages;
         const uint32_t ph = (uint32_t)(issued / kStages) & 1u;
-        if (!wait_bounded(empty_bar(st), ph ^ 1u, abort_flag, err, 501)) break;
+        if (!wait_backoff(empty_bar(st), ph ^ 1u, abort_flag, err, 501, kProducerSleepNs)) break;
         const int nh = w.units_here();
         mbar_arrive_tx(full_bar(st), tx_bytes(nh));
-        issue_weights(st, w.u, nh);
-        issue_x(st, w.u, nh);
-        w.u += nh;
+        issue_weights(st, w.tile, w.rb, nh);
+        issue_x(st, w.rb, nh);
+        w.advance(nh);
       }
       // never leave the CTA with copies in flight: the last stages issued must have landed
       volatile int no_abort = 0;
@@ -389,24 +401,30 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     GroupConsts gc;                   // zero / scale constants of the current group (cached_grp)
     int cached_grp = -1;
     int i = 0;                        // stage counter, identical to the producer's
+    int cst = 0;                      // its ring slot (i % kStages) and phase ((i / kStages) & 1)
+    uint32_t cph = 0;
     StageWalk w(u0, u1, RB);
     while (w.u < u1) {
-      const int tile = w.u / RB;
-      const int seg_end = min(u1, (tile + 1) * RB);
+      const int tile = w.tile;
       float acc[4][4];
 #pragma unroll
       for (int b = 0; b < 4; ++b)
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[b][e] = 0.f;
       cached_grp = -1;  // a new tile: other columns
-      for (; w.u < seg_end; ++i) {
+      for (; w.u < u1 && w.tile == tile; ++i) {
         const int nh = w.units_here();
-        w.u += nh;
-        const int st = i % kStages;
-        const uint32_t ph = (uint32_t)(i / kStages) & 1u;
+        const int grp = w.rb / (kGroup / kRows);
+        w.advance(nh);
+        const int st = cst;
+        const uint32_t ph = cph;
+        if (++cst == kStages) {
+          cst = 0;
+          cph ^= 1u;
+        }
         const uint8_t* sb = smem + st * kStageBytes;
-        const int grp = (w.u - nh - tile * RB) / (kGroup / kRows);
-        const bool ok = wait_bounded(full_bar(st), ph, abort_flag, err, 503);
+        const bool ok = kConsumerSleepNs ? wait_backoff(full_bar(st), ph, abort_flag, err, 503, kConsumerSleepNs)
+                                         : wait_bounded(full_bar(st), ph, abort_flag, err, 503);
         if (ok && grp != cached_grp) {  // a stage never spans two groups
           const uint32_t zword = has_z ? reinterpret_cast<const uint32_t*>(sb + kZOff)[word] : 0x88888888u;
           group_consts(zword, reinterpret_cast<const uint4*>(sb + kSOff)[word], gc);

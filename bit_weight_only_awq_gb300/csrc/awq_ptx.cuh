@@ -53,6 +53,31 @@ __device__ __noinline__ bool wait_bounded_slow(uint32_t bar, uint32_t parity, vo
     }
   }
 }
+// Bounded wait that sleeps `sleep_ns` between polls: for a thread that shares its scheduler with
+// warps that have work and does not need to react within nanoseconds (a copy producer refilling a
+// ring several microseconds deep), so that its polling does not take their issue slots.
+__device__ __noinline__ bool wait_backoff_slow(uint32_t bar, uint32_t parity, volatile int* abort, int* err, int id,
+                                               uint32_t sleep_ns) {
+  const long long t0 = now_ns();
+  for (uint32_t spin = 1;; ++spin) {
+    if (mbar_try(bar, parity)) return true;
+    __nanosleep(sleep_ns);
+    if ((spin & 15u) == 0) {
+      if (*abort) return false;
+      if (now_ns() - t0 > kWaitLimitNs) {
+        if (err) atomicExch(err, id);
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+__device__ __forceinline__ bool wait_backoff(uint32_t bar, uint32_t parity, volatile int* abort, int* err, int id,
+                                             uint32_t sleep_ns) {
+  if (mbar_try(bar, parity)) return true;
+  return wait_backoff_slow(bar, parity, abort, err, id, sleep_ns);
+}
+
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort, int* err, int id) {
   if (mbar_try(bar, parity)) return true;  // fast path stays inline
   return wait_bounded_slow(bar, parity, abort, err, id);
