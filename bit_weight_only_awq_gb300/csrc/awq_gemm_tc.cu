@@ -229,37 +229,53 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     }
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer
+    // One thread shares its scheduler with four busy dequant warps, and with narrow token tiles its
+    // mmas are short, so the loop keeps per-mma work to 64-bit adds on precomputed descriptors (the
+    // start address is the low field, in 16-byte units) and tracks ring slots without division.
     if (lane == 0) {
       bool ok = true;
+      const uint64_t adesc0 = smem_desc_sw128(smem_u32(wring), 1024, 2048);
+      const uint64_t bdesc0 =
+          C::kXK == 32 ? smem_desc_sw64(smem_u32(xring)) : smem_desc_sw128(smem_u32(xring), 16, 1024);
+      int ws = 0, xs = 0, chunk = 0, within = 0;
+      uint32_t wph = 0, xph = 0;
       for (int it = 0; it < nsteps && ok; ++it) {
-        const int ws = it % kWStages;
-        ok = wait_bounded(wready(ws), (uint32_t)(it / kWStages) & 1u, abort_flag, err, 202);
-        const uint32_t wa = smem_u32(wring + ws * kWBytes);
-        const int chunk = MODE == kModeW4A8 ? it / chunk_steps : 0;
-        const int within = MODE == kModeW4A8 ? it - chunk * chunk_steps : it;
+        ok = wait_bounded(wready(ws), wph, abort_flag, err, 202);
+        const uint64_t ad_s = adesc0 + (uint64_t)((ws * kWBytes) >> 4);
         for (int h = 0; h < C::kXSub && ok; ++h) {
-          const int j = it * C::kXSub + h;
-          const int xs = j % SX;
-          ok = wait_bounded(fullx(xs), (uint32_t)(j / SX) & 1u, abort_flag, err, 201);
+          ok = wait_bounded(fullx(xs), xph, abort_flag, err, 201);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t xa = smem_u32(xring + xs * C::kXSlotBytes);
+          const uint64_t bd_s = bdesc0 + (uint64_t)((xs * C::kXSlotBytes) >> 4);
 #pragma unroll
           for (int k2 = 0; k2 < C::kXK / 16; ++k2) {
             const int kk = h * (C::kXK / 16) + k2;
-            // B: activations, K-major; 16 k = 32 B inside the 64- or 128-byte swizzle row, 8-row groups
-            // 512 or 1024 B apart
-            const uint64_t bd = C::kXK == 32 ? smem_desc_sw64(xa + k2 * 32) : smem_desc_sw128(xa + k2 * 32, 16, 1024);
+            // B: activations, K-major; 16 k = 32 B inside the 64- or 128-byte swizzle row
+            const uint64_t bd = bd_s + (uint64_t)(k2 * 2);
 #pragma unroll
             for (int b = 0; b < NB; ++b) {
-              // A: weights of M-block b, MN-major; 64-column atoms 1024 B apart (LBO), 8-row k groups 2048 B apart (SBO)
-              const uint64_t ad = smem_desc_sw128(wa + b * kWBlockBytes + kk * 2 * 2048, 1024, 2048);
+              // A: weights of M-block b, MN-major; 64-column atoms 1024 B apart (LBO), 8-row k groups
+              // 2048 B apart (SBO); k16 step kk starts 4096 B further
+              const uint64_t ad = ad_s + (uint64_t)((b * kWBlockBytes + kk * 4096) >> 4);
               mma_f16(tmem + (uint32_t)((chunk * NB + b) * BT), ad, bd, C::kIdesc, (within > 0 || kk > 0) ? 1u : 0u);
             }
           }
-          mma_commit(emptyx(xs));  // this half of the activation tile is free once its mmas have read it
+          mma_commit(emptyx(xs));  // this part of the activation tile is free once its mmas have read it
+          if (++xs == SX) {
+            xs = 0;
+            xph ^= 1u;
+          }
         }
         if (ok) mma_commit(wempty(ws));
+        if (++ws == kWStages) {
+          ws = 0;
+          wph ^= 1u;
+        }
+        ++within;  // k-steps accumulated into the current chunk (W4A16: one chunk)
+        if (MODE == kModeW4A8 && within == chunk_steps) {
+          within = 0;
+          ++chunk;
+        }
       }
       mma_commit(accf_bar);  // arrives once every issued mma has completed
       volatile int no_abort = 0;
