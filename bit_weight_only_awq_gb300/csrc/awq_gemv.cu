@@ -75,7 +75,8 @@ constexpr int kXOff = kQBytes;
 constexpr int kZOff = kXOff + kXBytes;
 constexpr int kSOff = kZOff + kZBytes;
 constexpr int kStageBytes = ((kSOff + kSBytes) + 1023) / 1024 * 1024;
-constexpr int kSmemBytes = kStages * kStageBytes + 256 + 1024;
+constexpr int kTicketBatch = 32;               // shared tiles whose tickets are taken together
+constexpr int kSmemBytes = kStages * kStageBytes + 512 + 1024;  // ring | barriers, flags, tile table
 static_assert(kSmemBytes * kCtasPerSm <= 227 * 1024 - 2048, "shared memory budget: two CTAs per SM");
 static_assert(kTileWords == kConsumers * 8, "one 8-word slice per consumer warp");
 
@@ -255,42 +256,57 @@ struct StageWalk {
   }
 };
 
-// Sum of the tile's partials in contributor order, rounded once to fp16 (run by the last contributor).
-__device__ __forceinline__ void reduce_tile(const float* __restrict__ part, __half* __restrict__ y, int tile,
-                                            int nt, int maxc, int M, int N, int tid, int nthreads) {
-  const float4* base = reinterpret_cast<const float4*>(part + (size_t)tile * maxc * kGemvMaxM * kTileCols);
+// Sums of the partials of the `nl` tiles in `tiles` (contributor counts `nts`), each in contributor
+// order and rounded once to fp16; run by the last contributor of those tiles.  Work items are
+// (tile, 4-column quad, token) over all tiles of the table, two per thread and eight contributors per
+// step: sixteen 16-byte loads in flight.
+__device__ __forceinline__ void reduce_tiles(const float* __restrict__ part, __half* __restrict__ y,
+                                             const int* tiles, const int* nts, int nl, int maxc, int M, int N,
+                                             int tid, int nthreads) {
   constexpr int kQuads = kTileCols / 4;
   constexpr size_t kSlotQuads = (size_t)kGemvMaxM * kQuads;
-  // two quads per thread and eight contributors per step: sixteen 16-byte loads in flight
-  for (int q0 = tid; q0 < M * kQuads; q0 += 2 * nthreads) {
-    const int q1 = q0 + nthreads;
-    const bool has1 = q1 < M * kQuads;
-    float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0;
-    for (int j0 = 0; j0 < nt; j0 += 8) {
-      float4 v0[8], v1[8];
+  const int per_tile = M * kQuads;
+  const int items = nl * per_tile;
+  for (int i0 = tid; i0 < items; i0 += 2 * nthreads) {
+    int tile[2], nt[2], q[2];
+    bool has[2];
+    const float4* base[2];
 #pragma unroll
-      for (int jj = 0; jj < 8; ++jj) {
-        const bool in = j0 + jj < nt;
-        v0[jj] = in ? __ldcg(base + (size_t)(j0 + jj) * kSlotQuads + q0) : make_float4(0.f, 0.f, 0.f, 0.f);
-        v1[jj] = (in && has1) ? __ldcg(base + (size_t)(j0 + jj) * kSlotQuads + q1) : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
+    for (int k = 0; k < 2; ++k) {
+      const int i = i0 + k * nthreads;
+      has[k] = i < items;
+      const int tk = has[k] ? i / per_tile : 0;
+      tile[k] = tiles[tk];
+      nt[k] = has[k] ? nts[tk] : 0;
+      q[k] = i - tk * per_tile;
+      base[k] = reinterpret_cast<const float4*>(part + (size_t)tile[k] * maxc * kGemvMaxM * kTileCols);
+    }
+    float4 s[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+    const int ntmax = max(nt[0], nt[1]);
+    for (int j0 = 0; j0 < ntmax; j0 += 8) {
+      float4 v[2][8];
 #pragma unroll
-      for (int jj = 0; jj < 8; ++jj) {
-        s0.x += v0[jj].x; s0.y += v0[jj].y; s0.z += v0[jj].z; s0.w += v0[jj].w;
-        s1.x += v1[jj].x; s1.y += v1[jj].y; s1.z += v1[jj].z; s1.w += v1[jj].w;
-      }
+      for (int k = 0; k < 2; ++k)
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj)
+          v[k][jj] = j0 + jj < nt[k] ? __ldcg(base[k] + (size_t)(j0 + jj) * kSlotQuads + q[k])
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < 2; ++k)
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          s[k].x += v[k][jj].x; s[k].y += v[k][jj].y; s[k].z += v[k][jj].z; s[k].w += v[k][jj].w;
+        }
     }
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
-      const int q = k ? q1 : q0;
-      if (k && !has1) break;
-      const float4 sv = k ? s1 : s0;
-      const int m = q / kQuads;
-      const int n = tile * kTileCols + (q - m * kQuads) * 4;
+      if (!has[k]) continue;
+      const int m = q[k] / kQuads;
+      const int n = tile[k] * kTileCols + (q[k] - m * kQuads) * 4;
       if (n < N) {  // N % 32 == 0: all four outputs are in range
         __half2* dst = reinterpret_cast<__half2*>(y + (size_t)m * N + n);
-        dst[0] = __floats2half2_rn(sv.x, sv.y);
-        dst[1] = __floats2half2_rn(sv.z, sv.w);
+        dst[0] = __floats2half2_rn(s[k].x, s[k].y);
+        dst[1] = __floats2half2_rn(s[k].z, s[k].w);
       }
     }
   }
@@ -310,7 +326,9 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kStages);
-  int* last_flag = reinterpret_cast<int*>(bars + 2 * kStages) + 1;
+  int* last_flag = reinterpret_cast<int*>(bars + 2 * kStages) + 1;  // number of tiles in the table
+  int* last_tile = last_flag + 1;                                  // [kTicketBatch] tiles this CTA completes
+  int* last_nt = last_tile + kTicketBatch;                         // [kTicketBatch] their contributor counts
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -471,23 +489,44 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       }
     }
 
-    // ---- tickets of the shared tiles, after the whole range: one fence for all partials
+    // ---- tickets of the shared tiles, after the whole range: one fence for all partials, the
+    // tickets of up to kTicketBatch tiles taken back to back, and the tiles this CTA completes
+    // reduced together by all consumer threads
     if (shared_tiles) {
       __threadfence();
       consumers_sync();
-      for (int tile = u0 / RB; tile <= (u1 - 1) / RB; ++tile) {
-        const int pf = (int)cta_of_unit(tile * RB, units, P);
-        const int pl = (int)cta_of_unit((tile + 1) * RB - 1, units, P);
-        if (pf == pl) continue;
-        const int nt = pl - pf + 1;
-        if (threadIdx.x == 0) *last_flag = (atomicAdd(counters + tile, 1) == nt - 1);
-        consumers_sync();
-        if (*last_flag) {
-          __threadfence();
-          reduce_tile(part, y, tile, nt, maxc, M, N, threadIdx.x, kConsumers * 32);
-          if (threadIdx.x == 0) atomicExch(counters + tile, 0);  // leave the ticket at zero for the next call
+      const int tlast = (u1 - 1) / RB;
+      for (int tb = u0 / RB; tb <= tlast; tb += kTicketBatch) {
+        const int te = min(tlast + 1, tb + kTicketBatch);
+        if (threadIdx.x == 0) {
+          int tk[kTicketBatch];
+          for (int tile = tb; tile < te; ++tile) {
+            const int pf = (int)cta_of_unit(tile * RB, units, P);
+            const int pl = (int)cta_of_unit((tile + 1) * RB - 1, units, P);
+            tk[tile - tb] = pf == pl ? -1 : atomicAdd(counters + tile, 1);
+          }
+          int nl = 0;
+          for (int tile = tb; tile < te; ++tile) {
+            if (tk[tile - tb] < 0) continue;
+            const int nt = (int)(cta_of_unit((tile + 1) * RB - 1, units, P) - cta_of_unit(tile * RB, units, P)) + 1;
+            if (tk[tile - tb] == nt - 1) {
+              last_tile[nl] = tile;
+              last_nt[nl] = nt;
+              ++nl;
+            }
+          }
+          *last_flag = nl;
         }
-        consumers_sync();  // last_flag is reused by the next tile
+        consumers_sync();
+        const int nl = *last_flag;
+        if (nl > 0) {
+          __threadfence();
+          reduce_tiles(part, y, last_tile, last_nt, nl, maxc, M, N, threadIdx.x, kConsumers * 32);
+          consumers_sync();
+          // leave the tickets at zero for the next call
+          if (threadIdx.x < nl) atomicExch(counters + last_tile[threadIdx.x], 0);
+        }
+        consumers_sync();  // the tile table is reused by the next batch
       }
     }
   }
