@@ -44,6 +44,7 @@ _SIGS = {
     "w4a8_quant_act": (_i32, [_p, _p, _p, _i64, _i64, _p]),
     "w4a8_gemm": (_i32, [_p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _i32, _p, _sz, _p]),
     "awq_last_device_error": (_i32, [ctypes.POINTER(_i32)]),
+    "awq_selftest_wait_timeout": (_i32, [_i64, _p]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(lib, _name)
@@ -200,3 +201,8 @@ def awq_last_device_error() -> int:
     if status not in (0, -5):
         raise AwqError("awq_last_device_error", status)
     return int(code.value)
+
+
+def awq_selftest_wait_timeout(limit_ns: int = 1_000_000, stream=None) -> None:
+    """Run one bounded device wait that expires after `limit_ns` (see include/awq.h)."""
+    _check("awq_selftest_wait_timeout", lib.awq_selftest_wait_timeout(int(limit_ns), _stream(stream)))

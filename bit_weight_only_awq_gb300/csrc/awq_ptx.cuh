@@ -39,13 +39,14 @@ __device__ __forceinline__ long long now_ns() {
 // Bounded wait on an mbarrier phase.  Gives up when `abort` is raised by another
 // thread or after kWaitLimitNs; a timeout records `id` in the device error word
 // and raises `abort`.  Returns true when the phase completed.
-__device__ __noinline__ bool wait_bounded_slow(uint32_t bar, uint32_t parity, volatile int* abort, int* err, int id) {
+__device__ __noinline__ bool wait_bounded_slow(uint32_t bar, uint32_t parity, volatile int* abort, int* err, int id,
+                                               long long limit_ns = kWaitLimitNs) {
   const long long t0 = now_ns();
   for (uint32_t spin = 1;; ++spin) {
     if (mbar_try(bar, parity)) return true;
     if ((spin & 255u) == 0) {
       if (*abort) return false;
-      if (now_ns() - t0 > kWaitLimitNs) {
+      if (now_ns() - t0 > limit_ns) {
         if (err) atomicExch(err, id);
         *abort = 1;
         return false;

@@ -198,6 +198,19 @@ awq_status w4a8_gemm(const int8_t *xq, const float *s_tok, const int32_t *wq,
  */
 awq_status awq_last_device_error(int32_t *code);
 
+/*
+ * awq_selftest_wait_timeout -- runs, on `stream`, one bounded device-side wait on
+ * an mbarrier that nothing arrives on, with a limit of `limit_ns` nanoseconds
+ * (0 < limit_ns <= 2e9) instead of the kernels' 2 s.  The wait expires, records
+ * id 901 in the device error word and returns; awq_last_device_error() then
+ * reports AWQ_ETIMEOUT with code 901, and the context stays usable.  It lets a
+ * caller (and the tests) check the failure path of every kernel's waits without
+ * faulting or hanging the GPU.  No source passage: the pages describe no
+ * failure handling.  Returns AWQ_EINVAL for a limit outside the range,
+ * AWQ_EARCH off sm_103, AWQ_ECUDA when the launch fails.
+ */
+awq_status awq_selftest_wait_timeout(int64_t limit_ns, awq_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

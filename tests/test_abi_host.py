@@ -116,6 +116,12 @@ def test_workspace_layout(awq):
     assert awq.awq_workspace_bytes(awq.OP_GEMM, 16, 100, 4096, 0) == 0
 
 
+def test_selftest_rejects_bad_limits_before_launch(awq):
+    assert awq.lib.awq_selftest_wait_timeout(0, None) == EINVAL
+    assert awq.lib.awq_selftest_wait_timeout(-5, None) == EINVAL
+    assert awq.lib.awq_selftest_wait_timeout(3_000_000_000, None) == EINVAL
+
+
 def test_binding_has_no_fallback(awq):
     src = open(awq.__file__).read()
     assert "oracle" not in src
