@@ -40,7 +40,7 @@ def test_expired_wait_is_reported_and_the_context_stays_usable(awq):
                      torch.from_numpy(p["qzeros"]).cuda(), torch.from_numpy(p["scales"]).cuda(), 128)
     got = y.cpu().numpy().astype(np.float64)
     ref = oracle.awq_linear(p["x"], p["qweight"], p["qzeros"], p["scales"], 128)
-    assert np.max(np.abs(got - ref)) <= 2e-3 * np.sqrt(np.mean(ref ** 2))
+    assert np.max(np.abs(got - ref) - 2.0 ** -11 * np.abs(ref)) <= 2e-3 * np.sqrt(np.mean(ref ** 2))
     assert awq.awq_last_device_error() == 0
 
 

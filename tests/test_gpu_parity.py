@@ -3,8 +3,10 @@
 Bars (written here, derived in the design doc):
 * packing, unpacking, dequantized weights, W4A8 codes / scales / int32 accumulators
   and W4A8 fp16 outputs: bit-exact;
-* W4A16 fp16 outputs (GEMV, GEMM): max |y_gpu - y_oracle| <= 2e-3 * rms(y_oracle),
-  with y_oracle the unrounded float64 product of the oracle's fp16 weights.
+* W4A16 fp16 outputs (GEMV, GEMM): |y_gpu - y_oracle| <= 2e-3 * rms(y_oracle) + 2^-11 |y_oracle|
+  element by element, with y_oracle the unrounded float64 product of the oracle's fp16 weights:
+  the 2e-3 * rms budget is for the computation, and the fp16 output format adds its own rounding of
+  at most half an ulp (2^-11 relative), which alone can exceed 2e-3 * rms on the largest outputs.
 Small cases cover several tiles and ragged tails; full workload shapes are checked
 on seeded column / row samples that the oracle computes one by one.
 """
@@ -40,12 +42,15 @@ def host(t):
     return t.cpu().numpy()
 
 
+FP16_HALF_ULP = 2.0 ** -11  # relative rounding bound of an fp16 output
+
+
 def assert_within_tol(y_gpu16, ref64, what=""):
     y = y_gpu16.astype(np.float64)
     rms = np.sqrt(np.mean(ref64 ** 2))
-    err = np.max(np.abs(y - ref64))
+    err = np.max(np.abs(y - ref64) - FP16_HALF_ULP * np.abs(ref64))
     assert np.all(np.isfinite(y)), what
-    assert err <= TOL * rms, f"{what}: max err {err:.3e} > {TOL} * rms {rms:.3e}"
+    assert err <= TOL * rms, f"{what}: max err beyond the output rounding {err:.3e} > {TOL} * rms {rms:.3e}"
 
 
 def oracle_columns(p, word_cols):

@@ -61,7 +61,8 @@ def test_noalloc_matches_gemv_on_two_calls_in_a_row(awq, M, K, N, split_k, symme
         torch.cuda.synchronize()
         got = y.cpu().numpy().astype(np.float64)
         assert np.all(np.isfinite(got))
-        assert np.max(np.abs(got - ref)) <= TOL * rms
+        # both outputs are fp16: each carries its own output rounding (half an ulp, 2^-11 relative)
+        assert np.max(np.abs(got - ref) - 2 * 2.0 ** -11 * np.abs(ref)) <= TOL * rms
 
 
 def test_noalloc_rejects_a_split_whose_scratch_exceeds_the_array(awq):
