@@ -438,7 +438,7 @@ def main():
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_value, 2), "unit": unit, "h2d_bytes_per_step": r["h2d"],
-                    "d2h_bytes_per_step": r["d2h"], "path": "python binding, one call per GEMV, pinned copies"},
+                    "d2h_bytes_per_step": r["d2h"], "path": "python binding, one API call per layer call of the step, pinned copies"},
             "gpu_launches": r["launches_per_step"] * args.steps,
             "clocks": r["clocks"],
         }

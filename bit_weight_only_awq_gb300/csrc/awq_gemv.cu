@@ -466,25 +466,42 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       }
       const int pf = (int)cta_of_unit(tile * RB, units, P);
       const int pl = (int)cta_of_unit((tile + 1) * RB - 1, units, P);
-      // D fragment: acc[b][0/1] = (column lo of byte b, tokens 2t / 2t+1), acc[b][2/3] = column hi
+      // D fragment: acc[b][0/1] = (slot 2b, tokens 2t / 2t+1), acc[b][2/3] = slot 2b+1: the lane holds
+      // all 8 columns of its word for tokens 2t and 2t+1, stored as one 16-byte (fp16) or two
+      // 16-byte (fp32) vectors per token
+      const int n0 = tile * kTileCols + word * 8;
       if (pf == pl) {
 #pragma unroll
-        for (int b = 0; b < 4; ++b)
+        for (int par = 0; par < 2; ++par) {
+          const int m = 2 * t + par;
+          if (m < M && n0 < N) {  // N % 32 == 0: the word's 8 columns are all in range
+            uint32_t h[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int m = 2 * t + (e & 1);
-            const int n = tile * kTileCols + word * 8 + order_map(2 * b + (e >> 1));
-            if (m < M && n < N) y[(size_t)m * N + n] = __float2half_rn(acc[b][e]);
+            for (int c = 0; c < 8; c += 2) {
+              const int s0 = slot_of_col(c), s1 = slot_of_col(c + 1);
+              __half2 v = __floats2half2_rn(acc[s0 >> 1][(s0 & 1) * 2 + par], acc[s1 >> 1][(s1 & 1) * 2 + par]);
+              h[c / 2] = *reinterpret_cast<uint32_t*>(&v);
+            }
+            *reinterpret_cast<uint4*>(y + (size_t)m * N + n0) = make_uint4(h[0], h[1], h[2], h[3]);
           }
+        }
       } else {
         float* slot = part + ((size_t)tile * maxc + (size_t)(p - pf)) * kGemvMaxM * kTileCols;
 #pragma unroll
-        for (int b = 0; b < 4; ++b)
+        for (int par = 0; par < 2; ++par) {
+          const int m = 2 * t + par;
+          if (m < M) {
+            float v[8];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int m = 2 * t + (e & 1);
-            if (m < M) slot[m * kTileCols + word * 8 + order_map(2 * b + (e >> 1))] = acc[b][e];
+            for (int c = 0; c < 8; ++c) {
+              const int sl = slot_of_col(c);
+              v[c] = acc[sl >> 1][(sl & 1) * 2 + par];
+            }
+            float4* dst = reinterpret_cast<float4*>(slot + m * kTileCols + word * 8);
+            dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+            dst[1] = make_float4(v[4], v[5], v[6], v[7]);
           }
+        }
         shared_tiles = true;
       }
     }
