@@ -9,15 +9,15 @@
 //    TMA stream reaches ~6.1 TB/s with 32 KB stages but only ~5.4 TB/s with 16 KB ones,
 //    whatever the ring depth; and a decode GEMV of a 7B-model layer moves only 8-47 MB,
 //    so per-call latency (first bytes, the cross-CTA reduction, the launch) matters as
-//    much as the streaming rate.  The kernel therefore uses at most half of an SM: one
-//    persistent CTA per SM per call, a producer warp streaming 36 KB stages (one whole
-//    quantization group: 128 rows x 512 columns of packed words as four
-//    128-byte-swizzled TMA boxes, the group's zero-point / scale rows and the 128
-//    activations of every token) through a 3-deep ring, and 8 consumer warps (one
-//    64-column slice each) that copy their share of a stage into registers 64 rows at a
-//    time and release the slot after the last copy.  The other half of every SM takes the
-//    next call's CTA, which programmatic dependent launch starts early: it streams its
-//    weights while this call finishes, so consecutive calls overlap their latencies.
+//    much as the streaming rate.  One persistent CTA per SM: a producer warp streams
+//    36 KB stages (one whole quantization group: 128 rows x 512 columns of packed words
+//    as four 128-byte-swizzled TMA boxes, the group's zero-point / scale rows and the
+//    128 activations of every token) through a 3-deep ring, and 8 consumer warps (one
+//    64-column slice each) copy their share of a stage into registers 64 rows at a time
+//    and release the slot after the last copy.  The registers are sized for one CTA per
+//    SM (the SM sub-partition holding the producer warp runs three warps); programmatic
+//    dependent launch starts the next call's CTA on an SM as soon as this call's CTA
+//    there exits, and it streams its first stages before waiting for this call.
 //  * Persistent, evenly balanced grid: the (512-column tile, 64-row block) units are cut
 //    into equal contiguous ranges, one per SM; a CTA's units are grouped into stages of
 //    one quantization group (or a lone 64-row block at a range edge).  A tile finished by
@@ -29,14 +29,20 @@
 //  * Programmatic dependent launch: the GEMV starts streaming its weights before waiting
 //    for the previous kernel, and touches activations, outputs and the workspace only
 //    after that wait.
-//  * The multiply runs on the tensor pipe: mma.sync m16n8k16 with the dequantized
-//    weights as the A operand (16 output columns x 16 k) and the activations as B
-//    (16 k x 8 tokens), fp32 accumulation.  The mma wants k-pairs in each 32-bit A
-//    register while a packed word holds 8 columns of one k, so a PRMT takes the same
-//    byte of two consecutive rows, and a LOP3 with the fp16 magic 0x6400 turns its low /
-//    high nibbles into (1024 + q) / (1024 + 16 q) halves.  HSUB2 of the zero (same
-//    magic) then HMUL2 by the scale (s, or s / 16 for the high nibble) give
-//    fp16_RN((q - z) * s), the same value the dequant kernel writes.
+//  * The multiply runs on the tensor pipe: mma.sync m16n8k16 with the packed weights as
+//    the A operand (16 output columns x 16 k) and the activations as B (16 k x 8 tokens),
+//    fp32 accumulation.  The mma wants k-pairs in each 32-bit A register while a packed
+//    word holds 8 columns of one k, so a PRMT takes the same byte of two consecutive rows,
+//    and a LOP3 with the fp16 magic 0x6400 turns its low / high nibbles into the exact
+//    halves 1024 + q / 1024 + 16 q.  Those enter the mma as they are: the group's zero
+//    point and scale are applied once per group and column to the fp32 sums, by linearity
+//        sum_k (q - z) s x = s (sum_k (1024 + q) x - (1024 + z) sum_k x)
+//    (high nibble: s / 16 and 1024 + 16 z), with sum_k x from one more mma against an
+//    all-ones A.  This drops the two fp16 operations per weight pair that dominated the
+//    issue slots; the price is that the products use s (q - z) in fp32 instead of its
+//    fp16 rounding, a relative difference of at most 2^-11 per weight, far inside the
+//    output tolerance, and a cancellation of the 1024 offsets in fp32 that costs about
+//    eight of its 24 bits.
 //  * Lane (g, t) of the mma reads rows 2t, 2t+1 (+8) of each 16-row step; with the
 //    128-byte swizzle those 32-bit shared-memory loads, and the activation loads, are
 //    free of bank conflicts, and every address is a lane constant plus an immediate.
@@ -52,7 +58,6 @@ namespace {
 
 constexpr int kConsumers = 8;                  // consumer warps, one 64-column slice of the tile each
 constexpr int kThreads = (kConsumers + 1) * 32;
-constexpr int kCtasPerSm = 2;                  // this call's CTA and the next call's
 constexpr int kStages = 3;
 // Polling pauses: the producer's empty-slot waits and the consumers' full-slot waits share their
 // schedulers with consumer warps that have arithmetic to issue.
@@ -77,7 +82,7 @@ constexpr int kSOff = kZOff + kZBytes;
 constexpr int kStageBytes = ((kSOff + kSBytes) + 1023) / 1024 * 1024;
 constexpr int kTicketBatch = 32;               // shared tiles whose tickets are taken together
 constexpr int kSmemBytes = kStages * kStageBytes + 512 + 1024;  // ring | barriers, flags, tile table
-static_assert(kSmemBytes * kCtasPerSm <= 227 * 1024 - 2048, "shared memory budget: two CTAs per SM");
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget of one CTA");
 static_assert(kTileWords == kConsumers * 8, "one 8-word slice per consumer warp");
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
@@ -94,14 +99,6 @@ __device__ __forceinline__ uint32_t magic(uint32_t a) {
   return d;
 }
 
-__device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
-  __half2 r = __hsub2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
-  return *reinterpret_cast<uint32_t*>(&r);
-}
-__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
-  __half2 r = __hmul2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
-  return *reinterpret_cast<uint32_t*>(&r);
-}
 
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
@@ -114,12 +111,6 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
 // PRMT selector: byte b of operand a -> result bytes 0,1; byte b of operand b -> bytes 2,3.
 __device__ __forceinline__ constexpr uint32_t byte_sel(int b) {
   return (uint32_t)(b | (b << 4) | ((b + 4) << 8) | ((b + 4) << 12));
-}
-
-// Broadcast fp16 number `idx` (0..7) of an 8-half vector into both halves.
-__device__ __forceinline__ uint32_t bcast_half(const uint4& v, int idx) {
-  const uint32_t w = idx < 2 ? v.x : idx < 4 ? v.y : idx < 6 ? v.z : v.w;
-  return (idx & 1) ? prmt(w, w, 0x3232u) : prmt(w, w, 0x1010u);
 }
 
 __device__ __forceinline__ void consumers_sync() {  // the consumer warps only (named barrier 1)
@@ -178,27 +169,32 @@ __device__ __forceinline__ void load_stage(const uint8_t* sb, int hh, const Lane
   }
 }
 
-// Zero-point / scale constants of this lane's packed word for one quantization group:
-// zlo / zhi = 1024 + z and 1024 + 16 z of slots 2b / 2b + 1 (both halves), slo / shi = s and s / 16.
+// Zero-point / scale constants of this lane's packed word for one quantization group, as the fp32
+// factors of the fold: sf[b] = s and s / 16 of slots 2b / 2b + 1 (low / high nibble of byte b), and
+// szc[b] = sf times the magic-offset zero point, 1024 + z and 1024 + 16 z.
 struct GroupConsts {
-  uint32_t zlo[4], zhi[4], slo[4], shi[4];
+  float sf[4][2], szc[4][2];
 };
 
 __device__ __forceinline__ void group_consts(uint32_t zword, const uint4& sv, GroupConsts& c) {
 #pragma unroll
   for (int b = 0; b < 4; ++b) {
-    const uint32_t zb = prmt(zword, zword, byte_sel(b));
-    c.zlo[b] = magic<0x000F000Fu>(zb);  // 1024 + z(slot 2b)
-    c.zhi[b] = magic<0x00F000F0u>(zb);  // 1024 + 16 z(slot 2b+1)
-    c.slo[b] = bcast_half(sv, order_map(2 * b));
-    c.shi[b] = hmul2(bcast_half(sv, order_map(2 * b + 1)), 0x2C002C00u);  // s / 16, exact
+    const float zl = (float)((zword >> (8 * b)) & 15u) + 1024.f;
+    const float zh = (float)((zword >> (8 * b + 4)) & 15u) * 16.f + 1024.f;
+    const __half* sh = reinterpret_cast<const __half*>(&sv);
+    c.sf[b][0] = __half2float(sh[order_map(2 * b)]);
+    c.sf[b][1] = __half2float(sh[order_map(2 * b + 1)]) * 0.0625f;  // s / 16, exact
+    c.szc[b][0] = c.sf[b][0] * zl;
+    c.szc[b][1] = c.sf[b][1] * zh;
   }
 }
 
-// acc += W^T x over the 64 rows held in `sr` (this lane's packed word column, 8 tokens).  Each
-// 16-row step is written as phases over its four independent byte positions (PRMT, LOP3, HSUB2,
-// HMUL2, mma) so that no instruction waits on the one issued just before it.
-__device__ __forceinline__ void compute_stage(const StageRegs& sr, const GroupConsts& c, float (&acc)[4][4]) {
+// Over the 64 rows held in `sr` (this lane's packed word column, 8 tokens): acc += (1024 + q)^T x
+// (1024 + 16 q for the high nibbles) and sx += sum_k x, the latter as an mma against an all-ones A
+// so that it lands in the accumulator layout.  Each 16-row step is written as phases over its four
+// independent byte positions (PRMT, LOP3, mma) so that no instruction waits on the one issued just
+// before it.
+__device__ __forceinline__ void compute_stage(const StageRegs& sr, float (&acc)[4][4], float (&sx)[4]) {
 #pragma unroll
   for (int it = 0; it < 4; ++it) {
     uint32_t p01[4], p23[4], a[4][4];
@@ -215,21 +211,8 @@ __device__ __forceinline__ void compute_stage(const StageRegs& sr, const GroupCo
       a[b][3] = magic<0x00F000F0u>(p23[b]);
     }
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      a[b][0] = hsub2(a[b][0], c.zlo[b]);
-      a[b][1] = hsub2(a[b][1], c.zhi[b]);
-      a[b][2] = hsub2(a[b][2], c.zlo[b]);
-      a[b][3] = hsub2(a[b][3], c.zhi[b]);
-    }
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      a[b][0] = hmul2(a[b][0], c.slo[b]);
-      a[b][1] = hmul2(a[b][1], c.shi[b]);
-      a[b][2] = hmul2(a[b][2], c.slo[b]);
-      a[b][3] = hmul2(a[b][3], c.shi[b]);
-    }
-#pragma unroll
     for (int b = 0; b < 4; ++b) mma16816(acc[b], a[b][0], a[b][1], a[b][2], a[b][3], sr.b[it][0], sr.b[it][1]);
+    mma16816(sx, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u, sr.b[it][0], sr.b[it][1]);
   }
 }
 
@@ -312,9 +295,10 @@ __device__ __forceinline__ void reduce_tiles(const float* __restrict__ part, __h
   }
 }
 
-// Register cap that still lets two CTAs share an SM (a launch-bounds hint made the compiler stop at 96
-// and spill).
-constexpr int kMaxRegs = (65536 / (kThreads * kCtasPerSm)) / 8 * 8;
+// Register cap for one CTA per SM: the 288 threads are 9 warps, so one SM sub-partition (a quarter of
+// the 64 K registers) holds three of them.
+constexpr int kMaxRegs = (65536 / 4) / (((kThreads / 32 + 3) / 4) * 32) / 8 * 8;
+static_assert(kMaxRegs == 168, "9 warps: three on one sub-partition");
 
 __global__ void __maxnreg__(kMaxRegs)
 gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_x,
@@ -416,6 +400,7 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     const LaneOffsets lo = lane_offsets(word, g, t);
     bool waited = false;
     bool shared_tiles = false;        // any tile of this range also computed by another CTA
+    bool failed = false;              // a wait ran out: error recorded, the rest of the call skipped
     GroupConsts gc;                   // zero / scale constants of the current group (cached_grp)
     int cached_grp = -1;
     int i = 0;                        // stage counter, identical to the producer's
@@ -443,21 +428,39 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         const uint8_t* sb = smem + st * kStageBytes;
         const bool ok = kConsumerSleepNs ? wait_backoff(full_bar(st), ph, abort_flag, err, 503, kConsumerSleepNs)
                                          : wait_bounded(full_bar(st), ph, abort_flag, err, 503);
-        if (ok && grp != cached_grp) {  // a stage never spans two groups
+        if (!ok) {  // error recorded; this CTA's outputs and tickets are abandoned
+          failed = true;
+          break;
+        }
+        if (grp != cached_grp) {  // a stage never spans two groups
           const uint32_t zword = has_z ? reinterpret_cast<const uint32_t*>(sb + kZOff)[word] : 0x88888888u;
           group_consts(zword, reinterpret_cast<const uint4*>(sb + kSOff)[word], gc);
           cached_grp = grp;
         }
-        for (int hh = 0; hh < nh; ++hh) {
-          StageRegs sr;
-          if (ok) load_stage(sb, hh, lo, sr);
-          if (hh == nh - 1) {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(empty_bar(st));  // slot free before the last unit's arithmetic
-          }
-          if (ok) compute_stage(sr, gc, acc);
+        float gacc[4][4], sx[4];  // this stage's (1024 + q)^T x and sum_k x
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          sx[b] = 0.f;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) gacc[b][e] = 0.f;
         }
+        StageRegs sr;
+        load_stage(sb, 0, lo, sr);
+        if (nh == 2) {
+          compute_stage(sr, gacc, sx);
+          load_stage(sb, 1, lo, sr);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_bar(st));  // slot free before the last unit's arithmetic
+        compute_stage(sr, gacc, sx);
+        // the group's zero point and scale: acc += s (gacc - (1024 + z) sx)  (high nibble: s / 16, 1024 + 16 z)
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            acc[b][e] = fmaf(gacc[b][e], gc.sf[b][e >> 1], fmaf(-gc.szc[b][e >> 1], sx[e & 1], acc[b][e]));
       }
+      if (failed) break;
 
       // ---- flush: this warp owns its 64 columns; CTAs sharing the tile meet in the workspace
       if (!waited) {
@@ -509,7 +512,7 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     // ---- tickets of the shared tiles, after the whole range: one fence for all partials, the
     // tickets of up to kTicketBatch tiles taken back to back, and the tiles this CTA completes
     // reduced together by all consumer threads
-    if (shared_tiles) {
+    if (shared_tiles && !failed) {
       __threadfence();
       consumers_sync();
       const int tlast = (u1 - 1) / RB;

@@ -133,6 +133,26 @@ def test_gemv_llama2_shapes_sampled(awq, name, K, N, M):
     assert_within_tol(y[:, cols], ref, f"gemv {name} M={M}")
 
 
+@pytest.mark.parametrize("xkind", ["positive_offset", "common_mode", "outliers"])
+@pytest.mark.parametrize("M", [1, 8])
+def test_gemv_activation_offsets(awq, M, xkind):
+    # The decode kernel applies each group's zero point and scale to fp32 sums of (1024 + q) x, so
+    # activations with a large common component cancel the most bits; they stay inside the tolerance.
+    p = synth.awq_problem(M, 4096, 1024, seed=300 + M)
+    rng = np.random.default_rng(301 + M)
+    z = rng.standard_normal((M, 4096))
+    if xkind == "positive_offset":
+        x = np.abs(z) + 2.0
+    elif xkind == "common_mode":
+        x = 20.0 + 0.1 * z
+    else:
+        x = z * np.where(rng.random((M, 4096)) < 0.01, 100.0, 1.0)
+    p["x"] = x.astype(np.float16)
+    y = run_w4a16(awq, awq.awq_gemv, p)
+    ref = oracle.awq_linear(p["x"], p["qweight"], p["qzeros"], p["scales"], 128)
+    assert_within_tol(y, ref, f"gemv {xkind} M={M}")
+
+
 def test_gemv_repeatable_with_workspace_reuse(awq):
     p = synth.awq_problem(4, 4096, 4096, seed=77)
     y1 = run_w4a16(awq, awq.awq_gemv, p, 8)
