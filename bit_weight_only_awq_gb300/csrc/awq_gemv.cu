@@ -513,12 +513,12 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     // tickets of up to kTicketBatch tiles taken back to back, and the tiles this CTA completes
     // reduced together by all consumer threads
     if (shared_tiles && !failed) {
-      __threadfence();
-      consumers_sync();
+      consumers_sync();  // every partial of this CTA written (thread 0's fence below publishes them)
       const int tlast = (u1 - 1) / RB;
       for (int tb = u0 / RB; tb <= tlast; tb += kTicketBatch) {
         const int te = min(tlast + 1, tb + kTicketBatch);
         if (threadIdx.x == 0) {
+          __threadfence();
           int tk[kTicketBatch];
           for (int tile = tb; tile < te; ++tile) {
             const int pf = (int)cta_of_unit(tile * RB, units, P);
@@ -535,16 +535,16 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
               ++nl;
             }
           }
+          if (nl > 0) __threadfence();  // the other contributors' partials, before the barrier below
           *last_flag = nl;
         }
         consumers_sync();
         const int nl = *last_flag;
         if (nl > 0) {
-          __threadfence();
           reduce_tiles(part, y, last_tile, last_nt, nl, maxc, M, N, threadIdx.x, kConsumers * 32);
           consumers_sync();
           // leave the tickets at zero for the next call
-          if (threadIdx.x < nl) atomicExch(counters + last_tile[threadIdx.x], 0);
+          if (threadIdx.x < nl) reinterpret_cast<volatile int*>(counters)[last_tile[threadIdx.x]] = 0;
         }
         consumers_sync();  // the tile table is reused by the next batch
       }
