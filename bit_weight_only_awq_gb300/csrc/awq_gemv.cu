@@ -80,8 +80,8 @@ constexpr int kXOff = kQBytes;
 constexpr int kZOff = kXOff + kXBytes;
 constexpr int kSOff = kZOff + kZBytes;
 constexpr int kStageBytes = ((kSOff + kSBytes) + 1023) / 1024 * 1024;
-constexpr int kTicketBatch = 32;               // shared tiles whose tickets are taken together
-constexpr int kSmemBytes = kStages * kStageBytes + 512 + 1024;  // ring | barriers, flags, tile table
+constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 512;  // 1 KB alignment slack | ring | barriers, flags
+static_assert(kGemvMaxM * kTileCols * 4 <= kStageBytes, "a completer's own sums fit one ring slot");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget of one CTA");
 static_assert(kTileWords == kConsumers * 8, "one 8-word slice per consumer warp");
 
@@ -115,6 +115,13 @@ __device__ __forceinline__ constexpr uint32_t byte_sel(int b) {
 
 __device__ __forceinline__ void consumers_sync() {  // the consumer warps only (named barrier 1)
   asm volatile("bar.sync 1, %0;" ::"r"(kConsumers * 32) : "memory");
+}
+// consumers_sync that also returns whether `v` holds in any consumer thread
+__device__ __forceinline__ bool consumers_any(bool v) {
+  uint32_t r;
+  asm volatile("{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 1, %2, p;\n selp.u32 %0, 1, 0, q;\n}"
+               : "=r"(r) : "r"((uint32_t)v), "r"(kConsumers * 32) : "memory");
+  return r != 0;
 }
 
 // 32-bit word `word` (0..63) of packed row `row` (0..127) in the stage tile: 128-byte-swizzled
@@ -239,62 +246,6 @@ struct StageWalk {
   }
 };
 
-// Sums of the partials of the `nl` tiles in `tiles` (contributor counts `nts`), each in contributor
-// order and rounded once to fp16; run by the last contributor of those tiles.  Work items are
-// (tile, 4-column quad, token) over all tiles of the table, two per thread and eight contributors per
-// step: sixteen 16-byte loads in flight.
-__device__ __forceinline__ void reduce_tiles(const float* __restrict__ part, __half* __restrict__ y,
-                                             const int* tiles, const int* nts, int nl, int maxc, int M, int N,
-                                             int tid, int nthreads) {
-  constexpr int kQuads = kTileCols / 4;
-  constexpr size_t kSlotQuads = (size_t)kGemvMaxM * kQuads;
-  const int per_tile = M * kQuads;
-  const int items = nl * per_tile;
-  for (int i0 = tid; i0 < items; i0 += 2 * nthreads) {
-    int tile[2], nt[2], q[2];
-    bool has[2];
-    const float4* base[2];
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const int i = i0 + k * nthreads;
-      has[k] = i < items;
-      const int tk = has[k] ? i / per_tile : 0;
-      tile[k] = tiles[tk];
-      nt[k] = has[k] ? nts[tk] : 0;
-      q[k] = i - tk * per_tile;
-      base[k] = reinterpret_cast<const float4*>(part + (size_t)tile[k] * maxc * kGemvMaxM * kTileCols);
-    }
-    float4 s[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
-    const int ntmax = max(nt[0], nt[1]);
-    for (int j0 = 0; j0 < ntmax; j0 += 8) {
-      float4 v[2][8];
-#pragma unroll
-      for (int k = 0; k < 2; ++k)
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj)
-          v[k][jj] = j0 + jj < nt[k] ? __ldcg(base[k] + (size_t)(j0 + jj) * kSlotQuads + q[k])
-                                     : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int k = 0; k < 2; ++k)
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj) {
-          s[k].x += v[k][jj].x; s[k].y += v[k][jj].y; s[k].z += v[k][jj].z; s[k].w += v[k][jj].w;
-        }
-    }
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      if (!has[k]) continue;
-      const int m = q[k] / kQuads;
-      const int n = tile[k] * kTileCols + (q[k] - m * kQuads) * 4;
-      if (n < N) {  // N % 32 == 0: all four outputs are in range
-        __half2* dst = reinterpret_cast<__half2*>(y + (size_t)m * N + n);
-        dst[0] = __floats2half2_rn(s[k].x, s[k].y);
-        dst[1] = __floats2half2_rn(s[k].z, s[k].w);
-      }
-    }
-  }
-}
-
 // Register cap for one CTA per SM: the 288 threads are 9 warps, so one SM sub-partition (a quarter of
 // the 64 K registers) holds three of them.
 constexpr int kMaxRegs = (65536 / 4) / (((kThreads / 32 + 3) / 4) * 32) / 8 * 8;
@@ -310,9 +261,7 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kStages);
-  int* last_flag = reinterpret_cast<int*>(bars + 2 * kStages) + 1;  // number of tiles in the table
-  int* last_tile = last_flag + 1;                                  // [kTicketBatch] tiles this CTA completes
-  int* last_nt = last_tile + kTicketBatch;                         // [kTicketBatch] their contributor counts
+  volatile int* ready_flag = abort_flag + 1;  // the designated tile's partials have all arrived
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -330,7 +279,7 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       mbar_init(empty_bar(s), kConsumers);
     }
     *abort_flag = 0;
-    *last_flag = 0;
+    *ready_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     // the next kernel in the stream may launch now; it waits for this grid before touching shared data
@@ -399,7 +348,9 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     const int word = warp * 8 + g;    // this lane's packed word column in the tile
     const LaneOffsets lo = lane_offsets(word, g, t);
     bool waited = false;
-    bool shared_tiles = false;        // any tile of this range also computed by another CTA
+    int part_tile = -1;               // a shared tile whose partial this CTA wrote (at most one)
+    int own_tile = -1;                // the shared tile this CTA completes (it holds its first unit)
+    float hold[4][4];                 // own_tile's sums, kept in registers for its reduction
     bool failed = false;              // a wait ran out: error recorded, the rest of the call skipped
     GroupConsts gc;                   // zero / scale constants of the current group (cached_grp)
     int cached_grp = -1;
@@ -488,6 +439,14 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             *reinterpret_cast<uint4*>(y + (size_t)m * N + n0) = make_uint4(h[0], h[1], h[2], h[3]);
           }
         }
+      } else if (p == pf) {
+        // this CTA holds the tile's first unit, so the tile is the last of its range: it completes
+        // the tile after its range, from these registers and the other contributors' partials
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) hold[b][e] = acc[b][e];
+        own_tile = tile;
       } else {
         float* slot = part + ((size_t)tile * maxc + (size_t)(p - pf)) * kGemvMaxM * kTileCols;
 #pragma unroll
@@ -505,48 +464,107 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             dst[1] = make_float4(v[4], v[5], v[6], v[7]);
           }
         }
-        shared_tiles = true;
+        part_tile = tile;
       }
     }
 
-    // ---- tickets of the shared tiles, after the whole range: one fence for all partials, the
-    // tickets of up to kTicketBatch tiles taken back to back, and the tiles this CTA completes
-    // reduced together by all consumer threads
-    if (shared_tiles && !failed) {
-      consumers_sync();  // every partial of this CTA written (thread 0's fence below publishes them)
-      const int tlast = (u1 - 1) / RB;
-      for (int tb = u0 / RB; tb <= tlast; tb += kTicketBatch) {
-        const int te = min(tlast + 1, tb + kTicketBatch);
-        if (threadIdx.x == 0) {
-          __threadfence();
-          int tk[kTicketBatch];
-          for (int tile = tb; tile < te; ++tile) {
-            const int pf = (int)cta_of_unit(tile * RB, units, P);
-            const int pl = (int)cta_of_unit((tile + 1) * RB - 1, units, P);
-            tk[tile - tb] = pf == pl ? -1 : atomicAdd(counters + tile, 1);
+    // ---- split K, after the whole range.  A shared tile is completed by the contributor that holds
+    // its first unit (pf); every other contributor publishes its partial (fence, then a count on the
+    // tile) and is done.  pf waits for the count, adds the partials to its own sums in contributor
+    // order and rounds once to fp16, so results are bit-reproducible.  No CTA waits before it has
+    // published its own partial, and the grid is at most one CTA per SM, so every wait ends.
+    // a timed-out wait in any warp abandons the rest of the call for the whole CTA (every consumer
+    // thread takes the same branches below, so the named barriers in them always complete)
+    failed = consumers_any(failed);
+    if (!failed && part_tile >= 0) {
+      consumers_sync();  // every partial store of this CTA issued
+      if (threadIdx.x == 0) {
+        __threadfence();
+        atomicAdd(counters + part_tile, 1);
+      }
+    }
+    if (!failed && own_tile >= 0) {
+      const int pf = p;
+      const int nt = (int)cta_of_unit((own_tile + 1) * RB - 1, units, P) - pf + 1;
+      if (threadIdx.x == 0) {
+        volatile int* cnt = reinterpret_cast<volatile int*>(counters + own_tile);
+        const long long t0 = now_ns();
+        bool ok = true;
+        while (*cnt != nt - 1) {
+          if (now_ns() - t0 > kWaitLimitNs) {
+            atomicExch(err, 504);
+            ok = false;
+            break;
           }
-          int nl = 0;
-          for (int tile = tb; tile < te; ++tile) {
-            if (tk[tile - tb] < 0) continue;
-            const int nt = (int)(cta_of_unit((tile + 1) * RB - 1, units, P) - cta_of_unit(tile * RB, units, P)) + 1;
-            if (tk[tile - tb] == nt - 1) {
-              last_tile[nl] = tile;
-              last_nt[nl] = nt;
-              ++nl;
+        }
+        if (ok) {
+          __threadfence();  // the partials, before the barrier below hands them to the other threads
+          *cnt = 0;         // every other contributor has counted: the ticket is free for the next call
+        }
+        *ready_flag = ok ? 1 : 0;
+      }
+      // the ring is idle now (every stage consumed): its first slot takes this CTA's own sums in the
+      // partials' layout, [token][512 columns] fp32
+      float* own = reinterpret_cast<float*>(smem);
+      consumers_sync();
+#pragma unroll
+      for (int par = 0; par < 2; ++par) {
+        const int m = 2 * t + par;
+        if (m < M) {
+          float v[8];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const int sl = slot_of_col(c);
+            v[c] = hold[sl >> 1][(sl & 1) * 2 + par];
+          }
+          float4* dst = reinterpret_cast<float4*>(own + m * kTileCols + word * 8);
+          dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+          dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+        }
+      }
+      consumers_sync();
+      if (*ready_flag) {
+        // items (token, 4 columns): up to four per thread, each with eight contributors' loads in flight
+        constexpr int kQuads = kTileCols / 4;
+        constexpr int kThreadsC = kConsumers * 32;
+        const int items = M * kQuads;
+        const float4* base = reinterpret_cast<const float4*>(part + (size_t)own_tile * maxc * kGemvMaxM * kTileCols);
+        constexpr size_t kSlotQuads = (size_t)kGemvMaxM * kQuads;
+        float4 s4[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int it = threadIdx.x + k * kThreadsC;
+          s4[k] = it < items ? reinterpret_cast<const float4*>(own)[it] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        for (int j0 = 1; j0 < nt; j0 += 8) {
+          float4 a[4][8];
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+              const int it = threadIdx.x + k * kThreadsC;
+              a[k][jj] = (it < items && j0 + jj < nt) ? __ldcg(base + (size_t)(j0 + jj) * kSlotQuads + it)
+                                                      : make_float4(0.f, 0.f, 0.f, 0.f);
             }
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+              s4[k].x += a[k][jj].x; s4[k].y += a[k][jj].y; s4[k].z += a[k][jj].z; s4[k].w += a[k][jj].w;
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int it = threadIdx.x + k * kThreadsC;
+          if (it >= items) continue;
+          const int m = it / kQuads;
+          const int n = own_tile * kTileCols + (it - m * kQuads) * 4;
+          if (n < N) {  // N % 32 == 0: all four outputs are in range
+            __half2* dst = reinterpret_cast<__half2*>(y + (size_t)m * N + n);
+            dst[0] = __floats2half2_rn(s4[k].x, s4[k].y);
+            dst[1] = __floats2half2_rn(s4[k].z, s4[k].w);
           }
-          if (nl > 0) __threadfence();  // the other contributors' partials, before the barrier below
-          *last_flag = nl;
         }
-        consumers_sync();
-        const int nl = *last_flag;
-        if (nl > 0) {
-          reduce_tiles(part, y, last_tile, last_nt, nl, maxc, M, N, threadIdx.x, kConsumers * 32);
-          consumers_sync();
-          // leave the tickets at zero for the next call
-          if (threadIdx.x < nl) reinterpret_cast<volatile int*>(counters)[last_tile[threadIdx.x]] = 0;
-        }
-        consumers_sync();  // the tile table is reused by the next batch
       }
     }
   }
@@ -580,13 +598,41 @@ bool make_map_2d(CUtensorMap* map, CUtensorMapDataType dt, int elem_bytes, const
 
 }  // namespace
 
+// SMs of the current device (the grid is at most one CTA per SM, so that every CTA of a call is
+// resident together and a tile's completer may wait for its other contributors); GB300's count
+// when no device can be queried.
+int device_sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return kNumSMs;
+  }
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = kNumSMs;
+    }
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
 GemvPlan gemv_plan(int64_t M, int64_t K, int64_t N, int split_k) {
   (void)M;
   GemvPlan p;
   p.tiles = (int)((N / 8 + kTileWords - 1) / kTileWords);
   p.groups = (int)(K / kRows);  // row blocks of 64 (two per quantization group)
   const int64_t units = (int64_t)p.tiles * p.groups;
-  int64_t ctas = split_k > 0 ? (int64_t)p.tiles * split_k : (int64_t)kNumSMs;
+  const int64_t sms = device_sm_count();
+  int64_t ctas;
+  if (split_k == 1) {
+    ctas = p.tiles;  // one CTA per tile: no tile is shared, so no CTA waits for another
+  } else {
+    ctas = split_k > 1 ? (int64_t)p.tiles * split_k : sms;
+    if (ctas > sms) ctas = sms;  // shared tiles: at most one CTA per SM, all resident together
+  }
   if (ctas > units) ctas = units;
   if (ctas < 1) ctas = 1;
   if (p.tiles > kMaxCounters) ctas = p.tiles;  // the tickets would not fit the workspace block

@@ -65,9 +65,9 @@ extern "C" awq_status awq_gemv_noalloc(const uint16_t* x, const int32_t* qweight
   GemvPlan plan = gemv_plan(M, K, N, split_k);
   if (gemv_workspace_bytes(plan, M, N) > kNoAllocScratchBytes) {
     if (split_k > 0) return AWQ_EWORKSPACE;
+    // split 1 (one CTA per tile) needs no scratch, so the search always ends
     int s = plan.split;
-    while (s > 1 && gemv_workspace_bytes(plan, M, N) > kNoAllocScratchBytes) plan = gemv_plan(M, K, N, --s);
-    if (gemv_workspace_bytes(plan, M, N) > kNoAllocScratchBytes) return AWQ_EWORKSPACE;
+    while (gemv_workspace_bytes(plan, M, N) > kNoAllocScratchBytes) plan = gemv_plan(M, K, N, s > 1 ? --s : 1);
   }
 
   int dev = 0, major = 0, minor = 0;

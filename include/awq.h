@@ -102,11 +102,19 @@ size_t awq_workspace_bytes(awq_op op, int64_t M, int64_t K, int64_t N, int32_t s
  * x fp16 [M, K]; qweight int32 [K, N/8]; qzeros int32 [K/128, N/8] or NULL
  * (symmetric, z = 8); scales fp16 [K/128, N]; y fp16 [M, N] (output).
  * 1 <= M <= 8 (0 = no-op), K % 128 == 0, N % 32 == 0, group_size == 128.
- * split_k: number of K slices per 128-column tile, reduced in fp32 (0 =
- * automatic: a persistent grid of two CTAs per SM, each owning an equal share
- * of the (tile, 128-row group) units); the fp16 output is rounded once from
- * the fp32 sum.  Needs a workspace when a tile is shared by several CTAs
- * (awq_workspace_bytes() > 0).
+ * split_k: number of CTAs per 512-column tile, whose K slices are reduced in
+ * fp32 (0 = automatic: a persistent grid of one CTA per SM, each owning an
+ * equal share of the (tile, 64-row block) units; 1 = one CTA per tile, no
+ * shared tile).  When tiles are shared the grid never exceeds one CTA per SM,
+ * so a larger split_k is clamped: a tile is completed by the CTA holding its
+ * first 64-row block, which waits (bounded) for the other contributors'
+ * partials, so the call assumes its CTAs can all be resident at once (no
+ * other kernel holding SMs indefinitely).  The fp16 output is rounded once
+ * from the fp32 sum, adding the partials in a fixed order (bit-reproducible).
+ * Needs a workspace when a tile is shared by several CTAs
+ * (awq_workspace_bytes() > 0).  The group's zero point and scale are applied
+ * to fp32 sums of the integer codes, so the products use s * (q - z) in fp32
+ * rather than its fp16 rounding (well inside the fp16 output tolerance).
  * Source: the M <= 8 branch of the dispatch snippet, gemv_forward_cuda(inputs,
  * qweight, scales, qzeros, group_size) ("Speed up AWQ 2.5x with updated kernel").
  */
@@ -127,9 +135,10 @@ awq_status awq_gemv(const uint16_t *x, const int32_t *qweight, const int32_t *qz
  *  - The first call on each device resolves the array's device address
  *    (cudaGetSymbolAddress with that device current); make that first call before
  *    any stream capture.
- *  - Automatic split (split_k = 0) shrinks the split until its scratch fits 8 MiB;
- *    an explicit split_k whose scratch (64 KB of tickets + split * M * N * 4 bytes)
- *    exceeds 8 MiB is rejected with AWQ_EWORKSPACE.
+ *  - Automatic split (split_k = 0) shrinks the split until its scratch fits 8 MiB
+ *    (split 1 needs none); an explicit split_k whose scratch (64 KB of tickets +
+ *    contributors per tile * tiles * 8 * 512 * 4 bytes) exceeds 8 MiB is rejected
+ *    with AWQ_EWORKSPACE.
  *  - Every call shares the array and clears the tickets it needs on `stream` before
  *    its kernel; calls whose kernels overlap on the GPU (other streams, other host
  *    threads) race on the array and must be serialized by the caller.

@@ -66,10 +66,16 @@ def test_noalloc_matches_gemv_on_two_calls_in_a_row(awq, M, K, N, split_k, symme
 
 
 def test_noalloc_rejects_a_split_whose_scratch_exceeds_the_array(awq):
-    # 64 splits of an 8 x 22016 output need 64 * 8 * 22016 * 4 bytes = 45 MB > 8 MiB
-    M, K, N = 8, 8192, 22016
+    # N = 153600 is 300 tiles of 512 columns.  split_k = 2 asks for 600 CTAs, clamped to one per SM;
+    # with K = 256 (4 row blocks per tile) the tiles then straddle CTAs, two contributors each:
+    # 300 tiles * 2 * (8 tokens * 512 columns * 4 bytes) = 9.8 MB of partials > 8 MiB.
+    M, K, N = 8, 256, 153600
     x = torch.zeros((M, K), dtype=torch.float16, device="cuda")
     qw = torch.zeros((K, N // 8), dtype=torch.int32, device="cuda")
     sc = torch.zeros((K // 128, N), dtype=torch.float16, device="cuda")
     y = torch.empty((M, N), dtype=torch.float16, device="cuda")
-    assert _noalloc_via_abi(awq, x, qw, None, sc, y, 64) == EWORKSPACE
+    assert _noalloc_via_abi(awq, x, qw, None, sc, y, 2) == EWORKSPACE
+    # the automatic split falls back to one CTA per tile, which needs no scratch
+    assert _noalloc_via_abi(awq, x, qw, None, sc, y, 0) == 0
+    torch.cuda.synchronize()
+    assert torch.all(y == 0)
