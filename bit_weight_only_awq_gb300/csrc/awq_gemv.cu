@@ -21,11 +21,15 @@
 //  * Persistent, evenly balanced grid: the (512-column tile, 64-row block) units are cut
 //    into equal contiguous ranges, one per SM; a CTA's units are grouped into stages of
 //    one quantization group (or a lone 64-row block at a range edge).  A tile finished by
-//    one CTA is written directly; a tile shared by several CTAs leaves one fp32 partial per
-//    CTA in the workspace.  The tickets are taken only after the CTA's last unit, so no
-//    CTA stalls mid-range on a fence; the last contributor of a tile (atomic ticket) sums
-//    the partials in contributor order and rounds once to fp16, so results are
-//    bit-reproducible.
+//    one CTA is written directly.  A tile shared by several CTAs is completed by the one
+//    holding its first row block (for which it is the last tile of the range): after its
+//    range it waits, bounded, until the other contributors have published their fp32
+//    partials (stores, a fence, a count on the tile), adds them to its own sums in
+//    contributor order and rounds once to fp16, so results are bit-reproducible.  The
+//    other contributors publish after their range and exit at once, which frees their SMs
+//    for the next call.  No CTA waits before publishing its own partial, and a grid with
+//    shared tiles has at most one CTA per SM, so all of them are resident and every wait
+//    ends.
 //  * Programmatic dependent launch: the GEMV starts streaming its weights before waiting
 //    for the previous kernel, and touches activations, outputs and the workspace only
 //    after that wait.
