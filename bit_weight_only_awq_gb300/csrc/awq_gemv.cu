@@ -63,6 +63,10 @@ namespace {
 constexpr int kConsumers = 8;                  // consumer warps, one 64-column slice of the tile each
 constexpr int kThreads = (kConsumers + 1) * 32;
 constexpr int kStages = 3;
+// Stages streamed before the wait on the previous kernel: more of them compete with that kernel's
+// last CTAs for DRAM and measured slower (3: -2 to -3 % on 12-25 MB calls).
+constexpr int kPrefetch = 2;
+static_assert(kPrefetch >= 1 && kPrefetch <= kStages, "prefetch within the ring");
 // Polling pauses: the producer's empty-slot waits and the consumers' full-slot waits share their
 // schedulers with consumer warps that have arithmetic to issue.
 constexpr uint32_t kProducerSleepNs = 1000;
@@ -318,7 +322,7 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       StageWalk w(u0, u1, RB);
       int pre = 0;
       int pre_rb[kStages], pre_nh[kStages];
-      while (pre < kStages && w.u < u1) {
+      while (pre < kPrefetch && w.u < u1) {
         const int nh = w.units_here();
         mbar_arrive_tx(full_bar(pre), tx_bytes(nh));
         issue_weights(pre, w.tile, w.rb, nh);
@@ -482,29 +486,27 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     failed = consumers_any(failed);
     if (!failed && part_tile >= 0) {
       consumers_sync();  // every partial store of this CTA issued
-      if (threadIdx.x == 0) {
-        __threadfence();
-        atomicAdd(counters + part_tile, 1);
-      }
+      if (threadIdx.x == 0)  // release: the CTA's partial stores (ordered by the barrier) before the count
+        asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(counters + part_tile) : "memory");
     }
     if (!failed && own_tile >= 0) {
       const int pf = p;
       const int nt = (int)cta_of_unit((own_tile + 1) * RB - 1, units, P) - pf + 1;
       if (threadIdx.x == 0) {
-        volatile int* cnt = reinterpret_cast<volatile int*>(counters + own_tile);
+        int* cnt = counters + own_tile;
         const long long t0 = now_ns();
         bool ok = true;
-        while (*cnt != nt - 1) {
+        for (;;) {
+          int c;
+          asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(c) : "l"(cnt) : "memory");
+          if (c == nt - 1) break;
           if (now_ns() - t0 > kWaitLimitNs) {
             atomicExch(err, 504);
             ok = false;
             break;
           }
         }
-        if (ok) {
-          __threadfence();  // the partials, before the barrier below hands them to the other threads
-          *cnt = 0;         // every other contributor has counted: the ticket is free for the next call
-        }
+        if (ok) *reinterpret_cast<volatile int*>(cnt) = 0;  // every other contributor has counted
         *ready_flag = ok ? 1 : 0;
       }
       // the ring is idle now (every stage consumed): its first slot takes this CTA's own sums in the
