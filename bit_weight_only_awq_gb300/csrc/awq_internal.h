@@ -41,8 +41,8 @@ cudaError_t launch_dequant(const uint32_t* qw, const uint32_t* qz, const uint16_
 // ---- decode GEMV (awq_gemv.cu)
 constexpr int kNumSMs = 152;  // GB300
 
-// Work partition of the decode GEMV: units are (128-column tile, 128-row group) pairs in
-// tile-major order; CTA p of P owns units [unit_begin(p), unit_begin(p + 1)).
+// Work partition of the decode GEMV: units are (512-column tile, 64-row block) pairs in tile-major
+// order; CTA p of P owns units [unit_begin(p), unit_begin(p + 1)).
 __host__ __device__ inline int64_t unit_begin(int64_t p, int64_t units, int64_t ctas) {
   return p * units / ctas;
 }
@@ -52,8 +52,8 @@ __host__ __device__ inline int64_t cta_of_unit(int64_t u, int64_t units, int64_t
 }
 
 struct GemvPlan {
-  int tiles;   // 128-column tiles
-  int groups;  // 128-row groups (K / 128)
+  int tiles;   // 512-column tiles
+  int groups;  // 64-row blocks per tile (K / 64)
   int ctas;    // grid size P
   int maxc;    // most CTAs contributing to one tile (1 = no cross-CTA reduction)
   int split;   // effective K split (ceil(ctas / tiles)), the knob callers pass as split_k
