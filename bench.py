@@ -9,8 +9,8 @@ every step streams its weights from HBM).
 Timed region (device value): the step captured as one CUDA graph, replayed K times
 between CUDA events on the launching stream, barrier + synchronize on both sides,
 max over ranks.  e2e: the same step through the public Python API (one call per
-GEMV), with the activations copied in from pinned host memory and the outputs copied
-back every step.  The CPU baseline and `--impl reference` time the numpy oracle on a
+layer call), with all of the step's activations copied in from pinned host memory as
+one transfer and all of its outputs copied back as one, every step.  The CPU baseline and `--impl reference` time the numpy oracle on a
 bounded sample of the same workload.
 
 Other workloads (`--workload prefill|crossover|w4a8`) print the same line for the
@@ -200,7 +200,9 @@ def load_peaks():
 
 
 def build_inputs(torch, workload, device):
-    """Per-call device buffers (weights distinct per call), plus pinned host copies of the activations."""
+    """Per-call device buffers (weights distinct per call).  The activations and outputs of all calls
+    are views into one device buffer each, mirrored by one pinned host buffer each, so that the e2e
+    step moves them with one host-to-device and one device-to-host copy."""
     bufs = []
     for i, (kind, name, M, K, N) in enumerate(workload_calls(workload, **WORKLOAD_FILTER)):
         seed = 10_000 + i
@@ -213,11 +215,26 @@ def build_inputs(torch, workload, device):
         else:
             p = synth.awq_problem(M, K, N, seed=seed)
             b = {k: torch.from_numpy(p[k]).to(device) for k in ("x", "qweight", "qzeros", "scales")}
-        b["y"] = torch.empty((M, N), dtype=torch.float16, device=device)
-        b["x_host"] = torch.from_numpy(p["x"]).pin_memory()
-        b["y_host"] = torch.empty((M, N), dtype=torch.float16).pin_memory()
+        b["x_np"] = p["x"]
         b["meta"] = (kind, name, M, K, N)
         bufs.append(b)
+    # every view starts on a 16-byte boundary: M * K and M * N are multiples of 8 halves
+    nx = sum(b["meta"][2] * b["meta"][3] for b in bufs)
+    ny = sum(b["meta"][2] * b["meta"][4] for b in bufs)
+    packed = {"x": torch.empty(nx, dtype=torch.float16, device=device),
+              "x_host": torch.empty(nx, dtype=torch.float16).pin_memory(),
+              "y": torch.empty(ny, dtype=torch.float16, device=device),
+              "y_host": torch.empty(ny, dtype=torch.float16).pin_memory()}
+    ox = oy = 0
+    for b in bufs:
+        _, _, M, K, N = b["meta"]
+        b["x"] = packed["x"][ox:ox + M * K].view(M, K)
+        b["x"].copy_(torch.from_numpy(b.pop("x_np")))
+        packed["x_host"][ox:ox + M * K].copy_(b["x"].view(-1).cpu())
+        b["y"] = packed["y"][oy:oy + M * N].view(M, N)
+        ox += M * K
+        oy += M * N
+    bufs[0]["packed"] = packed
     return bufs
 
 
@@ -290,11 +307,10 @@ def gpu_arm(args, rank, world, torch, dist):
     # e2e through the public API: pinned H2D of the activations, every call, D2H of the outputs
     def e2e_step():
         with torch.cuda.stream(stream):
-            for b in bufs:
-                b["x"].copy_(b["x_host"], non_blocking=True)
+            packed = bufs[0]["packed"]
+            packed["x"].copy_(packed["x_host"], non_blocking=True)
             issue_step(awq, bufs, stream)
-            for b in bufs:
-                b["y_host"].copy_(b["y"], non_blocking=True)
+            packed["y_host"].copy_(packed["y"], non_blocking=True)
         stream.synchronize()
 
     for _ in range(max(1, args.warmup)):
@@ -438,7 +454,7 @@ def main():
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_value, 2), "unit": unit, "h2d_bytes_per_step": r["h2d"],
-                    "d2h_bytes_per_step": r["d2h"], "path": "python binding, one API call per layer call of the step, pinned copies"},
+                    "d2h_bytes_per_step": r["d2h"], "path": "python binding, one API call per layer call; one pinned copy in and one out per step"},
             "gpu_launches": r["launches_per_step"] * args.steps,
             "clocks": r["clocks"],
         }

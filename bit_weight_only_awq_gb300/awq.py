@@ -101,6 +101,19 @@ def awq_workspace_bytes(op: int, M: int, K: int, N: int, split_k: int = 0) -> in
     return int(lib.awq_workspace_bytes(op, M, K, N, split_k))
 
 
+# Workspace sizes by (op, M, K, N, split_k, device): the size depends only on these (the plan reads
+# the device's SM count), and a decode loop repeats the same few shapes.
+_ws_need: dict[tuple, int] = {}
+
+
+def _workspace_need(op: int, M: int, K: int, N: int, split_k: int, device: torch.device) -> int:
+    key = (op, M, K, N, split_k, device.index)
+    need = _ws_need.get(key)
+    if need is None:
+        need = _ws_need[key] = awq_workspace_bytes(op, M, K, N, split_k)
+    return need
+
+
 def awq_pack(q: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     rows, n = q.shape
     if out is None:
@@ -131,9 +144,8 @@ def _gemm_like(name, op, x, qweight, qzeros, scales, group_size, split_k, out, w
     N = qweight.shape[1] * 8
     if out is None:
         out = torch.empty((M, N), dtype=torch.float16, device=x.device)
-    need = awq_workspace_bytes(op, M, K, N, split_k)
     if ws is None:
-        ws = device_workspace(need, x.device)
+        ws = device_workspace(_workspace_need(op, M, K, N, split_k, x.device), x.device)
     nbytes = 0 if ws is None else ws.numel() * ws.element_size()
     fn = getattr(lib, name)
     _check(name, fn(_ptr(x), _ptr(qweight), _ptr(qzeros), _ptr(scales), _ptr(out), M, K, N, group_size,

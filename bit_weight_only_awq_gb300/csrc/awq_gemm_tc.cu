@@ -38,6 +38,7 @@
 #include <cuda_fp16.h>
 
 #include "awq_internal.h"
+#include "awq_host.h"
 #include "awq_ptx.cuh"
 
 namespace awq {
@@ -423,30 +424,6 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
 }
 
 // ------------------------------------------------------------------ host side
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
-bool make_map_2d(CUtensorMap* map, CUtensorMapDataType dt, int elem_bytes, const void* base, uint64_t inner,
-                 uint64_t outer, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[2] = {inner, outer};
-  const cuuint64_t strides[1] = {inner * (uint64_t)elem_bytes};
-  const cuuint32_t box[2] = {box_inner, box_outer};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
 
 template <int BT, int NB, int MODE>
 cudaError_t launch_t(const uint16_t* x16, const uint32_t* qw, const uint32_t* qz, const uint16_t* sc,
@@ -471,7 +448,7 @@ cudaError_t launch_t(const uint16_t* x16, const uint32_t* qw, const uint32_t* qz
                                 CU_TENSOR_MAP_SWIZZLE_NONE));
   if (!ok) return cudaErrorInvalidValue;
   auto kern = gemm_kernel<BT, NB, MODE>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), C::kSmem);
   if (e != cudaSuccess) return e;
   dim3 grid(p.n_tiles, p.m_tiles, p.split);
   kern<<<grid, kThreads, C::kSmem, s>>>(tx, tq, tz, ts, reinterpret_cast<__half*>(y), acc_out, s_tok,
