@@ -7,12 +7,77 @@
 // note that this per-token scale is computed online.
 #include <cuda_fp16.h>
 
+#include "awq_host.h"
 #include "awq_internal.h"
 
 namespace awq {
 namespace {
 
 constexpr int kQThreads = 256;
+constexpr int kQ1MaxK = 32768;  // rows up to this length are held in shared memory (64 KB)
+
+// code = rint(x / s) for s > 0, clamped to [-128, 127], with the IEEE fp32 quotient of the pages' script.
+// x * (1 / s) differs from the correctly rounded quotient by at most a few ulp, which can change the
+// rounded integer only next to a half-integer; there the quotient is taken exactly.
+__device__ __forceinline__ uint32_t code_of(float xv, float s, float inv) {
+  const float r = xv * inv;
+  const float f = r - floorf(r);
+  float q = fabsf(f - 0.5f) < 1.0e-4f ? rintf(__fdiv_rn(xv, s)) : rintf(r);
+  q = fminf(fmaxf(q, -128.f), 127.f);
+  return (uint32_t)(int)q & 0xFFu;
+}
+
+// One CTA per token row, the row read from DRAM once: it is kept in shared memory between the absmax
+// pass and the coding pass.
+__global__ void __launch_bounds__(kQThreads)
+quant_act_smem_kernel(const __half* __restrict__ x, int8_t* __restrict__ xq, float* __restrict__ s_tok, int K) {
+  extern __shared__ uint4 row[];
+  __shared__ uint32_t warp_max[kQThreads / 32];
+  __shared__ float s_shared;
+  const int64_t r = blockIdx.x;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + r * (int64_t)K);
+  const int nvec = K / 8;
+  uint32_t mx = 0;  // |x| as fp16 bits: integer order equals magnitude order for finite values
+  for (int i = threadIdx.x; i < nvec; i += kQThreads) {
+    const uint4 v = __ldcs(xr + i);
+    row[i] = v;
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      mx = max(mx, w[j] & 0x7FFFu);
+      mx = max(mx, (w[j] >> 16) & 0x7FFFu);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+  if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = mx;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t m = 0;
+    for (int w = 0; w < kQThreads / 32; ++w) m = max(m, warp_max[w]);
+    const float absmax = __half2float(__ushort_as_half((unsigned short)m));
+    const float s = __half2float(__float2half_rn(__fdiv_rn(absmax, 127.0f)));
+    s_shared = s;
+    s_tok[r] = s;
+  }
+  __syncthreads();
+  const float s = s_shared;
+  const float inv = s > 0.f ? __frcp_rn(s) : 0.f;
+  uint2* qr = reinterpret_cast<uint2*>(xq + r * (int64_t)K);
+  for (int i = threadIdx.x; i < nvec; i += kQThreads) {
+    const uint4 v = row[i];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t out[2] = {0, 0};
+    if (s > 0.f) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float xv = __half2float(__ushort_as_half((unsigned short)(w[j >> 1] >> (16 * (j & 1)))));
+        out[j >> 2] |= code_of(xv, s, inv) << (8 * (j & 3));
+      }
+    }
+    qr[i] = make_uint2(out[0], out[1]);
+  }
+}
 
 // One CTA per token row: pass 1 finds absmax, pass 2 writes the codes (second read hits L2).
 __global__ void __launch_bounds__(kQThreads)
@@ -85,7 +150,17 @@ __global__ void i8_to_f16_kernel(const int8_t* __restrict__ xq, __half* __restri
 
 cudaError_t launch_quant_act(const uint16_t* x, int8_t* xq, float* s_tok, int64_t M, int64_t K, cudaStream_t s) {
   if (M == 0) return cudaSuccess;
-  quant_act_kernel<<<(unsigned)M, kQThreads, 0, s>>>(reinterpret_cast<const __half*>(x), xq, s_tok, (int)K);
+  if (K <= kQ1MaxK) {
+    const int smem = (int)K * 2;
+    if (smem > 48 * 1024) {
+      const cudaError_t e = set_smem_once(reinterpret_cast<const void*>(quant_act_smem_kernel), kQ1MaxK * 2);
+      if (e != cudaSuccess) return e;
+    }
+    quant_act_smem_kernel<<<(unsigned)M, kQThreads, smem, s>>>(reinterpret_cast<const __half*>(x), xq, s_tok,
+                                                               (int)K);
+  } else {
+    quant_act_kernel<<<(unsigned)M, kQThreads, 0, s>>>(reinterpret_cast<const __half*>(x), xq, s_tok, (int)K);
+  }
   return cudaGetLastError();
 }
 

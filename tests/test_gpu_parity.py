@@ -234,6 +234,24 @@ def test_quant_act_bitexact(awq, M, K):
     assert np.array_equal(host(xq), want_q)
 
 
+def test_quant_act_half_integer_ties_and_long_rows(awq):
+    # scale exactly 1 (absmax 127): x = k + 1/2 divides to an exact tie, which rounds to even
+    K = 1024
+    ties = (np.arange(K) % 254 - 127 + 0.5).astype(np.float16)
+    ties[0] = 127
+    x = np.stack([ties, -ties]).astype(np.float16)
+    xq, s = awq.w4a8_quant_act(dev(x))
+    want_q, want_s = oracle.quant_act(x)
+    assert np.array_equal(host(s).view(np.uint32), want_s.view(np.uint32))
+    assert np.array_equal(host(xq), want_q)
+    # rows longer than the shared-memory path take the two-pass kernel
+    x = synth.activations(np.random.default_rng(7), 2, 40960)
+    xq, s = awq.w4a8_quant_act(dev(x))
+    want_q, want_s = oracle.quant_act(x)
+    assert np.array_equal(host(s).view(np.uint32), want_s.view(np.uint32))
+    assert np.array_equal(host(xq), want_q)
+
+
 def _w4a8_run(awq, p, split_k=0, with_acc=True):
     x = dev(p["x"])
     xq, s = awq.w4a8_quant_act(x)
