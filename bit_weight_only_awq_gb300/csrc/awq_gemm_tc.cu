@@ -52,6 +52,9 @@ constexpr int kDqWarps = kDqGroupWarps * kDqGroups;
 constexpr int kThreads = (3 + kDqWarps) * 32;   // x producer, MMA, q producer, dequant
 constexpr int kWBlockBytes = kBK * kBN * 2;     // dequantized tile of one M-block, 16 KB
 
+template <int MODE>
+constexpr bool kIsW4A8 = MODE == kModeW4A8 || MODE == kModeW4A8One;
+
 // NB M-blocks of 128 weight columns share every activation tile: with NB = 2 a CTA owns 256 columns
 // and the activation bytes per flop halve (the ring that feeds them was the measured limit at NB = 1).
 template <int BT, int NB, int MODE>
@@ -76,7 +79,7 @@ struct Cfg {
   static constexpr int kFit = (227 * 1024 - 1024 - kFixed) / kXSlotBytes;
   static constexpr int kXStages = kFit > 16 ? 16 : kFit;   // slots
   static constexpr int kSmem = kXStages * kXSlotBytes + kFixed + 1024;
-  static constexpr int kAccs = MODE == kModeW4A8 ? 2 : 1;  // W4A8: one accumulator per exact K chunk
+  static constexpr int kAccs = MODE == kModeW4A8 ? 2 : 1;  // W4A8: one accumulator per exact K chunk (two)
   static constexpr int kTmemCols = NB * kAccs * BT < 32 ? 32 : NB * kAccs * BT;
   // tcgen05 instruction descriptor, kind::f16: D f32, A/B f16, A MN-major, B K-major, M=128, N=BT
   static constexpr uint32_t kIdesc = (1u << 4) | (1u << 15) | ((uint32_t)(BT >> 3) << 17) |
@@ -203,7 +206,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
       const int S = is_x ? SX : kQStages;
       const uint32_t tx = is_x ? (uint32_t)C::kXSlotBytes
                                : (uint32_t)(kQBytes + (MODE == kModeZeroPoint ? C::kZBytes : 0) +
-                                            (MODE != kModeW4A8 ? C::kSBytes : 0));
+                                            (!kIsW4A8<MODE> ? C::kSBytes : 0));
       const int units = is_x ? nsteps * C::kXSub : nsteps;  // x: (k-step, 32-k half) slots
       int issued = 0;
       for (int j = 0; j < units; ++j, ++issued) {
@@ -220,7 +223,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
           mbar_arrive_tx(fullq(st), tx);
           tma_load_2d(smem_u32(qb), &tm_q, n0 / 8, kb, fullq(st));
           if (MODE == kModeZeroPoint) tma_load_2d(smem_u32(qb + kQBytes), &tm_z, n0 / 8, grp, fullq(st));
-          if (MODE != kModeW4A8) tma_load_2d(smem_u32(qb + kQBytes + 128), &tm_s, n0, grp, fullq(st));
+          if (!kIsW4A8<MODE>) tma_load_2d(smem_u32(qb + kQBytes + 128), &tm_s, n0, grp, fullq(st));
         }
       }
       // never leave the CTA with copies in flight
@@ -300,7 +303,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
       const uint32_t* qw = reinterpret_cast<const uint32_t*>(qb);
       uint8_t* wt = wring + ws * kWBytes;
       uint32_t zp[4], sp[4];
-      if (MODE != kModeW4A8) {
+      if (!kIsW4A8<MODE>) {
         const uint32_t zword = MODE == kModeZeroPoint ? reinterpret_cast<const uint32_t*>(qb + kQBytes)[c]
                                                       : 0x88888888u;
         const uint4 sv = reinterpret_cast<const uint4*>(qb + kQBytes + 128)[c];
@@ -320,7 +323,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const uint32_t h = pair_magic(words[jr], j);
-          o[j] = (MODE == kModeW4A8) ? hsub2(h, 0x64086408u) /* u - 8, exact */
+          o[j] = kIsW4A8<MODE> ? hsub2(h, 0x64086408u) /* u - 8, exact */
                                      : hmul2(hsub2(h, zp[j]), sp[j]);
         }
         const uint32_t off =
@@ -347,17 +350,17 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     const int split = gridDim.z;
     constexpr int kHalf = BT / 2;
     float sch = 0.f;
-    if (MODE == kModeW4A8 && n_ok) sch = __half2float(s_ch[n]);
+    if (kIsW4A8<MODE> && n_ok) sch = __half2float(s_ch[n]);
     if (have) {
 #pragma unroll 1
       for (int cb = half * kHalf; cb < (half + 1) * kHalf; cb += 8) {
         float v[8];
         tmem_ld8(tmem + ((uint32_t)(lq * 32) << 16) + dcol + (uint32_t)cb, v);
         int vi[8];
-        if (MODE == kModeW4A8) {
+        if (kIsW4A8<MODE>) {
 #pragma unroll
           for (int j = 0; j < 8; ++j) vi[j] = __float2int_rn(v[j]);  // exact integers
-          if (nsteps > chunk_steps) {
+          if (MODE == kModeW4A8 && nsteps > chunk_steps) {
             float v2[8];
             tmem_ld8(tmem + ((uint32_t)(lq * 32) << 16) + dcol + (uint32_t)(NB * BT + cb), v2);
 #pragma unroll
@@ -369,7 +372,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
           const int m = m0 + cb + j;
           if (!n_ok || m >= M) continue;
           const size_t o = (size_t)m * N + n;
-          if (MODE == kModeW4A8) {
+          if (kIsW4A8<MODE>) {
             const int a = vi[j];
             if (split == 1) {
               if (acc_out) acc_out[o] = a;
@@ -398,7 +401,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
           const int m = m0 + cb;
           if (!n_ok || m >= M) continue;
           const size_t o = (size_t)m * N + n;
-          if (MODE == kModeW4A8) {
+          if (kIsW4A8<MODE>) {
             int a = 0;
             for (int sp = 0; sp < split; ++sp) a += __ldcg(reinterpret_cast<const int32_t*>(part) + (size_t)sp * M * N + o);
             if (acc_out) acc_out[o] = a;
@@ -441,7 +444,7 @@ cudaError_t launch_t(const uint16_t* x16, const uint32_t* qw, const uint32_t* qz
   // zero-point and scale maps: dummies (the weight map) when the mode does not read them
   ok = ok && make_map_2d(&tz, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, qz ? (const void*)qz : (const void*)qw, nw,
                          qz ? ng : (uint64_t)K, kQWords, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
-  ok = ok && (MODE == kModeW4A8
+  ok = ok && (kIsW4A8<MODE>
                   ? make_map_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, qw, nw, (uint64_t)K, kQWords, 1,
                                 CU_TENSOR_MAP_SWIZZLE_NONE)
                   : make_map_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, sc, (uint64_t)N, ng, NB * kBN, 1,
@@ -462,13 +465,14 @@ cudaError_t launch_mode(const uint16_t* x16, const uint32_t* qw, const uint32_t*
                         const float* s_tok, const uint16_t* s_ch, uint16_t* y, int32_t* acc_out, int64_t M,
                         int64_t K, int64_t N, const GemmPlan& p, void* part, int* counters, int* err,
                         cudaStream_t s) {
-  if constexpr (MODE != kModeW4A8) {
-    if (p.nb == 2) {
-      switch (p.bt) {
-        case 128: return launch_t<128, 2, MODE>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters, err, s);
-        case 256: return launch_t<256, 2, MODE>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters, err, s);
-        default: return cudaErrorInvalidValue;
-      }
+  if (p.nb == 2) {
+    // W4A8 with two M-blocks: the plan keeps every K slice within one exact chunk
+    constexpr int M2 = MODE == kModeW4A8 ? kModeW4A8One : MODE;
+    if (MODE == kModeW4A8 && p.ksteps * kBK > kW4A8MaxKSlice) return cudaErrorInvalidValue;
+    switch (p.bt) {
+      case 128: return launch_t<128, 2, M2>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters, err, s);
+      case 256: return launch_t<256, 2, M2>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters, err, s);
+      default: return cudaErrorInvalidValue;
     }
   }
   if (p.nb != 1) return cudaErrorInvalidValue;
@@ -495,9 +499,11 @@ GemmPlan gemm_plan(int64_t M, int64_t K, int64_t N, int split_k, int mode) {
   p.nb = 1;
   p.bt = bt0;
   while (p.bt > 64 && tiles(p.bt, 1) < 114) p.bt /= 2;
-  // W4A16 with >= 128-token tiles: 256 weight columns per CTA (two M-blocks on one activation tile)
-  // whenever that still fills about a wave
-  if (mode != kModeW4A8 && bt0 >= 128) {
+  // >= 128-token tiles: 256 weight columns per CTA (two M-blocks on one activation tile) whenever that
+  // still fills about a wave.  W4A8 then has one exact accumulator per M-block, which holds K slices of
+  // at most 16384 rows: taken only when K fits one slice (at K = 21760 and 4096 tokens, two M-blocks
+  // with a K split of two measured 1375 us against 1150 us for one M-block with two accumulators)
+  if (bt0 >= 128 && (mode != kModeW4A8 || K <= kW4A8MaxKSlice)) {
     int bt = bt0;
     while (bt > 128 && tiles(bt, 2) < 114) bt /= 2;
     if (tiles(bt, 2) >= 114) {
@@ -519,8 +525,10 @@ GemmPlan gemm_plan(int64_t M, int64_t K, int64_t N, int split_k, int mode) {
         if (tiles * sp <= 152 && total / sp >= 8) split = sp;
   }
   if (mode == kModeW4A8) {
-    // two exact accumulators per CTA: each K slice spans at most 2 x 16384 rows
-    const int min_split = (int)((K + 2 * kW4A8MaxKSlice - 1) / (2 * kW4A8MaxKSlice));
+    // exact accumulators: each K slice spans at most 2 x 16384 rows with one M-block (two
+    // accumulators), at most 16384 with two M-blocks (one each)
+    const int64_t slice = p.nb == 2 ? kW4A8MaxKSlice : 2 * kW4A8MaxKSlice;
+    const int min_split = (int)((K + slice - 1) / slice);
     if (split < min_split) split = min_split;
   }
   if (split > total) split = total;

@@ -65,7 +65,10 @@ cudaError_t launch_gemv(const uint16_t* x, const uint32_t* qw, const uint32_t* q
                         int* err, cudaStream_t s);
 
 // ---- tensor-core GEMM (awq_gemm_tc.cu)
-enum GemmMode { kModeZeroPoint = 0, kModeSymmetric = 1, kModeW4A8 = 2 };
+// kModeW4A8One is the W4A8 kernel for K slices of at most 16384 rows (kW4A8MaxKSlice): one exact
+// accumulator per M-block instead of two, which leaves tensor memory for two M-blocks of 256 tokens.
+// The plan picks it; callers pass kModeW4A8.
+enum GemmMode { kModeZeroPoint = 0, kModeSymmetric = 1, kModeW4A8 = 2, kModeW4A8One = 3 };
 struct GemmPlan {
   int bt;        // token tile (MMA N): 16, 32, 64, 128 or 256
   int split;     // K slices (grid.z)

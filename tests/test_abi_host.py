@@ -103,7 +103,8 @@ def test_workspace_layout(awq):
     # GEMV: counters block + split x M x N fp32 partials (256-byte rounded)
     assert awq.awq_workspace_bytes(awq.OP_GEMV, 8, 4096, 4096, 1) == 0
     assert awq.awq_workspace_bytes(awq.OP_GEMV, 8, 4096, 4096, 4) == counters + 4 * 8 * 4096 * 4
-    # W4A8 at K = 21760: two exact accumulators per CTA (16384 rows each) cover K without a split
+    # W4A8 at K = 21760: one M-block per CTA with two exact accumulators (16384 rows each) covers K
+    # without a split
     x16 = 4096 * 21760 * 2
     assert awq.awq_workspace_bytes(awq.OP_W4A8_GEMM, 4096, 21760, 8192, 0) == counters + x16
     assert awq.awq_workspace_bytes(awq.OP_W4A8_GEMM, 16, 21760, 8192, 1) == counters + 16 * 21760 * 2

@@ -283,6 +283,19 @@ def test_w4a8_config_sampled_bitexact(awq, M):
     assert np.array_equal(y[:, cols].view(np.uint16), want_y.view(np.uint16))
 
 
+@pytest.mark.parametrize("M,K,N", [(1000, 21760, 8192), (1000, 4096, 16384)])
+def test_w4a8_large_tiles_bitexact(awq, M, K, N):
+    # >= 128-token tiles: at K = 21760 one M-block with two exact accumulators; at K = 4096 two M-blocks
+    # (256 weight columns per CTA) with one each; M = 1000 leaves a ragged last token tile
+    p = synth.w4a8_problem(M, K, N, seed=650 + M)
+    xq, s, y, acc = _w4a8_run(awq, p)
+    wc = sample_word_cols(N // 8, seed=M + 1, count=4)
+    cols = (8 * wc[:, None] + np.arange(8)[None, :]).ravel()
+    want_y, want_acc = oracle.w4a8_linear(xq, s, p["wq"][:, wc], p["s_ch"][cols])
+    assert np.array_equal(acc[:, cols], want_acc)
+    assert np.array_equal(y[:, cols].view(np.uint16), want_y.view(np.uint16))
+
+
 def test_no_device_timeouts_recorded(awq):
     torch.cuda.synchronize()
     assert awq.awq_last_device_error() == 0
