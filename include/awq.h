@@ -187,7 +187,9 @@ awq_status w4a8_quant_act(const uint16_t *x, int8_t *xq, float *s_tok, int64_t M
  * split_k: K slices reduced in int32 across CTAs (0 = automatic).  Inside a
  * CTA every 16384 inputs get their own fp32 tensor-memory accumulator (two at
  * most), so each fp32 sum is an exact integer; K beyond 32768 per slice is
- * split across CTAs.
+ * split across CTAs.  With 128 or more tokens and K <= 16384 a CTA covers 256
+ * output channels with one accumulator each (two 128-channel blocks sharing
+ * every activation tile).
  * Source: "Support W4A8 quantization for vllm": marlin_qqq_gemm(a, b_q_weight,
  * s1, s2, s3, workspace, size_m, size_n, size_k) in tlrmchlsmth's review;
  * HandH1998's per-channel dequantization (int4 to int8, channel scale on the
