@@ -52,6 +52,11 @@ def w4a8_bytes(M, K, N):
     return K * N / 2 + 2 * N + M * K + 4 * M + 2 * M * N
 
 
+def awq_linear_gemv_max():
+    """Largest token count the library's dispatch (awq_linear) sends to the GEMV kernel."""
+    return 16
+
+
 def workload_calls(workload, only=None, ms=None):
     """List of (kind, name, M, K, N) for one step (optionally filtered by shape name / M)."""
     calls = _workload_calls(workload)
@@ -73,7 +78,7 @@ def _workload_calls(workload):
         out = []
         for n, k, nn in synth.LLAMA31_8B_STACK:
             for m in synth.CROSSOVER_M:
-                out.append(("gemv" if m <= 8 else "gemm", n, m, k, nn))
+                out.append(("gemv" if m <= awq_linear_gemv_max() else "gemm", n, m, k, nn))
         return out
     if workload == "w4a8":
         k, nn = synth.W4A8_SHAPE

@@ -1,4 +1,4 @@
-// Decode GEMV (M <= 8 tokens): y[m, n] = sum_k x[m, k] * W[k, n], W dequantized in registers.
+// Decode GEMV (M <= 16 tokens): y[m, n] = sum_k x[m, k] * W[k, n], W dequantized in registers.
 //
 // Source of the operation: the M <= 8 branch of the AWQ dispatch snippet,
 // gemv_forward_cuda(inputs, qweight, scales, qzeros, group_size) ("Speed up AWQ
@@ -47,12 +47,20 @@
 //    fp16 rounding, a relative difference of at most 2^-11 per weight, far inside the
 //    output tolerance, and a cancellation of the 1024 offsets in fp32 that costs about
 //    eight of its 24 bits.
+//  * 9..16 tokens (gemv_kernel<16>): the same stages, with 16-token activation boxes; every
+//    dequantized A fragment feeds two mmas, one per 8-token half.  A per-group fold would need a
+//    second set of group sums and overflow the registers, so this variant makes W exactly as the
+//    dequant kernel does (HSUB2 of the zero, HMUL2 by the scale) and multiplies it straight into
+//    the accumulators; streaming the weights once for 16 tokens beats the tensor-core GEMM's
+//    16-token tiles by 1.3-2.9x.
 //  * Lane (g, t) of the mma reads rows 2t, 2t+1 (+8) of each 16-row step; with the
 //    128-byte swizzle those 32-bit shared-memory loads, and the activation loads, are
 //    free of bank conflicts, and every address is a lane constant plus an immediate.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
+
+#include <type_traits>
 
 #include "awq_internal.h"
 #include "awq_host.h"
@@ -81,17 +89,21 @@ constexpr int kUnitsPerStage = 2;              // 64-row units per stage: 2 = on
 constexpr int kUnitQBytes = kRows * kTileWords * 4;  // 16 KB of packed words per unit
 constexpr int kColStride = kUnitsPerStage * kBoxBytes;  // box (column half c, unit h) at c * kColStride + h * 8 KB
 constexpr int kQBytes = kUnitsPerStage * kUnitQBytes;
-constexpr int kXBoxBytes = kGemvMaxM * kRows * 2;  // 1 KB (one 128B-swizzled box, 8 tokens x 64)
-constexpr int kXBytes = kUnitsPerStage * kXBoxBytes;
 constexpr int kZBytes = kTileWords * 4;            // 256 B
 constexpr int kSBytes = kTileCols * 2;             // 1 KB
-constexpr int kXOff = kQBytes;
-constexpr int kZOff = kXOff + kXBytes;
-constexpr int kSOff = kZOff + kZBytes;
-constexpr int kStageBytes = ((kSOff + kSBytes) + 1023) / 1024 * 1024;
-constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 512;  // 1 KB alignment slack | ring | barriers, flags
-static_assert(kGemvMaxM * kTileCols * 4 <= kStageBytes, "a completer's own sums fit one ring slot");
-static_assert(kSmemBytes <= 227 * 1024, "shared memory budget of one CTA");
+// Stage layout for calls of up to T tokens: T = 8 (the folded kernel) or 16 (two 8-token halves)
+template <int T>
+struct Geo {
+  static constexpr int kXBoxBytes = T * kRows * 2;  // one 128B-swizzled box, T tokens x 64 (1 or 2 KB)
+  static constexpr int kXBytes = kUnitsPerStage * kXBoxBytes;
+  static constexpr int kXOff = kQBytes;
+  static constexpr int kZOff = kXOff + kXBytes;
+  static constexpr int kSOff = kZOff + kZBytes;
+  static constexpr int kStageBytes = ((kSOff + kSBytes) + 1023) / 1024 * 1024;
+  static constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 512;  // alignment slack | ring | barriers, flags
+  static_assert(T * kTileCols * 4 <= kStageBytes, "a completer's own sums fit one ring slot");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget of one CTA");
+};
 static_assert(kTileWords == kConsumers * 8, "one 8-word slice per consumer warp");
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
@@ -151,27 +163,30 @@ struct LaneOffsets {
   uint32_t x[4];  // activation pair k = 16i + 2t of token g for the four 16-row steps i
 };
 
+template <int T>
 __device__ __forceinline__ LaneOffsets lane_offsets(int word, int g, int t) {
   LaneOffsets o;
 #pragma unroll
   for (int c = 0; c < 2; ++c) o.q[c] = q_offset(2 * t + c, word);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) o.x[i] = kXOff + x_offset(g, 16 * i + 2 * t);
+  for (int i = 0; i < 4; ++i) o.x[i] = Geo<T>::kXOff + x_offset(g, 16 * i + 2 * t);
   return o;
 }
 
 // A consumer lane's share of one stage, copied out of shared memory so the slot can be
 // released before the arithmetic starts.
+template <int T>
 struct StageRegs {
-  uint32_t r[4][4];  // [16-row step][rows 2t, 2t+1, 2t+8, 2t+9]
-  uint32_t b[4][2];  // [16-row step][activation pairs k = 2t, 2t+8]
+  uint32_t r[4][4];         // [16-row step][rows 2t, 2t+1, 2t+8, 2t+9]
+  uint32_t b[T / 8][4][2];  // [8-token half][16-row step][activation pairs k = 2t, 2t+8]
 };
 
 // 64-row unit `hh` (0, 1) of the stage at `sb`
-__device__ __forceinline__ void load_stage(const uint8_t* sb, int hh, const LaneOffsets& lo, StageRegs& sr) {
+template <int T>
+__device__ __forceinline__ void load_stage(const uint8_t* sb, int hh, const LaneOffsets& lo, StageRegs<T>& sr) {
   const uint8_t* q0 = sb + hh * kBoxBytes + lo.q[0];
   const uint8_t* q1 = sb + hh * kBoxBytes + lo.q[1];
-  const uint8_t* xb = sb + hh * kXBoxBytes;
+  const uint8_t* xb = sb + hh * Geo<T>::kXBoxBytes;
 #pragma unroll
   for (int it = 0; it < 4; ++it) {
     const int base = 16 * it;  // (base + 2t + c) & 7 == (2t + c) & 7
@@ -179,9 +194,13 @@ __device__ __forceinline__ void load_stage(const uint8_t* sb, int hh, const Lane
     sr.r[it][1] = *reinterpret_cast<const uint32_t*>(q1 + base * 128);
     sr.r[it][2] = *reinterpret_cast<const uint32_t*>(q0 + (base + 8) * 128);
     sr.r[it][3] = *reinterpret_cast<const uint32_t*>(q1 + (base + 8) * 128);
-    // k + 8 is the neighbouring 16-byte chunk: physical chunk ^ 1, address ^ 16
-    sr.b[it][0] = *reinterpret_cast<const uint32_t*>(xb + lo.x[it]);
-    sr.b[it][1] = *reinterpret_cast<const uint32_t*>(xb + (lo.x[it] ^ 16u));
+    // k + 8 is the neighbouring 16-byte chunk: physical chunk ^ 1, address ^ 16; token g + 8 of the
+    // second half has the same swizzle, 8 rows (1 KB) further
+#pragma unroll
+    for (int h = 0; h < T / 8; ++h) {
+      sr.b[h][it][0] = *reinterpret_cast<const uint32_t*>(xb + h * 1024 + lo.x[it]);
+      sr.b[h][it][1] = *reinterpret_cast<const uint32_t*>(xb + h * 1024 + (lo.x[it] ^ 16u));
+    }
   }
 }
 
@@ -210,7 +229,7 @@ __device__ __forceinline__ void group_consts(uint32_t zword, const uint4& sv, Gr
 // so that it lands in the accumulator layout.  Each 16-row step is written as phases over its four
 // independent byte positions (PRMT, LOP3, mma) so that no instruction waits on the one issued just
 // before it.
-__device__ __forceinline__ void compute_stage(const StageRegs& sr, float (&acc)[4][4], float (&sx)[4]) {
+__device__ __forceinline__ void compute_stage(const StageRegs<8>& sr, float (&acc)[4][4], float (&sx)[4]) {
 #pragma unroll
   for (int it = 0; it < 4; ++it) {
     uint32_t p01[4], p23[4], a[4][4];
@@ -227,8 +246,69 @@ __device__ __forceinline__ void compute_stage(const StageRegs& sr, float (&acc)[
       a[b][3] = magic<0x00F000F0u>(p23[b]);
     }
 #pragma unroll
-    for (int b = 0; b < 4; ++b) mma16816(acc[b], a[b][0], a[b][1], a[b][2], a[b][3], sr.b[it][0], sr.b[it][1]);
-    mma16816(sx, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u, sr.b[it][0], sr.b[it][1]);
+    for (int b = 0; b < 4; ++b) mma16816(acc[b], a[b][0], a[b][1], a[b][2], a[b][3], sr.b[0][it][0], sr.b[0][it][1]);
+    mma16816(sx, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u, sr.b[0][it][0], sr.b[0][it][1]);
+  }
+}
+
+// Two-half (9..16 token) variant: each dequantized weight feeds two mmas, one per 8-token half, so the
+// weights are made exactly as the dequant kernel makes them, W = fp16_RN((q - z) s), and multiplied
+// straight into the fp32 accumulators (no per-group fold, which would need a second set of group
+// sums per half).  zlo / zhi = 1024 + z and 1024 + 16 z of slots 2b / 2b + 1 (both halves of the
+// register), slo / shi = s and s / 16.
+struct GroupConstsH {
+  uint32_t zlo[4], zhi[4], slo[4], shi[4];
+};
+
+__device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
+  __half2 r = __hsub2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  __half2 r = __hmul2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+// fp16 number `idx` (0..7) of an 8-half vector, in both halves of a register
+__device__ __forceinline__ uint32_t bcast_half(const uint4& v, int idx) {
+  const uint32_t w = idx < 2 ? v.x : idx < 4 ? v.y : idx < 6 ? v.z : v.w;
+  return (idx & 1) ? prmt(w, w, 0x3232u) : prmt(w, w, 0x1010u);
+}
+
+__device__ __forceinline__ void group_consts_h(uint32_t zword, const uint4& sv, GroupConstsH& c) {
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    const uint32_t zb = prmt(zword, zword, byte_sel(b));
+    c.zlo[b] = magic<0x000F000Fu>(zb);  // 1024 + z(slot 2b)
+    c.zhi[b] = magic<0x00F000F0u>(zb);  // 1024 + 16 z(slot 2b+1)
+    c.slo[b] = bcast_half(sv, order_map(2 * b));
+    c.shi[b] = hmul2(bcast_half(sv, order_map(2 * b + 1)), 0x2C002C00u);  // s / 16, exact
+  }
+}
+
+// acc[h] += W^T x_h over the 64 rows held in `sr`, for the two 8-token halves h.  HSUB2 of the zero
+// (exact) then HMUL2 by the scale (s / 16 for the 16 q of the high nibble) give W = fp16_RN((q - z) s).
+__device__ __forceinline__ void compute_stage16(const StageRegs<16>& sr, const GroupConstsH& c,
+                                                float (&acc)[2][4][4]) {
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    uint32_t p01[4], p23[4], a[4][4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      p01[b] = prmt(sr.r[it][0], sr.r[it][1], byte_sel(b));
+      p23[b] = prmt(sr.r[it][2], sr.r[it][3], byte_sel(b));
+    }
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      a[b][0] = hmul2(hsub2(magic<0x000F000Fu>(p01[b]), c.zlo[b]), c.slo[b]);
+      a[b][1] = hmul2(hsub2(magic<0x00F000F0u>(p01[b]), c.zhi[b]), c.shi[b]);
+      a[b][2] = hmul2(hsub2(magic<0x000F000Fu>(p23[b]), c.zlo[b]), c.slo[b]);
+      a[b][3] = hmul2(hsub2(magic<0x00F000F0u>(p23[b]), c.zhi[b]), c.shi[b]);
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int b = 0; b < 4; ++b)
+        mma16816(acc[h][b], a[b][0], a[b][1], a[b][2], a[b][3], sr.b[h][it][0], sr.b[h][it][1]);
   }
 }
 
@@ -260,6 +340,7 @@ struct StageWalk {
 constexpr int kMaxRegs = (65536 / 4) / (((kThreads / 32 + 3) / 4) * 32) / 8 * 8;
 static_assert(kMaxRegs == 168, "9 warps: three on one sub-partition");
 
+template <int T>
 __global__ void __maxnreg__(kMaxRegs)
 gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_x,
             const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_s, int has_z,
@@ -268,6 +349,13 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
   // RB = K / 64 row blocks per tile; unit u = (tile u / RB, row block u % RB); units < 2^31 (host check)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  using G = Geo<T>;
+  constexpr int kStageBytes = G::kStageBytes;
+  constexpr int kXBoxBytes = G::kXBoxBytes;
+  constexpr int kXOff = G::kXOff;
+  constexpr int kZOff = G::kZOff;
+  constexpr int kSOff = G::kSOff;
+  constexpr int kHalves = T / 8;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kStages);
   volatile int* ready_flag = abort_flag + 1;  // the designated tile's partials have all arrived
@@ -355,13 +443,14 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     const int g = lane >> 2;          // mma group: A rows g / g+8, B column (token) g
     const int t = lane & 3;           // mma thread-in-group
     const int word = warp * 8 + g;    // this lane's packed word column in the tile
-    const LaneOffsets lo = lane_offsets(word, g, t);
+    const LaneOffsets lo = lane_offsets<T>(word, g, t);
     bool waited = false;
     int part_tile = -1;               // a shared tile whose partial this CTA wrote (at most one)
     int own_tile = -1;                // the shared tile this CTA completes (it holds its first unit)
-    float hold[4][4];                 // own_tile's sums, kept in registers for its reduction
+    float hold[kHalves][4][4];        // own_tile's sums, kept in registers for its reduction
     bool failed = false;              // a wait ran out: error recorded, the rest of the call skipped
-    GroupConsts gc;                   // zero / scale constants of the current group (cached_grp)
+    // zero / scale constants of the current group (cached_grp)
+    typename std::conditional<T == 8, GroupConsts, GroupConstsH>::type gc;
     int cached_grp = -1;
     int i = 0;                        // stage counter, identical to the producer's
     int cst = 0;                      // its ring slot (i % kStages) and phase ((i / kStages) & 1)
@@ -369,11 +458,13 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     StageWalk w(u0, u1, RB);
     while (w.u < u1) {
       const int tile = w.tile;
-      float acc[4][4];
+      float acc[kHalves][4][4];
 #pragma unroll
-      for (int b = 0; b < 4; ++b)
+      for (int h = 0; h < kHalves; ++h)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc[b][e] = 0.f;
+        for (int b = 0; b < 4; ++b)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[h][b][e] = 0.f;
       cached_grp = -1;  // a new tile: other columns
       for (; w.u < u1 && w.tile == tile; ++i) {
         const int nh = w.units_here();
@@ -394,31 +485,44 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         }
         if (grp != cached_grp) {  // a stage never spans two groups
           const uint32_t zword = has_z ? reinterpret_cast<const uint32_t*>(sb + kZOff)[word] : 0x88888888u;
-          group_consts(zword, reinterpret_cast<const uint4*>(sb + kSOff)[word], gc);
+          if constexpr (T == 8) group_consts(zword, reinterpret_cast<const uint4*>(sb + kSOff)[word], gc);
+          else group_consts_h(zword, reinterpret_cast<const uint4*>(sb + kSOff)[word], gc);
           cached_grp = grp;
         }
-        float gacc[4][4], sx[4];  // this stage's (1024 + q)^T x and sum_k x
+        if constexpr (T == 8) {
+          float gacc[4][4], sx[4];  // this stage's (1024 + q)^T x and sum_k x
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          sx[b] = 0.f;
+          for (int b = 0; b < 4; ++b) {
+            sx[b] = 0.f;
 #pragma unroll
-          for (int e = 0; e < 4; ++e) gacc[b][e] = 0.f;
-        }
-        StageRegs sr;
-        load_stage(sb, 0, lo, sr);
-        if (nh == 2) {
+            for (int e = 0; e < 4; ++e) gacc[b][e] = 0.f;
+          }
+          StageRegs<8> sr;
+          load_stage<8>(sb, 0, lo, sr);
+          if (nh == 2) {
+            compute_stage(sr, gacc, sx);
+            load_stage<8>(sb, 1, lo, sr);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(empty_bar(st));  // slot free before the last unit's arithmetic
           compute_stage(sr, gacc, sx);
-          load_stage(sb, 1, lo, sr);
+          // the group's zero point and scale: acc += s (gacc - (1024 + z) sx)  (high nibble: s / 16, 1024 + 16 z)
+#pragma unroll
+          for (int b = 0; b < 4; ++b)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              acc[0][b][e] = fmaf(gacc[b][e], gc.sf[b][e >> 1], fmaf(-gc.szc[b][e >> 1], sx[e & 1], acc[0][b][e]));
+        } else {
+          StageRegs<16> sr;
+          load_stage<16>(sb, 0, lo, sr);
+          if (nh == 2) {
+            compute_stage16(sr, gc, acc);
+            load_stage<16>(sb, 1, lo, sr);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(empty_bar(st));  // slot free before the last unit's arithmetic
+          compute_stage16(sr, gc, acc);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(empty_bar(st));  // slot free before the last unit's arithmetic
-        compute_stage(sr, gacc, sx);
-        // the group's zero point and scale: acc += s (gacc - (1024 + z) sx)  (high nibble: s / 16, 1024 + 16 z)
-#pragma unroll
-        for (int b = 0; b < 4; ++b)
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            acc[b][e] = fmaf(gacc[b][e], gc.sf[b][e >> 1], fmaf(-gc.szc[b][e >> 1], sx[e & 1], acc[b][e]));
       }
       if (failed) break;
 
@@ -429,20 +533,22 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       }
       const int pf = (int)cta_of_unit(tile * RB, units, P);
       const int pl = (int)cta_of_unit((tile + 1) * RB - 1, units, P);
-      // D fragment: acc[b][0/1] = (slot 2b, tokens 2t / 2t+1), acc[b][2/3] = slot 2b+1: the lane holds
-      // all 8 columns of its word for tokens 2t and 2t+1, stored as one 16-byte (fp16) or two
-      // 16-byte (fp32) vectors per token
+      // D fragment of half h: acc[h][b][0/1] = (slot 2b, tokens 8h + 2t / 8h + 2t+1), acc[h][b][2/3] =
+      // slot 2b+1: the lane holds all 8 columns of its word for tokens 8h + 2t and 8h + 2t+1, stored as
+      // one 16-byte (fp16) or two 16-byte (fp32) vectors per token
       const int n0 = tile * kTileCols + word * 8;
       if (pf == pl) {
 #pragma unroll
+        for (int hf = 0; hf < kHalves; ++hf)
+#pragma unroll
         for (int par = 0; par < 2; ++par) {
-          const int m = 2 * t + par;
+          const int m = 8 * hf + 2 * t + par;
           if (m < M && n0 < N) {  // N % 32 == 0: the word's 8 columns are all in range
             uint32_t h[4];
 #pragma unroll
             for (int c = 0; c < 8; c += 2) {
               const int s0 = slot_of_col(c), s1 = slot_of_col(c + 1);
-              __half2 v = __floats2half2_rn(acc[s0 >> 1][(s0 & 1) * 2 + par], acc[s1 >> 1][(s1 & 1) * 2 + par]);
+              __half2 v = __floats2half2_rn(acc[hf][s0 >> 1][(s0 & 1) * 2 + par], acc[hf][s1 >> 1][(s1 & 1) * 2 + par]);
               h[c / 2] = *reinterpret_cast<uint32_t*>(&v);
             }
             *reinterpret_cast<uint4*>(y + (size_t)m * N + n0) = make_uint4(h[0], h[1], h[2], h[3]);
@@ -452,21 +558,25 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         // this CTA holds the tile's first unit, so the tile is the last of its range: it completes
         // the tile after its range, from these registers and the other contributors' partials
 #pragma unroll
-        for (int b = 0; b < 4; ++b)
+        for (int hf = 0; hf < kHalves; ++hf)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) hold[b][e] = acc[b][e];
+          for (int b = 0; b < 4; ++b)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) hold[hf][b][e] = acc[hf][b][e];
         own_tile = tile;
       } else {
-        float* slot = part + ((size_t)tile * maxc + (size_t)(p - pf)) * kGemvMaxM * kTileCols;
+        float* slot = part + ((size_t)tile * maxc + (size_t)(p - pf)) * T * kTileCols;
+#pragma unroll
+        for (int hf = 0; hf < kHalves; ++hf)
 #pragma unroll
         for (int par = 0; par < 2; ++par) {
-          const int m = 2 * t + par;
+          const int m = 8 * hf + 2 * t + par;
           if (m < M) {
             float v[8];
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
               const int sl = slot_of_col(c);
-              v[c] = acc[sl >> 1][(sl & 1) * 2 + par];
+              v[c] = acc[hf][sl >> 1][(sl & 1) * 2 + par];
             }
             float4* dst = reinterpret_cast<float4*>(slot + m * kTileCols + word * 8);
             dst[0] = make_float4(v[0], v[1], v[2], v[3]);
@@ -515,14 +625,16 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       float* own = reinterpret_cast<float*>(smem);
       consumers_sync();
 #pragma unroll
+      for (int hf = 0; hf < kHalves; ++hf)
+#pragma unroll
       for (int par = 0; par < 2; ++par) {
-        const int m = 2 * t + par;
+        const int m = 8 * hf + 2 * t + par;
         if (m < M) {
           float v[8];
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             const int sl = slot_of_col(c);
-            v[c] = hold[sl >> 1][(sl & 1) * 2 + par];
+            v[c] = hold[hf][sl >> 1][(sl & 1) * 2 + par];
           }
           float4* dst = reinterpret_cast<float4*>(own + m * kTileCols + word * 8);
           dst[0] = make_float4(v[0], v[1], v[2], v[3]);
@@ -531,45 +643,48 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       }
       consumers_sync();
       if (*ready_flag) {
-        // items (token, 4 columns): up to four per thread, each with eight contributors' loads in flight
+        // items (token, 4 columns): up to four per thread at a time, each with eight contributors' loads in
+        // flight
         constexpr int kQuads = kTileCols / 4;
         constexpr int kThreadsC = kConsumers * 32;
         const int items = M * kQuads;
-        const float4* base = reinterpret_cast<const float4*>(part + (size_t)own_tile * maxc * kGemvMaxM * kTileCols);
-        constexpr size_t kSlotQuads = (size_t)kGemvMaxM * kQuads;
-        float4 s4[4];
+        const float4* base = reinterpret_cast<const float4*>(part + (size_t)own_tile * maxc * T * kTileCols);
+        constexpr size_t kSlotQuads = (size_t)T * kQuads;
+        for (int i0 = threadIdx.x; i0 < items; i0 += 4 * kThreadsC) {
+          float4 s4[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int it = threadIdx.x + k * kThreadsC;
-          s4[k] = it < items ? reinterpret_cast<const float4*>(own)[it] : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        for (int j0 = 1; j0 < nt; j0 += 8) {
-          float4 a[4][8];
+          for (int k = 0; k < 4; ++k) {
+            const int it = i0 + k * kThreadsC;
+            s4[k] = it < items ? reinterpret_cast<const float4*>(own)[it] : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+          for (int j0 = 1; j0 < nt; j0 += 8) {
+            float4 a[4][8];
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
+            for (int k = 0; k < 4; ++k)
 #pragma unroll
-            for (int jj = 0; jj < 8; ++jj) {
-              const int it = threadIdx.x + k * kThreadsC;
-              a[k][jj] = (it < items && j0 + jj < nt) ? __ldcg(base + (size_t)(j0 + jj) * kSlotQuads + it)
-                                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+              for (int jj = 0; jj < 8; ++jj) {
+                const int it = i0 + k * kThreadsC;
+                a[k][jj] = (it < items && j0 + jj < nt) ? __ldcg(base + (size_t)(j0 + jj) * kSlotQuads + it)
+                                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+              }
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+#pragma unroll
+              for (int jj = 0; jj < 8; ++jj) {
+                s4[k].x += a[k][jj].x; s4[k].y += a[k][jj].y; s4[k].z += a[k][jj].z; s4[k].w += a[k][jj].w;
+              }
+          }
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int it = i0 + k * kThreadsC;
+            if (it >= items) continue;
+            const int m = it / kQuads;
+            const int n = own_tile * kTileCols + (it - m * kQuads) * 4;
+            if (n < N) {  // N % 32 == 0: all four outputs are in range
+              __half2* dst = reinterpret_cast<__half2*>(y + (size_t)m * N + n);
+              dst[0] = __floats2half2_rn(s4[k].x, s4[k].y);
+              dst[1] = __floats2half2_rn(s4[k].z, s4[k].w);
             }
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-#pragma unroll
-            for (int jj = 0; jj < 8; ++jj) {
-              s4[k].x += a[k][jj].x; s4[k].y += a[k][jj].y; s4[k].z += a[k][jj].z; s4[k].w += a[k][jj].w;
-            }
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int it = threadIdx.x + k * kThreadsC;
-          if (it >= items) continue;
-          const int m = it / kQuads;
-          const int n = own_tile * kTileCols + (it - m * kQuads) * 4;
-          if (n < N) {  // N % 32 == 0: all four outputs are in range
-            __half2* dst = reinterpret_cast<__half2*>(y + (size_t)m * N + n);
-            dst[0] = __floats2half2_rn(s4[k].x, s4[k].y);
-            dst[1] = __floats2half2_rn(s4[k].z, s4[k].w);
           }
         }
       }
@@ -631,17 +746,18 @@ GemvPlan gemv_plan(int64_t M, int64_t K, int64_t N, int split_k) {
 }
 
 size_t gemv_workspace_bytes(const GemvPlan& p, int64_t M, int64_t N) {
-  (void)M;
   (void)N;
   if (p.maxc <= 1) return 0;
-  return kCounterBytes + align256((size_t)p.tiles * p.maxc * kGemvMaxM * kTileCols * sizeof(float));
+  const size_t tokens = M <= 8 ? 8 : 16;  // token rows of a partial: the kernel's T
+  return kCounterBytes + align256((size_t)p.tiles * p.maxc * tokens * kTileCols * sizeof(float));
 }
 
-cudaError_t launch_gemv(const uint16_t* x, const uint32_t* qw, const uint32_t* qz, const uint16_t* sc,
-                        uint16_t* y, int64_t M, int64_t K, int64_t N, const GemvPlan& p, void* ws,
-                        int* err, cudaStream_t s) {
-  // the kernel counts (tile, 64-row block) units in 32 bits; any tensor that fits a GPU stays far below
-  if ((int64_t)p.tiles * p.groups >= ((int64_t)1 << 31)) return cudaErrorInvalidValue;
+namespace {
+
+template <int T>
+cudaError_t launch_gemv_t(const uint16_t* x, const uint32_t* qw, const uint32_t* qz, const uint16_t* sc,
+                          uint16_t* y, int64_t M, int64_t K, int64_t N, const GemvPlan& p, void* ws, int* err,
+                          cudaStream_t s) {
   float* part = nullptr;
   int* counters = nullptr;
   if (p.maxc > 1) {
@@ -654,14 +770,15 @@ cudaError_t launch_gemv(const uint16_t* x, const uint32_t* qw, const uint32_t* q
   const bool ok =
       make_map_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, qw, nw, (uint64_t)K, kBoxWords, kRows,
                   CU_TENSOR_MAP_SWIZZLE_128B) &&
-      make_map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x, (uint64_t)K, (uint64_t)M, kRows, kGemvMaxM,
+      make_map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x, (uint64_t)K, (uint64_t)M, kRows, T,
                   CU_TENSOR_MAP_SWIZZLE_128B) &&
       make_map_2d(&tz, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, qz ? (const void*)qz : (const void*)qw, nw,
                   qz ? ng : (uint64_t)K, kTileWords, 1, CU_TENSOR_MAP_SWIZZLE_NONE) &&
       make_map_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, sc, (uint64_t)N / 2, ng, kTileCols / 2, 1,
                   CU_TENSOR_MAP_SWIZZLE_NONE);
   if (!ok) return cudaErrorInvalidValue;
-  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(gemv_kernel), kSmemBytes);
+  constexpr int kSmemBytes = Geo<T>::kSmemBytes;
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(gemv_kernel<T>), kSmemBytes);
   if (e != cudaSuccess) return e;
 
   cudaLaunchConfig_t cfg = {};
@@ -674,10 +791,21 @@ cudaError_t launch_gemv(const uint16_t* x, const uint32_t* qw, const uint32_t* q
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, gemv_kernel, tq, tx, tz, ts, qz ? 1 : 0, reinterpret_cast<__half*>(y), part, counters,
-                         err, (int)M, (int)N, (int)(K / kRows), p.tiles, p.maxc);
+  e = cudaLaunchKernelEx(&cfg, gemv_kernel<T>, tq, tx, tz, ts, qz ? 1 : 0, reinterpret_cast<__half*>(y), part,
+                         counters, err, (int)M, (int)N, (int)(K / kRows), p.tiles, p.maxc);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemv(const uint16_t* x, const uint32_t* qw, const uint32_t* qz, const uint16_t* sc,
+                        uint16_t* y, int64_t M, int64_t K, int64_t N, const GemvPlan& p, void* ws,
+                        int* err, cudaStream_t s) {
+  // the kernel counts (tile, 64-row block) units in 32 bits; any tensor that fits a GPU stays far below
+  if ((int64_t)p.tiles * p.groups >= ((int64_t)1 << 31)) return cudaErrorInvalidValue;
+  if (M <= 8) return launch_gemv_t<8>(x, qw, qz, sc, y, M, K, N, p, ws, err, s);
+  return launch_gemv_t<16>(x, qw, qz, sc, y, M, K, N, p, ws, err, s);
 }
 
 }  // namespace awq

@@ -18,7 +18,7 @@ static_assert(order_map(0) == 0 && order_map(1) == 2 && order_map(3) == 6 && ord
               "AWQ order map");
 
 constexpr int kGroup = 128;          // GPU path group size (input channels per scale)
-constexpr int kGemvMaxM = 8;         // decode path handles up to 8 tokens
+constexpr int kGemvMaxM = 16;        // decode path handles up to 16 tokens (two 8-token halves above 8)
 constexpr int kW4A8MaxKSlice = 16384;  // exact-integer bound of an fp32 tensor-core sum
 
 // Workspace layout shared by every split-K call: a fixed 64 KB block of tile

@@ -98,10 +98,12 @@ awq_status awq_dequant(const int32_t *qweight, const int32_t *qzeros, const uint
 size_t awq_workspace_bytes(awq_op op, int64_t M, int64_t K, int64_t N, int32_t split_k);
 
 /*
- * awq_gemv -- y = x * W for M <= 8 tokens (decode), W dequantized on the fly.
+ * awq_gemv -- y = x * W for M <= 16 tokens (decode), W dequantized on the fly.
  * x fp16 [M, K]; qweight int32 [K, N/8]; qzeros int32 [K/128, N/8] or NULL
  * (symmetric, z = 8); scales fp16 [K/128, N]; y fp16 [M, N] (output).
- * 1 <= M <= 8 (0 = no-op), K % 128 == 0, N % 32 == 0, group_size == 128.
+ * 1 <= M <= 16 (0 = no-op), K % 128 == 0, N % 32 == 0, group_size == 128.
+ * M > 8 runs as two 8-token halves sharing each dequantized weight, which is
+ * made as W = fp16_RN((q - z) * s) like awq_dequant's.
  * split_k: number of CTAs per 512-column tile, whose K slices are reduced in
  * fp32 (0 = automatic: a persistent grid of one CTA per SM, each owning an
  * equal share of the (tile, 64-row block) units; 1 = one CTA per tile, no
@@ -112,9 +114,10 @@ size_t awq_workspace_bytes(awq_op op, int64_t M, int64_t K, int64_t N, int32_t s
  * other kernel holding SMs indefinitely).  The fp16 output is rounded once
  * from the fp32 sum, adding the partials in a fixed order (bit-reproducible).
  * Needs a workspace when a tile is shared by several CTAs
- * (awq_workspace_bytes() > 0).  The group's zero point and scale are applied
- * to fp32 sums of the integer codes, so the products use s * (q - z) in fp32
- * rather than its fp16 rounding (well inside the fp16 output tolerance).
+ * (awq_workspace_bytes() > 0).  For M <= 8 the group's zero point and scale
+ * are applied to fp32 sums of the integer codes, so the products use
+ * s * (q - z) in fp32 rather than its fp16 rounding (well inside the fp16
+ * output tolerance).
  * Source: the M <= 8 branch of the dispatch snippet, gemv_forward_cuda(inputs,
  * qweight, scales, qzeros, group_size) ("Speed up AWQ 2.5x with updated kernel").
  */

@@ -53,7 +53,7 @@ def _gemv(awq, M=1, K=4096, N=4096, g=128, split=0, x=FAKE, qw=FAKE, qz=FAKE, sc
 
 
 def test_gemv_rejects_bad_shapes_before_launch(awq):
-    assert _gemv(awq, M=9) == EINVAL
+    assert _gemv(awq, M=17) == EINVAL          # the decode kernel takes up to 16 tokens
     assert _gemv(awq, M=-1) == EINVAL
     assert _gemv(awq, K=100) == EINVAL
     assert _gemv(awq, N=24) == EINVAL
@@ -103,6 +103,8 @@ def test_workspace_layout(awq):
     # GEMV: counters block + split x M x N fp32 partials (256-byte rounded)
     assert awq.awq_workspace_bytes(awq.OP_GEMV, 8, 4096, 4096, 1) == 0
     assert awq.awq_workspace_bytes(awq.OP_GEMV, 8, 4096, 4096, 4) == counters + 4 * 8 * 4096 * 4
+    # 9..16 tokens: partials carry 16 token rows
+    assert awq.awq_workspace_bytes(awq.OP_GEMV, 12, 4096, 4096, 4) == counters + 4 * 16 * 4096 * 4
     # W4A8 at K = 21760: one M-block per CTA with two exact accumulators (16384 rows each) covers K
     # without a split
     x16 = 4096 * 21760 * 2

@@ -114,7 +114,7 @@ def test_gemv_tiny_config(awq):
 
 @pytest.mark.parametrize("symmetric", [False, True])
 @pytest.mark.parametrize("split_k", [1, 3, 0])
-@pytest.mark.parametrize("M", [1, 2, 3, 5, 8])
+@pytest.mark.parametrize("M", [1, 2, 3, 5, 8, 9, 13, 16])
 def test_gemv_small_ragged(awq, M, split_k, symmetric):
     # N = 416: 52 packed words, 4 column tiles with a ragged last tile; K = 1280: 10 groups
     p = synth.awq_problem(M, 1280, 416, seed=100 + M, symmetric=symmetric)
@@ -123,7 +123,7 @@ def test_gemv_small_ragged(awq, M, split_k, symmetric):
     assert_within_tol(y, ref, f"gemv M={M} split={split_k} sym={symmetric}")
 
 
-@pytest.mark.parametrize("M", [1, 8])
+@pytest.mark.parametrize("M", [1, 8, 16])
 @pytest.mark.parametrize("name,K,N", synth.LLAMA2_7B_DECODE)
 def test_gemv_llama2_shapes_sampled(awq, name, K, N, M):
     p = synth.awq_problem(M, K, N, seed=1000 + K + N + M)
@@ -134,7 +134,7 @@ def test_gemv_llama2_shapes_sampled(awq, name, K, N, M):
 
 
 @pytest.mark.parametrize("xkind", ["positive_offset", "common_mode", "outliers"])
-@pytest.mark.parametrize("M", [1, 8])
+@pytest.mark.parametrize("M", [1, 8, 16])
 def test_gemv_activation_offsets(awq, M, xkind):
     # The decode kernel applies each group's zero point and scale to fp32 sums of (1024 + q) x, so
     # activations with a large common component cancel the most bits; they stay inside the tolerance.
@@ -212,7 +212,7 @@ def test_gemm_largest_prefill_sampled_rows(awq):
     assert_within_tol(y[np.ix_(rows, cols)], ref, "gemm gate_up M=8192")
 
 
-@pytest.mark.parametrize("M", [1, 8])
+@pytest.mark.parametrize("M", [1, 8, 12, 16])
 def test_gemm_and_gemv_agree_at_small_m(awq, M):
     p = synth.awq_problem(M, 4096, 6144, seed=400 + M, symmetric=(M == 8))
     yv = run_w4a16(awq, awq.awq_gemv, p).astype(np.float64)

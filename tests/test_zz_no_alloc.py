@@ -46,6 +46,7 @@ def _noalloc_via_abi(awq, x, qw, qz, sc, y, split_k):
     (8, 4096, 12288, 0, False),   # automatic split: the fixed scratch array is used
     (3, 1280, 416, 3, True),      # explicit split, ragged column tile, symmetric
     (1, 11008, 4096, 0, False),
+    (16, 4096, 22016, 0, False),  # two 8-token halves: twice the partial rows per contributor
 ])
 def test_noalloc_matches_gemv_on_two_calls_in_a_row(awq, M, K, N, split_k, symmetric):
     p = synth.awq_problem(M, K, N, seed=900 + M + K, symmetric=symmetric)
