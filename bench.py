@@ -283,6 +283,20 @@ def issue_step(awq, bufs, stream):
     return launches
 
 
+def max_over_ranks(values, torch, dist, device):
+    """Element-wise maximum of `values` (times) over all ranks of `dist` (None: one rank)."""
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t]
+
+
+def whole_job_rate(units_per_rank_step, world, step_s):
+    """Weak scaling: every rank processes `units_per_rank_step` per step; the job's rate is all ranks'
+    units over the slowest rank's step time."""
+    return units_per_rank_step * world / step_s
+
+
 def gpu_arm(args, rank, world, torch, dist):
     from bit_weight_only_awq_gb300 import build as awq_build
     awq_build.build()
@@ -362,11 +376,7 @@ def gpu_arm(args, rank, world, torch, dist):
     barrier()
     e2e_s = time.perf_counter() - t0
 
-    # max over ranks
-    t = torch.tensor([ms, e2e_s], dtype=torch.float64, device=device)
-    if dist is not None:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms, e2e_s = float(t[0]), float(t[1])
+    ms, e2e_s = max_over_ranks([ms, e2e_s], torch, dist, device)
     return {
         "awq": awq, "calls": calls, "step_bytes": step_bytes, "step_flops": step_flops, "ms": ms,
         "e2e_s": e2e_s, "clocks": clocks, "launches_per_step": launches_per_step,
@@ -455,8 +465,8 @@ def main():
 
     r = gpu_arm(args, rank, world, torch, dist)
     step_s = r["ms"] / 1e3 / args.steps
-    gbs = r["step_bytes"] * world / step_s / 1e9
-    tfs = r["step_flops"] * world / step_s / 1e12
+    gbs = whole_job_rate(r["step_bytes"], world, step_s) / 1e9
+    tfs = whole_job_rate(r["step_flops"], world, step_s) / 1e12
     value = gbs if unit == "GB/s" else tfs
     e2e_step_s = r["e2e_s"] / args.steps
     e2e_value = (r["step_bytes"] * world / e2e_step_s / 1e9) if unit == "GB/s" else \
