@@ -49,7 +49,9 @@ constexpr int kBN = 128;         // weight columns per MMA (M) = per M-block
 constexpr int kDqGroupWarps = 8;              // one group dequantizes one stage (256 threads)
 constexpr int kDqGroups = 2;                  // groups alternate stages to overlap their latency
 constexpr int kDqWarps = kDqGroupWarps * kDqGroups;
-constexpr int kThreads = (3 + kDqWarps) * 32;   // x producer, MMA, q producer, dequant
+// Dequant warp rank of warp w >= 3 when the warps that share the mma warp's sub-partition (w % 4 == 1)
+// are left out of the dequantization.
+__device__ __forceinline__ int dq_rank_solo(int w) { return (w - 3) - ((w + 2) / 4 - 1); }
 constexpr int kWBlockBytes = kBK * kBN * 2;     // dequantized tile of one M-block, 16 KB
 
 template <int MODE>
@@ -81,6 +83,13 @@ struct Cfg {
   static constexpr int kSmem = kXStages * kXSlotBytes + kFixed + 1024;
   static constexpr int kAccs = MODE == kModeW4A8 ? 2 : 1;  // W4A8: one accumulator per exact K chunk (two)
   static constexpr int kTmemCols = NB * kAccs * BT < 32 ? 32 : NB * kAccs * BT;
+  // Warps: 0 copies activations, 1 issues the mmas (one thread), 2 copies packed weights, 16 dequantize.
+  // With tiles of at most 64 tokens the mmas are short and their issue rate limits the k-step, so
+  // the dequant warps skip the mma warp's sub-partition (warp % 4 == 1): 24 warps, of which 4..19 run
+  // the epilogue (measured 10-12 % faster at 16-64 tokens, 3-5 % slower with larger tiles).
+  static constexpr bool kSoloMma = BT <= 64;
+  static constexpr int kWarps = kSoloMma ? 24 : 3 + kDqWarps;
+  static constexpr int kThreads = kWarps * 32;
   // tcgen05 instruction descriptor, kind::f16: D f32, A/B f16, A MN-major, B K-major, M=128, N=BT
   static constexpr uint32_t kIdesc = (1u << 4) | (1u << 15) | ((uint32_t)(BT >> 3) << 17) |
                                      ((uint32_t)(kBN >> 4) << 24);
@@ -124,7 +133,7 @@ __device__ __forceinline__ uint32_t pair_magic(uint32_t w, int j) {
 
 // ------------------------------------------------------------------ kernel
 template <int BT, int NB, int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<BT, NB, MODE>::kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_q,
             const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_s,
             __half* __restrict__ y, int32_t* __restrict__ acc_out, const float* __restrict__ s_tok,
@@ -287,15 +296,20 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     }
   } else {
     // ------------------------------------------------ dequant warps (two groups, alternate k-steps)
-    const int group = (threadIdx.x - 96) / (kDqGroupWarps * 32);
-    const int d = (threadIdx.x - 96) % (kDqGroupWarps * 32);  // 0..255 within the group
+    int group = (threadIdx.x - 96) / (kDqGroupWarps * 32);
+    int d = (threadIdx.x - 96) % (kDqGroupWarps * 32);  // 0..255 within the group
+    if (C::kSoloMma) {
+      const int rk = dq_rank_solo(warp);
+      group = rk / kDqGroupWarps;
+      d = (rk % kDqGroupWarps) * 32 + lane;
+    }
     constexpr int kRowsPerPass = kDqGroupWarps * 32 / kQWords;  // 16 (NB = 1) or 8 (NB = 2)
     constexpr int kPasses = kBK / kRowsPerPass;                   // rows per thread: 4 NB
     const int c = d % kQWords;       // packed word column within the tile (M-block c / 16)
     const int r0 = d / kQWords;      // first of the thread's rows (r0 + kRowsPerPass j)
     const int cw = c & 15;           // word column within its M-block
     const uint32_t blk_off = (uint32_t)((c >> 4) * kWBlockBytes);
-    for (int it = group; it < nsteps; it += kDqGroups) {
+    for (int it = (C::kSoloMma && warp % 4 == 1) ? nsteps : group; it < nsteps; it += kDqGroups) {
       const int qs = it % kQStages, ws = it % kWStages;
       if (!wait_bounded(fullq(qs), (uint32_t)(it / kQStages) & 1u, abort_flag, err, 301)) break;
       if (!wait_bounded(wempty(ws), ((uint32_t)(it / kWStages) & 1u) ^ 1u, abort_flag, err, 302)) break;
@@ -338,11 +352,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     }
 
     // ------------------------------------------------ epilogue (dequant group b reads M-block b)
+    if (C::kSoloMma) {  // warps 4..19
+      group = warp >= 4 ? (warp - 4) / kDqGroupWarps : NB;
+      d = ((warp - 4) % kDqGroupWarps) * 32 + lane;
+    }
     if (group < NB) {
     const bool have = wait_bounded(accf_bar, 0, abort_flag, err, 401);
     tc_fence_after();
     const int lq = warp & 3;                 // TMEM lane quarter this warp may access
-    const int half = ((warp - 3) & 7) >> 2;  // which half of the BT token columns
+    const int half = ((warp - (C::kSoloMma ? 4 : 3)) & 7) >> 2;  // which half of the BT token columns
     const int nl = lq * 32 + lane;           // TMEM lane = weight column in the M-block
     const int n = n0 + group * kBN + nl;
     const uint32_t dcol = (uint32_t)(group * BT);  // this M-block's accumulator
@@ -454,7 +472,7 @@ cudaError_t launch_t(const uint16_t* x16, const uint32_t* qw, const uint32_t* qz
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), C::kSmem);
   if (e != cudaSuccess) return e;
   dim3 grid(p.n_tiles, p.m_tiles, p.split);
-  kern<<<grid, kThreads, C::kSmem, s>>>(tx, tq, tz, ts, reinterpret_cast<__half*>(y), acc_out, s_tok,
+  kern<<<grid, C::kThreads, C::kSmem, s>>>(tx, tq, tz, ts, reinterpret_cast<__half*>(y), acc_out, s_tok,
                                        reinterpret_cast<const __half*>(s_ch), part, counters, err, (int)M,
                                        (int)N, (int)K, p.ksteps, kW4A8MaxKSlice / kBK);
   return cudaGetLastError();
