@@ -415,19 +415,42 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
       asm volatile("bar.sync 1, %0;" ::"r"(NB * kDqGroupWarps * 32) : "memory");
       if (*last_flag) {
         __threadfence();
-        for (int cb = half * kHalf; cb < (half + 1) * kHalf; ++cb) {
-          const int m = m0 + cb;
-          if (!n_ok || m >= M) continue;
-          const size_t o = (size_t)m * N + n;
-          if (kIsW4A8<MODE>) {
-            int a = 0;
-            for (int sp = 0; sp < split; ++sp) a += __ldcg(reinterpret_cast<const int32_t*>(part) + (size_t)sp * M * N + o);
-            if (acc_out) acc_out[o] = a;
-            y[o] = __float2half_rn(__fmul_rn(__fmul_rn((float)a, s_tok[m]), sch));
-          } else {
-            float a = 0.f;
-            for (int sp = 0; sp < split; ++sp) a += __ldcg(reinterpret_cast<const float*>(part) + (size_t)sp * M * N + o);
-            y[o] = __float2half_rn(a);
+        // the split slices of kChunk tokens, two slices at a time, all their loads in flight together;
+        // each sum still runs over the slices in order (0 + s0 + s1 + ...)
+        constexpr int kChunk = kHalf < 8 ? kHalf : 8;
+        using P = typename std::conditional<kIsW4A8<MODE>, int32_t, float>::type;
+        const P* pp = reinterpret_cast<const P*>(part);
+        const size_t slice = (size_t)M * N;
+        for (int cb0 = half * kHalf; n_ok && cb0 < (half + 1) * kHalf && m0 + cb0 < M; cb0 += kChunk) {
+          P a[kChunk];
+#pragma unroll
+          for (int j = 0; j < kChunk; ++j) a[j] = P(0);
+          for (int sp = 0; sp < split; sp += 2) {
+            P v0[kChunk], v1[kChunk];
+#pragma unroll
+            for (int j = 0; j < kChunk; ++j) {
+              const int m = m0 + cb0 + j;
+              const size_t o = (size_t)m * N + n;
+              v0[j] = m < M ? __ldcg(pp + (size_t)sp * slice + o) : P(0);
+              v1[j] = (m < M && sp + 1 < split) ? __ldcg(pp + (size_t)(sp + 1) * slice + o) : P(0);
+            }
+#pragma unroll
+            for (int j = 0; j < kChunk; ++j) {
+              a[j] += v0[j];
+              if (sp + 1 < split) a[j] += v1[j];
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < kChunk; ++j) {
+            const int m = m0 + cb0 + j;
+            if (m >= M) break;
+            const size_t o = (size_t)m * N + n;
+            if constexpr (kIsW4A8<MODE>) {
+              if (acc_out) acc_out[o] = a[j];
+              y[o] = __float2half_rn(__fmul_rn(__fmul_rn((float)a[j], s_tok[m]), sch));
+            } else {
+              y[o] = __float2half_rn(a[j]);
+            }
           }
         }
         if (group == 0 && d == 0) atomicExch(counters + blockIdx.y * gridDim.x + blockIdx.x, 0);
