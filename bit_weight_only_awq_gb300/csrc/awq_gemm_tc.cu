@@ -529,9 +529,24 @@ cudaError_t launch_mode(const uint16_t* x16, const uint32_t* qw, const uint32_t*
 
 }  // namespace
 
+namespace {
+
+// The split that fills one wave of 152 CTAs (largest split <= 8 with at least min_slice k-steps per
+// slice), 1 if the unsplit grid already has a wave.
+int fill_split(int64_t tiles, int total_k, int min_slice) {
+  int sp = 1;
+  if (tiles < 152 && tiles <= kMaxCounters)
+    for (int s = 2; s <= 8; ++s)
+      if (tiles * s <= 152 && total_k / s >= min_slice) sp = s;
+  return sp;
+}
+
+}  // namespace
+
 GemmPlan gemm_plan(int64_t M, int64_t K, int64_t N, int split_k, int mode) {
   GemmPlan p;
   const int bt0 = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
+  const int total = (int)(K / kBK);
   auto tiles = [&](int bt, int nb) {
     return ((N + (int64_t)nb * kBN - 1) / ((int64_t)nb * kBN)) * ((M + bt - 1) / bt);
   };
@@ -549,11 +564,11 @@ GemmPlan gemm_plan(int64_t M, int64_t K, int64_t N, int split_k, int mode) {
     while (bt > 128 && tiles(bt, 2) < 114) bt /= 2;
     // under a wave, a K split with slices of at least 32 k-steps may fill it (M = 256, K = 14336,
     // N = 4096: 104 -> 76 us); shorter slices measured slower than one M-block without a split
-    const int total_k = (int)(K / kBK);
-    int sp_fill = 1;
-    if (split_k <= 0)
-      for (int sp = 2; sp <= 8; ++sp)
-        if (tiles(bt, 2) * sp <= 152 && total_k / sp >= 32) sp_fill = sp;
+    // (K = 4096, N = 4096: 31 -> 37 us with slices of 16), except where one M-block needs a second
+    // wave: W4A16 then takes slices of 16 (M = 256, K = 4096, N = 6144: 58 -> 39 us)
+    const int64_t waves1 = (tiles(p.bt, 1) + 151) / 152;
+    const int min_slice = (mode != kModeW4A8 && waves1 > 1) ? 16 : 32;
+    const int sp_fill = split_k > 0 ? 1 : fill_split(tiles(bt, 2), total, min_slice);
     if (tiles(bt, 2) * sp_fill >= 114) {
       p.nb = 2;
       p.bt = bt;
@@ -561,17 +576,9 @@ GemmPlan gemm_plan(int64_t M, int64_t K, int64_t N, int split_k, int mode) {
   }
   p.n_tiles = (int)((N + (int64_t)p.nb * kBN - 1) / ((int64_t)p.nb * kBN));
   p.m_tiles = (int)((M + p.bt - 1) / p.bt);
-  const int total = (int)(K / kBK);
-  int split = split_k;
-  if (split <= 0) {
-    // fill the 152 SMs: largest split (<= 8, >= 8 k-steps per slice) whose CTA count stays <= one wave,
-    // if the unsplit grid is under one wave
-    const int tiles = p.n_tiles * p.m_tiles;
-    split = 1;
-    if (tiles < 152 && tiles <= kMaxCounters)
-      for (int sp = 2; sp <= 8; ++sp)
-        if (tiles * sp <= 152 && total / sp >= 8) split = sp;
-  }
+  // fill the 152 SMs: largest split (<= 8, >= 8 k-steps per slice) whose CTA count stays <= one wave,
+  // if the unsplit grid is under one wave
+  int split = split_k > 0 ? split_k : fill_split((int64_t)p.n_tiles * p.m_tiles, total, 8);
   if (mode == kModeW4A8) {
     // exact accumulators: each K slice spans at most 2 x 16384 rows with one M-block (two
     // accumulators), at most 16384 with two M-blocks (one each)
