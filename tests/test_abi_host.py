@@ -119,6 +119,24 @@ def test_workspace_layout(awq):
     assert awq.awq_workspace_bytes(awq.OP_GEMM, 16, 100, 4096, 0) == 0
 
 
+def test_gemm_plan_split_choices(awq):
+    # The automatic GEMM plan shows in the workspace it asks for: the counters block plus
+    # split x M x N fp32 partials when it splits K, nothing otherwise.
+    counters = 65536
+    ws = lambda M, K, N: awq.awq_workspace_bytes(awq.OP_GEMM, M, K, N, 0)
+    # one M-block fits one wave (128 CTAs of 64 tokens): no split
+    assert ws(256, 4096, 4096) == 0
+    # one M-block would need a second wave (192 CTAs): two M-blocks with a split of three
+    assert ws(256, 4096, 6144) == counters + 3 * 256 * 6144 * 4
+    # two M-blocks fill the wave with slices of 56 k-steps: split of four
+    assert ws(256, 14336, 4096) == counters + 4 * 256 * 4096 * 4
+    # under a wave with one M-block: the largest split that stays within one wave (32 x 4 CTAs)
+    assert ws(64, 4096, 4096) == counters + 4 * 64 * 4096 * 4
+    # a full wave without splitting
+    assert ws(64, 4096, 28672) == 0
+    assert ws(1024, 4096, 6144) == 0
+
+
 def test_selftest_rejects_bad_limits_before_launch(awq):
     assert awq.lib.awq_selftest_wait_timeout(0, None) == EINVAL
     assert awq.lib.awq_selftest_wait_timeout(-5, None) == EINVAL
