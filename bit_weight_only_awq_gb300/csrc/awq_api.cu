@@ -121,6 +121,19 @@ static bool gemm_shape_ok(int64_t M, int64_t K, int64_t N, int32_t split_k) {
          N % 32 == 0 && N <= (int64_t)1 << 30 && split_k >= 0 && M * N < ((int64_t)1 << 40);
 }
 
+// W4A8 with at most 16 tokens runs on the 16-token GEMV (exact products, int32 reduction) when its plan
+// keeps every CTA's rows of a tile within 16384; otherwise, and for more tokens, on the GEMM.
+static bool w4a8_on_gemv(int64_t M, int64_t K, int64_t N, int32_t split_k, GemvPlan* plan) {
+  if (M < 1 || M > kGemvMaxM) return false;
+  *plan = gemv_plan(M, K, N, split_k);
+  return gemv_w4a8_ok(*plan, M);
+}
+// counters | fp16 copy of the codes | GEMV partials (16 token rows per slot)
+static size_t w4a8_gemv_workspace_bytes(const GemvPlan& p, int64_t M, int64_t K, int64_t N) {
+  const size_t part = gemv_workspace_bytes(p, 16, N);
+  return kCounterBytes + align256((size_t)M * (size_t)K * 2) + (part ? part - kCounterBytes : 0);
+}
+
 size_t awq_workspace_bytes(awq_op op, int64_t M, int64_t K, int64_t N, int32_t split_k) {
   switch (op) {
     case AWQ_OP_GEMV:
@@ -129,9 +142,12 @@ size_t awq_workspace_bytes(awq_op op, int64_t M, int64_t K, int64_t N, int32_t s
     case AWQ_OP_GEMM:
       if (!gemm_shape_ok(M, K, N, split_k) || M == 0) return 0;
       return gemm_workspace_bytes(gemm_plan(M, K, N, split_k, kModeZeroPoint), M, K, N, kModeZeroPoint);
-    case AWQ_OP_W4A8_GEMM:
+    case AWQ_OP_W4A8_GEMM: {
       if (!gemm_shape_ok(M, K, N, split_k) || M == 0) return 0;
+      GemvPlan gp;
+      if (w4a8_on_gemv(M, K, N, split_k, &gp)) return w4a8_gemv_workspace_bytes(gp, M, K, N);
       return gemm_workspace_bytes(gemm_plan(M, K, N, split_k, kModeW4A8), M, K, N, kModeW4A8);
+    }
     default:
       return 0;
   }
@@ -200,6 +216,20 @@ awq_status w4a8_gemm(const int8_t* xq, const float* s_tok, const int32_t* wq, co
   if (!xq || !s_tok || !wq || !s_ch || !y) return AWQ_ENULL;
   if (!aligned16(xq) || !aligned16(wq) || !aligned16(s_ch) || !aligned16(y) || (acc_out && !aligned16(acc_out)))
     return AWQ_EALIGN;
+  GemvPlan gp;
+  if (w4a8_on_gemv(M, K, N, split_k, &gp)) {
+    awq_status st = check_workspace(w4a8_gemv_workspace_bytes(gp, M, K, N), workspace, workspace_bytes);
+    if (st != AWQ_OK) return st;
+    st = check_arch();
+    if (st != AWQ_OK) return st;
+    int* err = device_error_ptr();
+    if (!err) return AWQ_ECUDA;
+    uint16_t* x16 = reinterpret_cast<uint16_t*>(static_cast<char*>(workspace) + kCounterBytes);
+    cudaError_t e = launch_i8_to_f16(xq, x16, M * K, (cudaStream_t)stream);
+    if (e != cudaSuccess) return AWQ_ECUDA;
+    return from_cuda(launch_gemv_w4a8(x16, reinterpret_cast<const uint32_t*>(wq), s_tok, s_ch, y, acc_out, M, K, N,
+                                      gp, workspace, err, (cudaStream_t)stream));
+  }
   const GemmPlan plan = gemm_plan(M, K, N, split_k, kModeW4A8);
   awq_status st = check_workspace(gemm_workspace_bytes(plan, M, K, N, kModeW4A8), workspace, workspace_bytes);
   if (st != AWQ_OK) return st;

@@ -312,6 +312,41 @@ __device__ __forceinline__ void compute_stage16(const StageRegs<16>& sr, const G
   }
 }
 
+__device__ __forceinline__ int4 f4_to_i4(const float4& v) {
+  return make_int4(__float2int_rn(v.x), __float2int_rn(v.y), __float2int_rn(v.z), __float2int_rn(v.w));
+}
+// W4A8 outputs of `n` consecutive columns of one token: y = fp16((acc * s_tok) * s_ch) (fp32 products in
+// that order, one rounding), and the exact accumulators when `acc_out` is given.
+__device__ __forceinline__ void store_w4a8(const int (&v)[8], float st, const __half* sch, __half* yp, int32_t* ap) {
+  const uint4 sc = *reinterpret_cast<const uint4*>(sch);
+  const __half* sh = reinterpret_cast<const __half*>(&sc);
+  uint32_t h[4];
+#pragma unroll
+  for (int c = 0; c < 8; c += 2) {
+    const __half lo = __float2half_rn(__fmul_rn(__fmul_rn((float)v[c], st), __half2float(sh[c])));
+    const __half hi = __float2half_rn(__fmul_rn(__fmul_rn((float)v[c + 1], st), __half2float(sh[c + 1])));
+    h[c / 2] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+  }
+  *reinterpret_cast<uint4*>(yp) = make_uint4(h[0], h[1], h[2], h[3]);
+  if (ap) {
+    reinterpret_cast<int4*>(ap)[0] = make_int4(v[0], v[1], v[2], v[3]);
+    reinterpret_cast<int4*>(ap)[1] = make_int4(v[4], v[5], v[6], v[7]);
+  }
+}
+__device__ __forceinline__ void store_w4a8_4(const int (&v)[4], float st, const __half* sch, __half* yp, int32_t* ap) {
+  const uint2 sc = *reinterpret_cast<const uint2*>(sch);
+  const __half* sh = reinterpret_cast<const __half*>(&sc);
+  uint32_t h[2];
+#pragma unroll
+  for (int c = 0; c < 4; c += 2) {
+    const __half lo = __float2half_rn(__fmul_rn(__fmul_rn((float)v[c], st), __half2float(sh[c])));
+    const __half hi = __float2half_rn(__fmul_rn(__fmul_rn((float)v[c + 1], st), __half2float(sh[c + 1])));
+    h[c / 2] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+  }
+  *reinterpret_cast<uint2*>(yp) = make_uint2(h[0], h[1]);
+  if (ap) *reinterpret_cast<int4*>(ap) = make_int4(v[0], v[1], v[2], v[3]);
+}
+
 // Stages of a CTA's unit range: a stage is a whole quantization group (two 64-row units) when the
 // range holds both halves of it, else a lone unit.  Every role walks the same sequence.
 // Tile and row block are tracked incrementally (no division per stage).
@@ -340,12 +375,19 @@ struct StageWalk {
 constexpr int kMaxRegs = (65536 / 4) / (((kThreads / 32 + 3) / 4) * 32) / 8 * 8;
 static_assert(kMaxRegs == 168, "9 warps: three on one sub-partition");
 
-template <int T>
+// EXACT (16 tokens only): the W4A8 product.  x holds int8 codes widened to fp16, the weights are
+// u - 8 with u the packed nibble (the symmetric zero point, unit scales), so every product and every
+// fp32 partial sum is an exact integer (the host keeps a CTA's rows of a tile at or below 16384, so
+// |sum| <= 1024 * 16384 = 2^24); partials are added as int32 and the output is
+// fp16((acc * s_tok[m]) * s_ch[n]), with acc also stored to acc_out when given.
+template <int T, bool EXACT>
 __global__ void __maxnreg__(kMaxRegs)
 gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_x,
             const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_s, int has_z,
             __half* __restrict__ y, float* __restrict__ part, int* __restrict__ counters, int* __restrict__ err,
-            int M, int N, int RB, int tiles, int maxc) {
+            int M, int N, int RB, int tiles, int maxc, const float* __restrict__ s_tok,
+            const __half* __restrict__ s_ch, int32_t* __restrict__ acc_out) {
+  static_assert(!EXACT || T == 16, "the exact product uses the 16-token instance");
   // RB = K / 64 row blocks per tile; unit u = (tile u / RB, row block u % RB); units < 2^31 (host check)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -388,7 +430,7 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     // ------------------------------------------------ TMA producer
     if (lane == 0) {
       auto tx_bytes = [&](int nh) {
-        return (uint32_t)(nh * (kUnitQBytes + kXBoxBytes) + (has_z ? kZBytes : 0) + kSBytes);
+        return (uint32_t)(nh * (kUnitQBytes + kXBoxBytes) + (has_z ? kZBytes : 0) + (EXACT ? 0 : kSBytes));
       };
       auto issue_weights = [&](int st, int tile, int rb, int nh) {
         const int grp = rb / (kGroup / kRows);
@@ -400,7 +442,7 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                         (rb + hh) * kRows, full_bar(st));
         if (has_z) tma_load_2d(smem_u32(sb + kZOff), &tm_z, tile * kTileWords, grp, full_bar(st));
         // scales viewed as int32 pairs: 512 columns = one 256-pair box
-        tma_load_2d(smem_u32(sb + kSOff), &tm_s, tile * (kTileCols / 2), grp, full_bar(st));
+        if (!EXACT) tma_load_2d(smem_u32(sb + kSOff), &tm_s, tile * (kTileCols / 2), grp, full_bar(st));
       };
       auto issue_x = [&](int st, int rb, int nh) {
         for (int hh = 0; hh < nh; ++hh)
@@ -485,8 +527,10 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         }
         if (grp != cached_grp) {  // a stage never spans two groups
           const uint32_t zword = has_z ? reinterpret_cast<const uint32_t*>(sb + kZOff)[word] : 0x88888888u;
-          if constexpr (T == 8) group_consts(zword, reinterpret_cast<const uint4*>(sb + kSOff)[word], gc);
-          else group_consts_h(zword, reinterpret_cast<const uint4*>(sb + kSOff)[word], gc);
+          const uint4 sv = EXACT ? make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u)  // 1.0
+                                 : reinterpret_cast<const uint4*>(sb + kSOff)[word];
+          if constexpr (T == 8) group_consts(zword, sv, gc);
+          else group_consts_h(zword, sv, gc);
           cached_grp = grp;
         }
         if constexpr (T == 8) {
@@ -543,7 +587,15 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 #pragma unroll
         for (int par = 0; par < 2; ++par) {
           const int m = 8 * hf + 2 * t + par;
-          if (m < M && n0 < N) {  // N % 32 == 0: the word's 8 columns are all in range
+          if (EXACT && m < M && n0 < N) {
+            int v[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const int sl = slot_of_col(c);
+              v[c] = __float2int_rn(acc[hf][sl >> 1][(sl & 1) * 2 + par]);
+            }
+            store_w4a8(v, s_tok[m], s_ch + n0, y + (size_t)m * N + n0, acc_out ? acc_out + (size_t)m * N + n0 : nullptr);
+          } else if (m < M && n0 < N) {  // N % 32 == 0: the word's 8 columns are all in range
             uint32_t h[4];
 #pragma unroll
             for (int c = 0; c < 8; c += 2) {
@@ -650,7 +702,44 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         const int items = M * kQuads;
         const float4* base = reinterpret_cast<const float4*>(part + (size_t)own_tile * maxc * T * kTileCols);
         constexpr size_t kSlotQuads = (size_t)T * kQuads;
-        for (int i0 = threadIdx.x; i0 < items; i0 += 4 * kThreadsC) {
+        for (int i0 = threadIdx.x; EXACT && i0 < items; i0 += 4 * kThreadsC) {
+          int4 s4[4];  // exact: every partial is an integer below 2^24 in magnitude, their sum need not be
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int it = i0 + k * kThreadsC;
+            s4[k] = it < items ? f4_to_i4(reinterpret_cast<const float4*>(own)[it]) : make_int4(0, 0, 0, 0);
+          }
+          for (int j0 = 1; j0 < nt; j0 += 8) {
+            float4 a[4][8];
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+#pragma unroll
+              for (int jj = 0; jj < 8; ++jj) {
+                const int it = i0 + k * kThreadsC;
+                a[k][jj] = (it < items && j0 + jj < nt) ? __ldcg(base + (size_t)(j0 + jj) * kSlotQuads + it)
+                                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+              }
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+#pragma unroll
+              for (int jj = 0; jj < 8; ++jj) {
+                const int4 b = f4_to_i4(a[k][jj]);
+                s4[k].x += b.x; s4[k].y += b.y; s4[k].z += b.z; s4[k].w += b.w;
+              }
+          }
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int it = i0 + k * kThreadsC;
+            if (it >= items) continue;
+            const int m = it / kQuads;
+            const int n = own_tile * kTileCols + (it - m * kQuads) * 4;
+            if (n < N) {
+              const int v[4] = {s4[k].x, s4[k].y, s4[k].z, s4[k].w};
+              store_w4a8_4(v, s_tok[m], s_ch + n, y + (size_t)m * N + n, acc_out ? acc_out + (size_t)m * N + n : nullptr);
+            }
+          }
+        }
+        for (int i0 = threadIdx.x; !EXACT && i0 < items; i0 += 4 * kThreadsC) {
           float4 s4[4];
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
@@ -754,15 +843,16 @@ size_t gemv_workspace_bytes(const GemvPlan& p, int64_t M, int64_t N) {
 
 namespace {
 
-template <int T>
+template <int T, bool EXACT>
 cudaError_t launch_gemv_t(const uint16_t* x, const uint32_t* qw, const uint32_t* qz, const uint16_t* sc,
                           uint16_t* y, int64_t M, int64_t K, int64_t N, const GemvPlan& p, void* ws, int* err,
-                          cudaStream_t s) {
+                          cudaStream_t s, const float* s_tok = nullptr, const uint16_t* s_ch = nullptr,
+                          int32_t* acc_out = nullptr, size_t part_offset = 0) {
   float* part = nullptr;
   int* counters = nullptr;
   if (p.maxc > 1) {
     counters = static_cast<int*>(ws);
-    part = reinterpret_cast<float*>(static_cast<char*>(ws) + kCounterBytes);
+    part = reinterpret_cast<float*>(static_cast<char*>(ws) + kCounterBytes + part_offset);
   }
   const uint64_t nw = (uint64_t)N / 8;
   const uint64_t ng = (uint64_t)K / kGroup;
@@ -774,11 +864,12 @@ cudaError_t launch_gemv_t(const uint16_t* x, const uint32_t* qw, const uint32_t*
                   CU_TENSOR_MAP_SWIZZLE_128B) &&
       make_map_2d(&tz, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, qz ? (const void*)qz : (const void*)qw, nw,
                   qz ? ng : (uint64_t)K, kTileWords, 1, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-      make_map_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, sc, (uint64_t)N / 2, ng, kTileCols / 2, 1,
-                  CU_TENSOR_MAP_SWIZZLE_NONE);
+      (EXACT || make_map_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, sc, (uint64_t)N / 2, ng, kTileCols / 2, 1,
+                            CU_TENSOR_MAP_SWIZZLE_NONE));
   if (!ok) return cudaErrorInvalidValue;
+  if (EXACT) ts = tq;  // no scale rows are copied
   constexpr int kSmemBytes = Geo<T>::kSmemBytes;
-  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(gemv_kernel<T>), kSmemBytes);
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(gemv_kernel<T, EXACT>), kSmemBytes);
   if (e != cudaSuccess) return e;
 
   cudaLaunchConfig_t cfg = {};
@@ -791,8 +882,9 @@ cudaError_t launch_gemv_t(const uint16_t* x, const uint32_t* qw, const uint32_t*
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, gemv_kernel<T>, tq, tx, tz, ts, qz ? 1 : 0, reinterpret_cast<__half*>(y), part,
-                         counters, err, (int)M, (int)N, (int)(K / kRows), p.tiles, p.maxc);
+  e = cudaLaunchKernelEx(&cfg, gemv_kernel<T, EXACT>, tq, tx, tz, ts, qz ? 1 : 0, reinterpret_cast<__half*>(y), part,
+                         counters, err, (int)M, (int)N, (int)(K / kRows), p.tiles, p.maxc, s_tok,
+                         reinterpret_cast<const __half*>(s_ch), acc_out);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -804,8 +896,23 @@ cudaError_t launch_gemv(const uint16_t* x, const uint32_t* qw, const uint32_t* q
                         int* err, cudaStream_t s) {
   // the kernel counts (tile, 64-row block) units in 32 bits; any tensor that fits a GPU stays far below
   if ((int64_t)p.tiles * p.groups >= ((int64_t)1 << 31)) return cudaErrorInvalidValue;
-  if (M <= 8) return launch_gemv_t<8>(x, qw, qz, sc, y, M, K, N, p, ws, err, s);
-  return launch_gemv_t<16>(x, qw, qz, sc, y, M, K, N, p, ws, err, s);
+  if (M <= 8) return launch_gemv_t<8, false>(x, qw, qz, sc, y, M, K, N, p, ws, err, s);
+  return launch_gemv_t<16, false>(x, qw, qz, sc, y, M, K, N, p, ws, err, s);
+}
+
+bool gemv_w4a8_ok(const GemvPlan& p, int64_t M) {
+  // every CTA's rows of a tile stay within 16384 (256 units of 64 rows), so fp32 sums stay exact
+  const int64_t units = (int64_t)p.tiles * p.groups;
+  return M >= 1 && M <= kGemvMaxM && (units + p.ctas - 1) / p.ctas <= 256;
+}
+
+cudaError_t launch_gemv_w4a8(const uint16_t* x16, const uint32_t* wq, const float* s_tok, const uint16_t* s_ch,
+                             uint16_t* y, int32_t* acc_out, int64_t M, int64_t K, int64_t N, const GemvPlan& p,
+                             void* ws, int* err, cudaStream_t s) {
+  if ((int64_t)p.tiles * p.groups >= ((int64_t)1 << 31) || !gemv_w4a8_ok(p, M)) return cudaErrorInvalidValue;
+  // workspace: counters | x16 (the caller's) | partials
+  return launch_gemv_t<16, true>(x16, wq, nullptr, nullptr, y, M, K, N, p, ws, err, s, s_tok, s_ch, acc_out,
+                                 align256((size_t)M * (size_t)K * 2));
 }
 
 }  // namespace awq

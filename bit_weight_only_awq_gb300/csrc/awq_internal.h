@@ -63,6 +63,12 @@ size_t gemv_workspace_bytes(const GemvPlan& p, int64_t M, int64_t N);
 cudaError_t launch_gemv(const uint16_t* x, const uint32_t* qw, const uint32_t* qz, const uint16_t* sc,
                         uint16_t* y, int64_t M, int64_t K, int64_t N, const GemvPlan& p, void* ws,
                         int* err, cudaStream_t s);
+// W4A8 on the 16-token GEMV (M <= 16): x16 = the int8 codes widened to fp16, wq = AWQ-packed u = q + 8,
+// exact int32 accumulators.  gemv_w4a8_ok: the plan keeps every CTA's rows of a tile within 16384.
+bool gemv_w4a8_ok(const GemvPlan& p, int64_t M);
+cudaError_t launch_gemv_w4a8(const uint16_t* x16, const uint32_t* wq, const float* s_tok, const uint16_t* s_ch,
+                             uint16_t* y, int32_t* acc_out, int64_t M, int64_t K, int64_t N, const GemvPlan& p,
+                             void* ws, int* err, cudaStream_t s);
 
 // ---- tensor-core GEMM (awq_gemm_tc.cu)
 // kModeW4A8One is the W4A8 kernel for K slices of at most 16384 rows (kW4A8MaxKSlice): one exact

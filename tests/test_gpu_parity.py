@@ -283,6 +283,42 @@ def test_w4a8_config_sampled_bitexact(awq, M):
     assert np.array_equal(y[:, cols].view(np.uint16), want_y.view(np.uint16))
 
 
+@pytest.mark.parametrize("M", [1, 9, 16])
+def test_w4a8_gemv_and_gemm_agree(awq, M):
+    # up to 16 tokens the automatic plan runs on the GEMV; split_k = 1 at K = 21760 gives one CTA per
+    # tile with more than 16384 rows, which the GEMV does not take, so that call runs on the GEMM
+    K, N = synth.W4A8_SHAPE
+    p = synth.w4a8_problem(M, K, N, seed=700 + M)
+    xq, s, y_v, acc_v = _w4a8_run(awq, p, split_k=0)
+    _, _, y_g, acc_g = _w4a8_run(awq, p, split_k=1)
+    assert np.array_equal(acc_v, acc_g)
+    assert np.array_equal(y_v.view(np.uint16), y_g.view(np.uint16))
+    wc = sample_word_cols(N // 8, seed=M + 7, count=8)
+    cols = (8 * wc[:, None] + np.arange(8)[None, :]).ravel()
+    want_y, want_acc = oracle.w4a8_linear(xq, s, p["wq"][:, wc], p["s_ch"][cols])
+    assert np.array_equal(acc_v[:, cols], want_acc)
+    assert np.array_equal(y_v[:, cols].view(np.uint16), want_y.view(np.uint16))
+
+
+@pytest.mark.parametrize("split_k", [0, 1, 3])
+def test_w4a8_gemv_sums_beyond_fp32_integers(awq, split_k):
+    # accumulators past 2^24: codes 127 against weights 7 (u = 15) over K = 21760 reach 19.3 million,
+    # so the partials of the CTAs that share a tile must be added as integers
+    M, K, N = 3, 21760, 1024
+    x = np.ones((M, K), dtype=np.float16)
+    x[1, ::2] = -1.0                       # alternating signs: a small sum
+    x[2, : K // 2] = 0.5                   # codes 64 and 127
+    wq = np.full((K, N // 8), -1, dtype=np.int32)  # every nibble 15
+    wq[:, 1::2] = 0                         # every nibble 0: q = -8
+    s_ch = np.full(N, 0.001, dtype=np.float16)
+    p = {"x": x, "wq": wq, "s_ch": s_ch}
+    xq, s, y, acc = _w4a8_run(awq, p, split_k=split_k)
+    want_y, want_acc = oracle.w4a8_linear(xq, s, wq, s_ch)
+    assert np.abs(want_acc).max() > 2 ** 24
+    assert np.array_equal(acc, want_acc)
+    assert np.array_equal(y.view(np.uint16), want_y.view(np.uint16))
+
+
 @pytest.mark.parametrize("M,K,N", [(1000, 21760, 8192), (1000, 4096, 16384)])
 def test_w4a8_large_tiles_bitexact(awq, M, K, N):
     # >= 128-token tiles: at K = 21760 one M-block with two exact accumulators; at K = 4096 two M-blocks
