@@ -53,6 +53,11 @@
 //    dequant kernel does (HSUB2 of the zero, HMUL2 by the scale) and multiplies it straight into
 //    the accumulators; streaming the weights once for 16 tokens beats the tensor-core GEMM's
 //    16-token tiles by 1.3-2.9x.
+//  * W4A8 up to 16 tokens (gemv_kernel<16, true>): the same instance with the symmetric zero point
+//    and unit scales, on activations that are int8 codes widened to fp16.  Each weight is the exact
+//    half u - 8 and each product an integer of magnitude at most 1024; with at most 16384 rows of a
+//    tile per CTA every fp32 sum is exact, partials are added across CTAs as int32, and the output
+//    is the W4A8 epilogue fp16((acc * s_tok) * s_ch) ("Support W4A8 quantization for vllm").
 //  * Lane (g, t) of the mma reads rows 2t, 2t+1 (+8) of each 16-row step; with the
 //    128-byte swizzle those 32-bit shared-memory loads, and the activation loads, are
 //    free of bank conflicts, and every address is a lane constant plus an immediate.
