@@ -219,8 +219,11 @@ struct GroupConsts {
 __device__ __forceinline__ void group_consts(uint32_t zword, const uint4& sv, GroupConsts& c) {
 #pragma unroll
   for (int b = 0; b < 4; ++b) {
-    const float zl = (float)((zword >> (8 * b)) & 15u) + 1024.f;
-    const float zh = (float)((zword >> (8 * b + 4)) & 15u) * 16.f + 1024.f;
+    // 1024 + z and 1024 + 16 z as fp32 bit patterns: byte b's nibbles land in the mantissa of 1024.0f
+    // (whose last place is 2^-13) at bits 13..16 and 17..20, both from one shift of the zero word
+    const uint32_t zs = 8 * b <= 13 ? zword << (13 - 8 * b) : zword >> (8 * b - 13);
+    const float zl = __uint_as_float(0x44800000u | (zs & 0x0001E000u));
+    const float zh = __uint_as_float(0x44800000u | (zs & 0x001E0000u));
     const __half* sh = reinterpret_cast<const __half*>(&sv);
     c.sf[b][0] = __half2float(sh[order_map(2 * b)]);
     c.sf[b][1] = __half2float(sh[order_map(2 * b + 1)]) * 0.0625f;  // s / 16, exact
