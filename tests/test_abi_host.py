@@ -137,6 +137,24 @@ def test_gemm_plan_split_choices(awq):
     assert ws(1024, 4096, 6144) == 0
 
 
+def test_w4a8_route_by_token_count(awq):
+    # W4A8 with at most 16 tokens runs on the 16-token GEMV when every CTA's rows of a tile stay within
+    # 16384; its workspace is counters | fp16 codes | the GEMV's 16-token partial slots.
+    counters = 65536
+    a256 = lambda b: (b + 255) // 256 * 256
+    ws = lambda M, K, N, sp: awq.awq_workspace_bytes(awq.OP_W4A8_GEMM, M, K, N, sp)
+    gemv_partials = awq.awq_workspace_bytes(awq.OP_GEMV, 16, 21760, 8192, 0) - counters
+    assert gemv_partials > 0
+    for M in (1, 16):
+        assert ws(M, 21760, 8192, 0) == counters + a256(M * 21760 * 2) + gemv_partials
+    # split_k = 1: one CTA per tile would cover all 21760 rows, so the GEMM takes the call
+    assert ws(16, 21760, 8192, 1) == counters + 16 * 21760 * 2
+    # 17 tokens: the GEMM (one M-block, two exact accumulators, K split of two to fill the SMs)
+    assert ws(17, 21760, 8192, 0) == counters + a256(17 * 21760 * 2) + 2 * 17 * 8192 * 4
+    # K = 4096 with one CTA per tile: the GEMV without partials
+    assert ws(8, 4096, 4096, 1) == counters + 8 * 4096 * 2
+
+
 def test_selftest_rejects_bad_limits_before_launch(awq):
     assert awq.lib.awq_selftest_wait_timeout(0, None) == EINVAL
     assert awq.lib.awq_selftest_wait_timeout(-5, None) == EINVAL
