@@ -277,9 +277,8 @@ def issue_step(awq, bufs, stream):
             awq.awq_gemm(b["x"], b["qweight"], b["qzeros"], b["scales"], out=b["y"], stream=stream)
             launches += 1
         else:
-            awq.w4a8_quant_act(b["x"], b["xq"], b["s_tok"], stream=stream)
-            awq.w4a8_gemm(b["xq"], b["s_tok"], b["wq"], b["s_ch"], out=b["y"], stream=stream)
-            launches += 3  # quantize, widen to fp16, tensor-core GEMM
+            awq.w4a8_linear(b["x"], b["wq"], b["s_ch"], out=b["y"], s_tok=b["s_tok"], stream=stream)
+            launches += 2  # quantize (fp16 codes into the workspace), then the GEMV or the tensor-core GEMM
     return launches
 
 
@@ -386,7 +385,7 @@ def gpu_arm(args, rank, world, torch, dist):
 
 def dominant_kernel(workload):
     return {"decode": ("awq_gemv (gemv_kernel)", "hbm"), "prefill": ("awq_gemm (gemm_kernel)", "tensor"),
-            "crossover": ("awq_gemv + awq_gemm", "hbm"), "w4a8": ("w4a8_gemm (gemm_kernel<W4A8>)", "tensor")}[workload]
+            "crossover": ("awq_gemv + awq_gemm", "hbm"), "w4a8": ("w4a8_linear (gemm_kernel<W4A8>)", "tensor")}[workload]
 
 
 def load_traffic(workload, algorithmic_bytes_per_launch):

@@ -43,6 +43,7 @@ _SIGS = {
     "awq_gemv_noalloc": (_i32, [_p, _p, _p, _p, _p, _i64, _i64, _i64, _i32, _i32, _p]),
     "w4a8_quant_act": (_i32, [_p, _p, _p, _i64, _i64, _p]),
     "w4a8_gemm": (_i32, [_p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _i32, _p, _sz, _p]),
+    "w4a8_linear": (_i32, [_p, _p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _i32, _p, _sz, _p]),
     "awq_last_device_error": (_i32, [ctypes.POINTER(_i32)]),
     "awq_selftest_wait_timeout": (_i32, [_i64, _p]),
 }
@@ -210,6 +211,23 @@ def w4a8_gemm(xq, s_tok, wq, s_ch, split_k: int = 0, out=None, acc_out=None, wor
     _check("w4a8_gemm", lib.w4a8_gemm(_ptr(xq), _ptr(s_tok), _ptr(wq), _ptr(s_ch), _ptr(out), _ptr(acc_out), M, K,
                                       N, split_k, _ptr(ws), nbytes, _stream(stream)))
     return out
+
+
+def w4a8_linear(x, wq, s_ch, split_k: int = 0, out=None, acc_out=None, xq_out=None, s_tok=None, workspace=None,
+                stream=None):
+    """W4A8 from fp16 activations in one call (quantization fused); returns (y, s_tok)."""
+    M, K = x.shape
+    N = wq.shape[1] * 8
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    if s_tok is None:
+        s_tok = torch.empty((M,), dtype=torch.float32, device=x.device)
+    need = awq_workspace_bytes(OP_W4A8_GEMM, M, K, N, split_k)
+    ws = workspace if workspace is not None else device_workspace(need, x.device)
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check("w4a8_linear", lib.w4a8_linear(_ptr(x), _ptr(wq), _ptr(s_ch), _ptr(out), _ptr(acc_out), _ptr(xq_out),
+                                          _ptr(s_tok), M, K, N, split_k, _ptr(ws), nbytes, _stream(stream)))
+    return out, s_tok
 
 
 def awq_last_device_error() -> int:

@@ -208,6 +208,43 @@ awq_status w4a8_quant_act(const uint16_t* x, int8_t* xq, float* s_tok, int64_t M
   return from_cuda(launch_quant_act(x, xq, s_tok, M, K, (cudaStream_t)stream));
 }
 
+}  // extern "C"
+
+// The W4A8 product once `fill` has written the fp16 codes of the activations into the workspace
+// (from int8 codes, or by quantizing fp16 activations): the 16-token GEMV or the GEMM, as planned.
+template <class Fill>
+static awq_status w4a8_product(Fill fill, const float* s_tok, const int32_t* wq, const uint16_t* s_ch, uint16_t* y,
+                               int32_t* acc_out, int64_t M, int64_t K, int64_t N, int32_t split_k, void* workspace,
+                               size_t workspace_bytes, awq_stream_t stream) {
+  GemvPlan gp;
+  const bool on_gemv = w4a8_on_gemv(M, K, N, split_k, &gp);
+  const GemmPlan plan = gemm_plan(M, K, N, split_k, kModeW4A8);
+  const size_t need = on_gemv ? w4a8_gemv_workspace_bytes(gp, M, K, N) : gemm_workspace_bytes(plan, M, K, N, kModeW4A8);
+  awq_status st = check_workspace(need, workspace, workspace_bytes);
+  if (st != AWQ_OK) return st;
+  if (!on_gemv && plan.split > 1 && (int64_t)plan.n_tiles * plan.m_tiles > kMaxCounters) return AWQ_EINVAL;
+  st = check_arch();
+  if (st != AWQ_OK) return st;
+  int* err = device_error_ptr();
+  if (!err) return AWQ_ECUDA;
+  char* ws = static_cast<char*>(workspace);
+  uint16_t* x16 = reinterpret_cast<uint16_t*>(ws + kCounterBytes);
+  const cudaStream_t s = (cudaStream_t)stream;
+  if (fill(x16, s) != cudaSuccess) return AWQ_ECUDA;
+  const uint32_t* w = reinterpret_cast<const uint32_t*>(wq);
+  if (on_gemv) return from_cuda(launch_gemv_w4a8(x16, w, s_tok, s_ch, y, acc_out, M, K, N, gp, workspace, err, s));
+  void* part = nullptr;
+  int* counters = nullptr;
+  if (plan.split > 1) {
+    counters = reinterpret_cast<int*>(ws);
+    part = ws + kCounterBytes + align256((size_t)M * (size_t)K * 2);
+  }
+  return from_cuda(launch_gemm(kModeW4A8, x16, w, nullptr, nullptr, s_tok, s_ch, y, acc_out, M, K, N, plan, part,
+                               counters, err, s));
+}
+
+extern "C" {
+
 awq_status w4a8_gemm(const int8_t* xq, const float* s_tok, const int32_t* wq, const uint16_t* s_ch, uint16_t* y,
                      int32_t* acc_out, int64_t M, int64_t K, int64_t N, int32_t split_k, void* workspace,
                      size_t workspace_bytes, awq_stream_t stream) {
@@ -216,40 +253,21 @@ awq_status w4a8_gemm(const int8_t* xq, const float* s_tok, const int32_t* wq, co
   if (!xq || !s_tok || !wq || !s_ch || !y) return AWQ_ENULL;
   if (!aligned16(xq) || !aligned16(wq) || !aligned16(s_ch) || !aligned16(y) || (acc_out && !aligned16(acc_out)))
     return AWQ_EALIGN;
-  GemvPlan gp;
-  if (w4a8_on_gemv(M, K, N, split_k, &gp)) {
-    awq_status st = check_workspace(w4a8_gemv_workspace_bytes(gp, M, K, N), workspace, workspace_bytes);
-    if (st != AWQ_OK) return st;
-    st = check_arch();
-    if (st != AWQ_OK) return st;
-    int* err = device_error_ptr();
-    if (!err) return AWQ_ECUDA;
-    uint16_t* x16 = reinterpret_cast<uint16_t*>(static_cast<char*>(workspace) + kCounterBytes);
-    cudaError_t e = launch_i8_to_f16(xq, x16, M * K, (cudaStream_t)stream);
-    if (e != cudaSuccess) return AWQ_ECUDA;
-    return from_cuda(launch_gemv_w4a8(x16, reinterpret_cast<const uint32_t*>(wq), s_tok, s_ch, y, acc_out, M, K, N,
-                                      gp, workspace, err, (cudaStream_t)stream));
-  }
-  const GemmPlan plan = gemm_plan(M, K, N, split_k, kModeW4A8);
-  awq_status st = check_workspace(gemm_workspace_bytes(plan, M, K, N, kModeW4A8), workspace, workspace_bytes);
-  if (st != AWQ_OK) return st;
-  st = check_arch();
-  if (st != AWQ_OK) return st;
-  int* err = device_error_ptr();
-  if (!err) return AWQ_ECUDA;
-  char* ws = static_cast<char*>(workspace);
-  uint16_t* x16 = reinterpret_cast<uint16_t*>(ws + kCounterBytes);
-  void* part = nullptr;
-  int* counters = nullptr;
-  if (plan.split > 1) {
-    if ((int64_t)plan.n_tiles * plan.m_tiles > kMaxCounters) return AWQ_EINVAL;
-    counters = reinterpret_cast<int*>(ws);
-    part = ws + kCounterBytes + align256((size_t)M * (size_t)K * 2);
-  }
-  cudaError_t e = launch_i8_to_f16(xq, x16, M * K, (cudaStream_t)stream);
-  if (e != cudaSuccess) return AWQ_ECUDA;
-  return from_cuda(launch_gemm(kModeW4A8, x16, reinterpret_cast<const uint32_t*>(wq), nullptr, nullptr, s_tok, s_ch,
-                               y, acc_out, M, K, N, plan, part, counters, err, (cudaStream_t)stream));
+  auto widen = [&](uint16_t* x16, cudaStream_t s) { return launch_i8_to_f16(xq, x16, M * K, s); };
+  return w4a8_product(widen, s_tok, wq, s_ch, y, acc_out, M, K, N, split_k, workspace, workspace_bytes, stream);
+}
+
+awq_status w4a8_linear(const uint16_t* x, const int32_t* wq, const uint16_t* s_ch, uint16_t* y, int32_t* acc_out,
+                       int8_t* xq_out, float* s_tok, int64_t M, int64_t K, int64_t N, int32_t split_k,
+                       void* workspace, size_t workspace_bytes, awq_stream_t stream) {
+  if (!gemm_shape_ok(M, K, N, split_k)) return AWQ_EINVAL;
+  if (M == 0) return AWQ_OK;
+  if (!x || !s_tok || !wq || !s_ch || !y) return AWQ_ENULL;
+  if (!aligned16(x) || !aligned16(wq) || !aligned16(s_ch) || !aligned16(y) || (acc_out && !aligned16(acc_out)) ||
+      (xq_out && !aligned16(xq_out)))
+    return AWQ_EALIGN;
+  auto quantize = [&](uint16_t* x16, cudaStream_t s) { return launch_quant_act(x, xq_out, s_tok, M, K, s, x16); };
+  return w4a8_product(quantize, s_tok, wq, s_ch, y, acc_out, M, K, N, split_k, workspace, workspace_bytes, stream);
 }
 
 awq_status awq_last_device_error(int32_t* code) {

@@ -92,8 +92,9 @@ cudaError_t launch_gemm(int mode, const uint16_t* x16, const uint32_t* qw, const
                         void* ws_partials, int* counters, int* err, cudaStream_t s);
 
 // ---- W4A8 activation kernels (w4a8_act.cu)
+// xq (int8 codes) and x16 (the codes widened to fp16) are each written when not null
 cudaError_t launch_quant_act(const uint16_t* x, int8_t* xq, float* s_tok, int64_t M, int64_t K,
-                             cudaStream_t s);
+                             cudaStream_t s, uint16_t* x16 = nullptr);
 cudaError_t launch_i8_to_f16(const int8_t* xq, uint16_t* x16, int64_t count, cudaStream_t s);
 
 }  // namespace awq

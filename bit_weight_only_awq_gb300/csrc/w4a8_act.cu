@@ -27,10 +27,27 @@ __device__ __forceinline__ uint32_t code_of(float xv, float s, float inv) {
   return (uint32_t)(int)q & 0xFFu;
 }
 
+// The eight codes of one 16-byte activation vector: as int8 into xq (when given) and widened to fp16
+// (exact) into x16 (when given), the operand of the fp16 tensor path.
+__device__ __forceinline__ void store_codes(const uint32_t (&out)[2], int8_t* xq, __half* x16, int64_t r, int K, int i) {
+  if (xq) reinterpret_cast<uint2*>(xq + r * (int64_t)K)[i] = make_uint2(out[0], out[1]);
+  if (x16) {
+    uint32_t h[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      const uint32_t w = out[p >> 1] >> (16 * (p & 1));
+      const int a = (int)(int8_t)(w & 0xFFu), b = (int)(int8_t)((w >> 8) & 0xFFu);
+      h[p] = (uint32_t)__half_as_ushort(__int2half_rn(a)) | ((uint32_t)__half_as_ushort(__int2half_rn(b)) << 16);
+    }
+    reinterpret_cast<uint4*>(x16 + r * (int64_t)K)[i] = make_uint4(h[0], h[1], h[2], h[3]);
+  }
+}
+
 // One CTA per token row, the row read from DRAM once: it is kept in shared memory between the absmax
 // pass and the coding pass.
 __global__ void __launch_bounds__(kQThreads)
-quant_act_smem_kernel(const __half* __restrict__ x, int8_t* __restrict__ xq, float* __restrict__ s_tok, int K) {
+quant_act_smem_kernel(const __half* __restrict__ x, int8_t* __restrict__ xq, float* __restrict__ s_tok,
+                      __half* __restrict__ x16, int K) {
   extern __shared__ uint4 row[];
   __shared__ uint32_t warp_max[kQThreads / 32];
   __shared__ float s_shared;
@@ -63,7 +80,6 @@ quant_act_smem_kernel(const __half* __restrict__ x, int8_t* __restrict__ xq, flo
   __syncthreads();
   const float s = s_shared;
   const float inv = s > 0.f ? __frcp_rn(s) : 0.f;
-  uint2* qr = reinterpret_cast<uint2*>(xq + r * (int64_t)K);
   for (int i = threadIdx.x; i < nvec; i += kQThreads) {
     const uint4 v = row[i];
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -75,13 +91,14 @@ quant_act_smem_kernel(const __half* __restrict__ x, int8_t* __restrict__ xq, flo
         out[j >> 2] |= code_of(xv, s, inv) << (8 * (j & 3));
       }
     }
-    qr[i] = make_uint2(out[0], out[1]);
+    store_codes(out, xq, x16, r, K, i);
   }
 }
 
 // One CTA per token row: pass 1 finds absmax, pass 2 writes the codes (second read hits L2).
 __global__ void __launch_bounds__(kQThreads)
-quant_act_kernel(const __half* __restrict__ x, int8_t* __restrict__ xq, float* __restrict__ s_tok, int K) {
+quant_act_kernel(const __half* __restrict__ x, int8_t* __restrict__ xq, float* __restrict__ s_tok,
+                 __half* __restrict__ x16, int K) {
   __shared__ uint32_t warp_max[kQThreads / 32];
   __shared__ float s_shared;
   const int64_t row = blockIdx.x;
@@ -113,7 +130,6 @@ quant_act_kernel(const __half* __restrict__ x, int8_t* __restrict__ xq, float* _
   }
   __syncthreads();
   const float s = s_shared;
-  uint2* qr = reinterpret_cast<uint2*>(xq + row * (int64_t)K);
   for (int i = threadIdx.x; i < nvec; i += kQThreads) {
     const uint4 v = __ldg(xr + i);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -127,7 +143,7 @@ quant_act_kernel(const __half* __restrict__ x, int8_t* __restrict__ xq, float* _
         out[j >> 2] |= ((uint32_t)(int)qv & 0xFFu) << (8 * (j & 3));
       }
     }
-    qr[i] = make_uint2(out[0], out[1]);
+    store_codes(out, xq, x16, row, K, i);
   }
 }
 
@@ -148,7 +164,8 @@ __global__ void i8_to_f16_kernel(const int8_t* __restrict__ xq, __half* __restri
 
 }  // namespace
 
-cudaError_t launch_quant_act(const uint16_t* x, int8_t* xq, float* s_tok, int64_t M, int64_t K, cudaStream_t s) {
+cudaError_t launch_quant_act(const uint16_t* x, int8_t* xq, float* s_tok, int64_t M, int64_t K, cudaStream_t s,
+                             uint16_t* x16) {
   if (M == 0) return cudaSuccess;
   if (K <= kQ1MaxK) {
     const int smem = (int)K * 2;
@@ -157,9 +174,10 @@ cudaError_t launch_quant_act(const uint16_t* x, int8_t* xq, float* s_tok, int64_
       if (e != cudaSuccess) return e;
     }
     quant_act_smem_kernel<<<(unsigned)M, kQThreads, smem, s>>>(reinterpret_cast<const __half*>(x), xq, s_tok,
-                                                               (int)K);
+                                                               reinterpret_cast<__half*>(x16), (int)K);
   } else {
-    quant_act_kernel<<<(unsigned)M, kQThreads, 0, s>>>(reinterpret_cast<const __half*>(x), xq, s_tok, (int)K);
+    quant_act_kernel<<<(unsigned)M, kQThreads, 0, s>>>(reinterpret_cast<const __half*>(x), xq, s_tok,
+                                                       reinterpret_cast<__half*>(x16), (int)K);
   }
   return cudaGetLastError();
 }

@@ -210,6 +210,24 @@ awq_status w4a8_gemm(const int8_t *xq, const float *s_tok, const int32_t *wq,
                      awq_stream_t stream);
 
 /*
+ * w4a8_linear -- w4a8_quant_act and w4a8_gemm in one call, from fp16 activations.
+ * x fp16 [M, K]; wq, s_ch, y, acc_out, split_k, workspace as for w4a8_gemm
+ * (the same workspace size: awq_workspace_bytes(AWQ_OP_W4A8_GEMM, ...));
+ * s_tok fp32 [M] (output, required: the per-token scales the epilogue uses);
+ * xq_out int8 [M, K] (optional output of the codes, NULL to skip).
+ * The quantization writes the codes widened to fp16 straight into the
+ * workspace for the fp16 tensor path, so the int8 codes need not round-trip
+ * through memory.  Results are bit-identical to w4a8_quant_act followed by
+ * w4a8_gemm.
+ * Source: "Support W4A8 quantization for vllm": the per-token scale computed
+ * online (HandH1998), fused into the product as the thread's follow-up work.
+ */
+awq_status w4a8_linear(const uint16_t *x, const int32_t *wq, const uint16_t *s_ch, uint16_t *y,
+                       int32_t *acc_out, int8_t *xq_out, float *s_tok, int64_t M, int64_t K,
+                       int64_t N, int32_t split_k, void *workspace, size_t workspace_bytes,
+                       awq_stream_t stream);
+
+/*
  * awq_last_device_error -- reads and clears the device-side error word of the
  * current device (synchronous: waits for the device).  *code receives 0 when
  * no bounded wait expired since the last read, else the id of the wait that

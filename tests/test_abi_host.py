@@ -30,7 +30,7 @@ FAKE_MISALIGNED = FAKE + 4
 def test_header_declares_the_boundary(awq):
     names = awq.header_functions()
     for want in ("awq_pack", "awq_unpack", "awq_dequant", "awq_gemv", "awq_gemm", "awq_workspace_bytes",
-                 "w4a8_quant_act", "w4a8_gemm", "awq_status_string", "awq_last_device_error"):
+                 "w4a8_quant_act", "w4a8_gemm", "w4a8_linear", "awq_status_string", "awq_last_device_error"):
         assert want in names
 
 
@@ -91,6 +91,12 @@ def test_gemm_and_w4a8_argument_checks(awq):
     g = awq.lib.w4a8_gemm
     assert g(FAKE, FAKE, FAKE, FAKE, FAKE, None, 4, 21760, 8192, 0, None, 0, None) == EWORKSPACE
     assert g(None, FAKE, FAKE, FAKE, FAKE, None, 4, 21760, 8192, 0, None, 0, None) == ENULL
+    lin = awq.lib.w4a8_linear  # x, wq, s_ch, y, acc_out, xq_out, s_tok, M, K, N, split_k, ws, bytes, stream
+    assert lin(FAKE, FAKE, FAKE, FAKE, None, None, FAKE, 4, 21760, 8192, 0, None, 0, None) == EWORKSPACE
+    assert lin(FAKE, FAKE, FAKE, FAKE, None, None, None, 4, 21760, 8192, 0, None, 0, None) == ENULL  # s_tok
+    assert lin(FAKE, FAKE, FAKE, FAKE, None, FAKE_MISALIGNED, FAKE, 4, 21760, 8192, 0, None, 0, None) == EALIGN
+    assert lin(FAKE, FAKE, FAKE, FAKE, None, None, FAKE, 4, 21700, 8192, 0, None, 0, None) == EINVAL   # K % 128
+    assert lin(None, FAKE, FAKE, FAKE, None, None, FAKE, 0, 21760, 8192, 0, None, 0, None) == 0       # M = 0
     q = awq.lib.w4a8_quant_act
     assert q(FAKE, FAKE, FAKE, 4, 100, None) == EINVAL
     assert q(FAKE, FAKE_MISALIGNED, FAKE, 4, 128, None) == EALIGN

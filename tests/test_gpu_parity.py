@@ -283,6 +283,25 @@ def test_w4a8_config_sampled_bitexact(awq, M):
     assert np.array_equal(y[:, cols].view(np.uint16), want_y.view(np.uint16))
 
 
+@pytest.mark.parametrize("M,K,N", [(1, 21760, 8192), (16, 21760, 8192), (300, 4096, 1024), (37, 256, 288)])
+def test_w4a8_linear_matches_two_calls(awq, M, K, N):
+    # the fused entry (quantization writes the fp16 codes into the workspace) against w4a8_quant_act
+    # followed by w4a8_gemm, on the GEMV route (M <= 16) and the GEMM route
+    p = synth.w4a8_problem(M, K, N, seed=800 + M)
+    xq, s, y2, acc2 = _w4a8_run(awq, p)
+    x = dev(p["x"])
+    acc = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    xq_out = torch.empty((M, K), dtype=torch.int8, device="cuda")
+    y, s_tok = awq.w4a8_linear(x, dev(p["wq"]), dev(p["s_ch"]), acc_out=acc, xq_out=xq_out)
+    assert np.array_equal(host(xq_out), xq)
+    assert np.array_equal(host(s_tok).view(np.uint32), s.view(np.uint32))
+    assert np.array_equal(host(acc), acc2)
+    assert np.array_equal(host(y).view(np.uint16), y2.view(np.uint16))
+    # without the optional outputs
+    y_only, _ = awq.w4a8_linear(x, dev(p["wq"]), dev(p["s_ch"]))
+    assert np.array_equal(host(y_only).view(np.uint16), y2.view(np.uint16))
+
+
 @pytest.mark.parametrize("M", [1, 9, 16])
 def test_w4a8_gemv_and_gemm_agree(awq, M):
     # up to 16 tokens the automatic plan runs on the GEMV; split_k = 1 at K = 21760 gives one CTA per
