@@ -57,3 +57,9 @@ def test_reference_arm_under_torchrun_prints_once():
     assert len(lines) == 1, res.stdout[-2000:]
     rec = json.loads(lines[0])
     assert rec["impl"] == "reference" and rec["value"] > 0 and rec["e2e"]["value"] == rec["value"]
+    # the same metric, unit and workload as the GPU arm's line, with the oracle described as the baseline
+    assert rec["metric"].startswith("W4A16 group-quant GEMM") and rec["unit"] == "GB/s"
+    assert rec["higher_is_better"] is True and rec["config"]["workload"].startswith("decode:")
+    assert rec["cpu_baseline"]["kind"] == "oracle" and rec["cpu_baseline"]["value"] == rec["value"]
+    assert rec["cpu_baseline"]["cores"] >= 1 and rec["cpu_baseline"]["sample"]
+    assert rec["e2e"]["h2d_bytes_per_step"] == 0 and rec["e2e"]["d2h_bytes_per_step"] == 0
