@@ -219,8 +219,11 @@ awq_status w4a8_gemm(const int8_t *xq, const float *s_tok, const int32_t *wq,
  * workspace for the fp16 tensor path, so the int8 codes need not round-trip
  * through memory.  Results are bit-identical to w4a8_quant_act followed by
  * w4a8_gemm.
- * Source: "Support W4A8 quantization for vllm": the per-token scale computed
- * online (HandH1998), fused into the product as the thread's follow-up work.
+ * Source: "Support W4A8 quantization for vllm": the description's news list
+ * (dynamic activation quantization fused into the QQQ linear method) and
+ * HandH1998's reply on moving the activation quantization out of the
+ * surrounding layers into the linear method; the per-token scale computed
+ * online.
  */
 awq_status w4a8_linear(const uint16_t *x, const int32_t *wq, const uint16_t *s_ch, uint16_t *y,
                        int32_t *acc_out, int8_t *xq_out, float *s_tok, int64_t M, int64_t K,
