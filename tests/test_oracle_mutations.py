@@ -81,6 +81,26 @@ def _w4a8_acc_offset7(xq, wq):
     return xq.astype(np.int64) @ (O.unpack(wq).astype(np.int64) - 7)
 
 
+def _w4a8_linear_factory(kind):
+    # wrong W4A8 epilogues: the token scale dropped, the scale product taken first, an fp16 intermediate
+    # after the token scale, and the whole chain in float64 (no fp32 rounding of acc or the products)
+    def w4a8_linear(xq, s_tok, wq_packed, s_ch):
+        acc = O.w4a8_accumulate(xq, wq_packed)
+        st = np.asarray(s_tok, dtype=np.float32)[:, None]
+        sc = np.asarray(s_ch, dtype=np.float16).astype(np.float32)[None, :]
+        a32 = acc.astype(np.float32)
+        if kind == "drop_tok":
+            y = a32 * sc
+        elif kind == "product_first":
+            y = a32 * (st * sc)
+        elif kind == "fp16_intermediate":
+            y = (a32 * st).astype(np.float16).astype(np.float32) * sc
+        else:
+            y = acc.astype(np.float64) * st.astype(np.float64) * sc.astype(np.float64)
+        return y.astype(np.float16), acc
+    return w4a8_linear
+
+
 MUTANTS = [
     ("unpack", _unpack_inverse_map, ["test_unpack_pack_golden"]),
     ("pack", _pack_no_clamp, ["test_pack_clamps_codes_above_15"]),
@@ -93,6 +113,10 @@ MUTANTS = [
     ("quant_act", _quant_act_fp32_scale, ["test_quant_act_golden"]),
     ("quant_act", _quant_act_half_up, ["test_quant_act_golden"]),
     ("w4a8_accumulate", _w4a8_acc_offset7, ["test_w4a8_accumulate_bruteforce"]),
+    ("w4a8_linear", _w4a8_linear_factory("drop_tok"), ["test_w4a8_epilogue_golden"]),
+    ("w4a8_linear", _w4a8_linear_factory("product_first"), ["test_w4a8_epilogue_golden"]),
+    ("w4a8_linear", _w4a8_linear_factory("fp16_intermediate"), ["test_w4a8_epilogue_golden"]),
+    ("w4a8_linear", _w4a8_linear_factory("float64"), ["test_w4a8_epilogue_golden"]),
 ]
 
 

@@ -269,3 +269,55 @@ def test_w4a8_unit_scales_return_integers():
 def test_w4a8_extremes_fit_int32_at_k21760():
     # worst case |acc| <= K * 128 * 8 stays below 2^31 at the largest K of the workloads
     assert 21760 * 128 * 8 < 2 ** 31
+
+
+# ---------------------------------------------------------------- W4A8 output epilogue
+def _binary_fraction(text: str) -> Fraction:
+    """'n/2^e' (or '-n/2^e') as an exact rational."""
+    num, den = text.split("/")
+    base, exp = den.split("^")
+    assert base.strip() == "2"
+    return Fraction(int(num)) / Fraction(2) ** int(exp)
+
+
+def _codes_for_accumulator(target: int, k: int):
+    """Activation codes xq (int8) and signed weights q (-8..7) over k rows with sum xq * q == target.
+
+    target = n * (127 * 7) + b * 7 + c with 0 <= b <= 126 and 0 <= c <= 6: n rows of 127 x 7, one of
+    b x 7 and one of c x 1 (negated codes for a negative target).
+    """
+    sign = -1 if target < 0 else 1
+    t = abs(target)
+    n, r = divmod(t, 127 * 7)
+    b, c = divmod(r, 7)
+    assert n + 2 <= k
+    xq = np.zeros(k, dtype=np.int64)
+    q = np.zeros(k, dtype=np.int64)
+    xq[:n], q[:n] = 127, 7
+    xq[n], q[n] = b, 7
+    xq[n + 1], q[n + 1] = c, 1
+    xq *= sign
+    assert int(np.dot(xq, q)) == target
+    return xq.astype(np.int8), q
+
+
+def test_w4a8_epilogue_golden(golden_dir):
+    # y = fp16(fp32(fp32(fp32(acc) * s_tok) * s_ch)) on hand-worked cases where an fp16 intermediate,
+    # a direct fp16 rounding of the exact product, the scale product taken first, an unrounded
+    # accumulator past 2^24 or a dropped token scale each give a different fp16 value
+    lines = read_golden(golden_dir, "w4a8_epilogue_examples.txt")
+    assert len(lines) == 6
+    for line in lines:
+        acc_t, st_t, sc_t, y_t, _ = (s.strip() for s in line.split(";"))
+        target = int(acc_t)
+        s_tok, s_ch, want = _binary_fraction(st_t), _binary_fraction(sc_t), _binary_fraction(y_t)
+        k = abs(target) // (127 * 7) + 2 + 6
+        xq, q = _codes_for_accumulator(target, k)
+        # one packed word: 8 output columns with the same weights and scale
+        wq = oracle.pack(np.repeat((q + 8)[:, None], 8, axis=1).astype(np.uint8))
+        st32 = np.array([float(s_tok)], dtype=np.float32)
+        sc16 = np.full(8, float(s_ch), dtype=np.float16)
+        assert Fraction(float(st32[0])) == s_tok and Fraction(float(sc16[0])) == s_ch  # exact inputs
+        y, acc = oracle.w4a8_linear(xq[None, :], st32, wq, sc16)
+        assert np.all(acc == target)
+        assert all(Fraction(float(v)) == want for v in y[0]), (line, y[0])
