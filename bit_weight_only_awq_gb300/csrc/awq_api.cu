@@ -166,8 +166,10 @@ awq_status awq_gemv(const uint16_t* x, const int32_t* qweight, const int32_t* qz
   if (st != AWQ_OK) return st;
   st = check_arch();
   if (st != AWQ_OK) return st;
+  int* err = device_error_ptr();
+  if (!err) return AWQ_ECUDA;
   return from_cuda(launch_gemv(x, reinterpret_cast<const uint32_t*>(qweight), reinterpret_cast<const uint32_t*>(qzeros),
-                               scales, y, M, K, N, plan, workspace, device_error_ptr(), (cudaStream_t)stream));
+                               scales, y, M, K, N, plan, workspace, err, (cudaStream_t)stream));
 }
 
 awq_status awq_gemm(const uint16_t* x, const int32_t* qweight, const int32_t* qzeros, const uint16_t* scales,

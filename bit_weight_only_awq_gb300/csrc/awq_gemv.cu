@@ -672,7 +672,7 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
           asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(c) : "l"(cnt) : "memory");
           if (c == nt - 1) break;
           if (now_ns() - t0 > kWaitLimitNs) {
-            atomicExch(err, 504);
+            if (err) atomicExch(err, 504);
             ok = false;
             break;
           }

@@ -77,6 +77,13 @@ extern "C" awq_status awq_gemv_noalloc(const uint16_t* x, const int32_t* qweight
     return AWQ_ECUDA;
   if (major != 10 || minor != 3) return AWQ_EARCH;
 
+  // The split-K tickets occupy the first kCounterBytes of the array, one per tile; the partials follow.
+  if (plan.maxc > 1 && plan.tiles > kMaxCounters) return AWQ_EINVAL;
+  // The device error word is another file-scope __device__ variable of the library, so reporting a
+  // timed-out wait (awq_last_device_error) allocates nothing either.
+  int* err = device_error_ptr();
+  if (!err) return AWQ_ECUDA;
+
   void* scratch = nullptr;
   if (gemv_workspace_bytes(plan, M, N) > 0) {
     scratch = scratch_address();
@@ -88,6 +95,6 @@ extern "C" awq_status awq_gemv_noalloc(const uint16_t* x, const int32_t* qweight
   }
   const cudaError_t e = launch_gemv(x, reinterpret_cast<const uint32_t*>(qweight),
                                     reinterpret_cast<const uint32_t*>(qzeros), scales, y, M, K, N, plan, scratch,
-                                    nullptr, (cudaStream_t)stream);
+                                    err, (cudaStream_t)stream);
   return e == cudaSuccess ? AWQ_OK : AWQ_ECUDA;
 }

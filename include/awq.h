@@ -140,11 +140,16 @@ awq_status awq_gemv(const uint16_t *x, const int32_t *qweight, const int32_t *qz
  *    any stream capture.
  *  - Automatic split (split_k = 0) shrinks the split until its scratch fits 8 MiB
  *    (split 1 needs none); an explicit split_k whose scratch (64 KB of tickets +
- *    contributors per tile * tiles * 8 * 512 * 4 bytes) exceeds 8 MiB is rejected
+ *    contributors per tile * tiles * T * 512 * 4 bytes, with T = 8 token rows per
+ *    partial for M <= 8 and T = 16 for 9..16 tokens; the same size
+ *    awq_workspace_bytes(AWQ_OP_GEMV, ...) gives awq_gemv) exceeds 8 MiB is rejected
  *    with AWQ_EWORKSPACE.
  *  - Every call shares the array and clears the tickets it needs on `stream` before
  *    its kernel; calls whose kernels overlap on the GPU (other streams, other host
  *    threads) race on the array and must be serialized by the caller.
+ *  - A bounded device wait that expires is recorded in the same device error word as
+ *    awq_gemv's (read it with awq_last_device_error); that word is also a fixed
+ *    variable inside the library, so reporting allocates nothing.
  */
 awq_status awq_gemv_noalloc(const uint16_t *x, const int32_t *qweight, const int32_t *qzeros,
                             const uint16_t *scales, uint16_t *y, int64_t M, int64_t K, int64_t N,

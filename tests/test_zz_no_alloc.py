@@ -11,6 +11,7 @@ use.  The file sorts last so that a run stopping at the first failure has run ev
 import numpy as np
 import pytest
 
+import oracle
 from bit_weight_only_awq_gb300 import synth
 
 torch = pytest.importorskip("torch")
@@ -64,6 +65,26 @@ def test_noalloc_matches_gemv_on_two_calls_in_a_row(awq, M, K, N, split_k, symme
         assert np.all(np.isfinite(got))
         # both outputs are fp16: each carries its own output rounding (half an ulp, 2^-11 relative)
         assert np.max(np.abs(got - ref) - 2 * 2.0 ** -11 * np.abs(ref)) <= TOL * rms
+        # no bounded device wait of either call gave up
+        assert awq.awq_last_device_error() == 0
+
+
+@pytest.mark.parametrize("M,K,N,split_k", [(3, 1280, 416, 3), (9, 1280, 416, 0)])
+def test_noalloc_matches_the_oracle(awq, M, K, N, split_k):
+    # the same check straight against the CPU oracle (unrounded float64 product of its fp16 weights):
+    # |y - ref| <= 2e-3 * rms(ref) + 2^-11 |ref|, the bar of the GEMV parity tests
+    p = synth.awq_problem(M, K, N, seed=950 + M)
+    x, qw, qz, sc = _dev(p["x"]), _dev(p["qweight"]), _dev(p["qzeros"]), _dev(p["scales"])
+    ref = oracle.awq_linear(p["x"], p["qweight"], p["qzeros"], p["scales"], 128)
+    rms = np.sqrt(np.mean(ref ** 2))
+    for _ in range(2):
+        y = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda")
+        assert _noalloc_via_abi(awq, x, qw, qz, sc, y, split_k) == 0
+        torch.cuda.synchronize()
+        got = y.cpu().numpy().astype(np.float64)
+        assert np.all(np.isfinite(got))
+        assert np.max(np.abs(got - ref) - 2.0 ** -11 * np.abs(ref)) <= TOL * rms
+        assert awq.awq_last_device_error() == 0
 
 
 def test_noalloc_rejects_a_split_whose_scratch_exceeds_the_array(awq):
