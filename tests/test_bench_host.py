@@ -70,3 +70,45 @@ def test_decode_step_sizes():
     assert packed == 4 * (4096 * 12288 + 4096 * 4096 + 4096 * 22016 + 11008 * 4096) / 2 == 404750336
     total = sum(bench.call_bytes(k, M, K, N) for k, _, M, K, N in calls)
     assert 422e6 < total < 423e6
+
+
+def test_crossover_symmetric_workload_and_bytes():
+    calls = bench.workload_calls("crossover_sym")
+    assert calls == bench.workload_calls("crossover") and bench.is_symmetric("crossover_sym")
+    # symmetric weights carry no packed zero points: 4 * (K/128) * (N/8) bytes fewer
+    assert bench.w4a16_bytes(1, 4096, 6144) - bench.w4a16_sym_bytes(1, 4096, 6144) == 4 * 32 * 768
+    assert bench.call_bytes("gemv", 1, 4096, 6144, symmetric=True) == bench.w4a16_sym_bytes(1, 4096, 6144)
+    assert bench.workload_unit("crossover_sym") == "GB/s" and bench.workload_unit("prefill") == "TFLOP/s"
+
+
+def test_windows_cover_the_minimum_time():
+    assert bench.windows_needed(3.6, 1.0) == 278          # 278 windows of 3.6 ms >= 1 s
+    assert bench.windows_needed(400.0, 1.0) == 5          # never fewer than 5 windows
+    assert bench.windows_needed(250.0, 1.0) == 5 and bench.windows_needed(150.0, 1.0) == 7
+
+
+def test_workload_record_from_fabricated_timings():
+    # a decode step of 16 calls timed at 0.2 ms per step over 20-step windows: value = bytes / time
+    args = type("A", (), {"steps": 20})()
+    calls = bench.workload_calls("decode")
+    r = {"calls": calls, "symmetric": False, "win_ms": [4.0, 4.0, 4.2], "n_windows": 3, "ms": 4.0, "e2e_s": 0.008,
+         "clocks": {"sm_mhz": 2070}, "launches_per_step": 16, "h2d": 1, "d2h": 2,
+         "per_m": [(m, [c for c in calls if c[2] == m], 0.05) for m in (1, 2, 4, 8)]}
+    rec = bench.workload_record("decode", r, args, world=1)
+    step_bytes = sum(bench.call_bytes(k, M, K, N) for k, _, M, K, N in calls)
+    assert rec["value"] == pytest.approx(step_bytes / 0.2e-3 / 1e9, rel=1e-4)
+    assert rec["roofline"]["bound"] == "hbm" and rec["roofline"]["frac"] == pytest.approx(
+        rec["roofline"]["achieved"] / rec["roofline"]["peak"], rel=1e-3)
+    assert rec["e2e"]["value"] == pytest.approx(step_bytes / 0.4e-3 / 1e9, rel=1e-4)
+    assert rec["gpu_launches"] == 16 * 20 * 3
+    assert [row["M"] for row in rec["vs_M"]] == [1, 2, 4, 8]
+    m1 = rec["vs_M"][0]
+    b1 = sum(bench.call_bytes(k, M, K, N) for k, _, M, K, N in calls if M == 1)
+    assert m1["GB/s"] == pytest.approx(b1 / 0.05e-3 / 1e9, rel=1e-3) and m1["us_per_call"] == 12.5
+    # a tensor-bound sweep reports TFLOP/s against the sustained peak, with the burst fraction beside it
+    pcalls = bench.workload_calls("prefill")
+    r2 = dict(r, calls=pcalls, per_m=[(256, [c for c in pcalls if c[2] == 256], 1.0)])
+    rec2 = bench.workload_record("prefill", r2, args, world=1)
+    flops = sum(2.0 * M * K * N for _, _, M, K, N in pcalls)
+    assert rec2["unit"] == "TFLOP/s" and rec2["value"] == pytest.approx(flops / 0.2e-3 / 1e12, rel=1e-4)
+    assert rec2["roofline"]["bound"] == "tensor" and "frac_of_burst" in rec2["roofline"]
