@@ -100,3 +100,39 @@ def w4a8_problem(m: int, k: int, n: int, seed: int) -> dict:
     s_ch = rng.uniform(0.001, 0.01, size=(n,)).astype(np.float16)
     x = activations(rng, m, k)
     return {"x": x, "wq": wq, "s_ch": s_ch}
+
+
+def to_bf16_bits(a: np.ndarray) -> np.ndarray:
+    """Synthetic bf16 inputs: the upper 16 bits of each float32 (truncation), as uint16 bit patterns.
+
+    Any bf16 value is a valid input; truncation is the input recipe here, not the layer's rounding.
+    """
+    f = np.ascontiguousarray(np.asarray(a, dtype=np.float32))
+    return (f.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+
+
+def awq_problem_bf16(m: int, k: int, n: int, seed: int, group_size: int = GROUP_SIZE,
+                     symmetric: bool = False) -> dict:
+    """Inputs of one bf16 W4A16 AWQ linear call: the W4A16 recipe with bf16 activations
+    (N(0, 1)) and bf16 scales (U[0.002, 0.02]), both as uint16 bit patterns."""
+    if n % 8 or k % group_size:
+        raise ValueError("N must be a multiple of 8 and K a multiple of the group size")
+    rng = rng_for(seed)
+    qweight = random_words(rng, k, n // 8)
+    qzeros = None if symmetric else random_words(rng, k // group_size, n // 8)
+    scales = to_bf16_bits(rng.uniform(0.002, 0.02, size=(k // group_size, n)))
+    x = to_bf16_bits(rng.standard_normal((m, k), dtype=np.float32))
+    return {"x": x, "qweight": qweight, "qzeros": qzeros, "scales": scales, "group_size": group_size}
+
+
+def w4a8_group_problem(m: int, k: int, n: int, seed: int, group_size: int = GROUP_SIZE) -> dict:
+    """Inputs of one per-group W4A8 call: fp16 activations, packed u = q + 8 weights, integer group
+    factors s3 uniform on 1..16 (fp16 [K/g, N]) and fp16 channel scales s2 uniform on [1e-4, 1e-3]."""
+    if n % 8 or k % group_size:
+        raise ValueError("N must be a multiple of 8 and K a multiple of the group size")
+    rng = rng_for(seed)
+    wq = random_words(rng, k, n // 8)
+    s3 = rng.integers(1, 17, size=(k // group_size, n)).astype(np.float16)
+    s2 = rng.uniform(0.0001, 0.001, size=(n,)).astype(np.float16)
+    x = activations(rng, m, k)
+    return {"x": x, "wq": wq, "s3": s3, "s2": s2, "group_size": group_size}

@@ -14,6 +14,7 @@ function to something other than itself.
 
 from .awq_oracle import (  # noqa: F401
     AWQ_ORDER,
+    AWQ_ORDER_NEW,
     unpack,
     pack,
     dequant,
@@ -23,4 +24,10 @@ from .awq_oracle import (  # noqa: F401
     quant_act,
     w4a8_accumulate,
     w4a8_linear,
+    bf16_to_float,
+    bf16_round,
+    dequant_bf16,
+    awq_linear_bf16,
+    w4a8_group_accumulate,
+    w4a8_group_linear,
 )

@@ -45,28 +45,32 @@ import numpy as np
 # Older-format AWQ order map ("Speed up AWQ 2.5x with updated kernel",
 # casper-hansen's list of format differences).
 AWQ_ORDER = (0, 2, 4, 6, 1, 3, 5, 7)
+# The new format's order map (same list): nibble slot i holds column 8c + i.
+AWQ_ORDER_NEW = (0, 1, 2, 3, 4, 5, 6, 7)
 
 
-def unpack(packed: np.ndarray) -> np.ndarray:
+def unpack(packed: np.ndarray, order=AWQ_ORDER) -> np.ndarray:
     """Unpack an AWQ-packed int32 array [R, C] to 4-bit codes uint8 [R, 8C].
 
-    Nibble slot i of word c holds logical column 8c + AWQ_ORDER[i].
+    Nibble slot i of word c holds logical column 8c + order[i] (the older
+    format's map by default; ``AWQ_ORDER_NEW`` for the new format's).
     Pins: hand-worked words (golden file), pack/unpack round trip.
     """
     words = np.ascontiguousarray(packed).view(np.uint32)
     rows, cols = words.shape
     out = np.empty((rows, 8 * cols), dtype=np.uint8)
-    for slot, col in enumerate(AWQ_ORDER):
+    for slot, col in enumerate(order):
         nib = (words >> np.uint32(4 * slot)) & np.uint32(0xF)
         out[:, col::8] = nib.astype(np.uint8)
     return out
 
 
-def pack(q: np.ndarray) -> np.ndarray:
+def pack(q: np.ndarray, order=AWQ_ORDER) -> np.ndarray:
     """Pack 4-bit codes uint8 [R, N] (N % 8 == 0) into AWQ int32 words [R, N/8].
 
     Codes above 15 are clamped to 15 (the W4A8 page reports a packer bug from
-    a missing clamp; clamping is the defined behaviour here).
+    a missing clamp; clamping is the defined behaviour here).  ``order`` as for
+    ``unpack``.
     Pins: hand-worked words (golden file), round trip with ``unpack``.
     """
     q = np.asarray(q)
@@ -75,7 +79,7 @@ def pack(q: np.ndarray) -> np.ndarray:
     codes = np.minimum(q.astype(np.uint32), np.uint32(15))
     rows, n = codes.shape
     words = np.zeros((rows, n // 8), dtype=np.uint32)
-    for slot, col in enumerate(AWQ_ORDER):
+    for slot, col in enumerate(order):
         words |= codes[:, col::8] << np.uint32(4 * slot)
     return words.view(np.int32)
 
@@ -183,4 +187,115 @@ def w4a8_linear(xq: np.ndarray, s_tok: np.ndarray, wq_packed: np.ndarray,
     acc = w4a8_accumulate(xq, wq_packed)
     y32 = (acc.astype(np.float32) * np.asarray(s_tok, dtype=np.float32)[:, None])
     y32 = y32 * np.asarray(s_ch, dtype=np.float16).astype(np.float32)[None, :]
+    return y32.astype(np.float16), acc
+
+
+# ---------------------------------------------------------------- bfloat16
+# "Support W4A8 quantization for vllm": brisker asks for bf16 because many
+# models are trained in bf16; HandH1998 answers that bf16 is not supported
+# there.  The bf16 variant of the W4A16 layer takes bf16 activations and
+# scales and gives bf16 outputs; numpy has no bf16 type, so bf16 values
+# travel here as their uint16 bit patterns (the upper half of an IEEE
+# binary32 with the same sign and exponent).
+
+def bf16_to_float(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns (uint16) -> the exact values as float64."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return b.view(np.float32).astype(np.float64)
+
+
+def bf16_round(v: np.ndarray) -> np.ndarray:
+    """Round float32 values to bf16, to nearest with ties to even; returns uint16 bit patterns.
+
+    bf16 keeps the upper 16 bits of a binary32.  Rounding to nearest adds
+    half of the dropped part's weight (0x7FFF) plus the kept part's lowest
+    bit (which turns an exact tie towards the even neighbour), then drops
+    the lower 16 bits.  Finite inputs only.  Pins: hand-worked values and a
+    brute-force nearest-neighbour search over exact rationals (tests).
+    """
+    f = np.ascontiguousarray(np.asarray(v, dtype=np.float32))
+    if not np.all(np.isfinite(f)):
+        raise ValueError("bf16_round takes finite values")
+    bits = f.view(np.uint32).astype(np.uint64)
+    keep_lsb = (bits >> np.uint64(16)) & np.uint64(1)
+    return ((bits + np.uint64(0x7FFF) + keep_lsb) >> np.uint64(16)).astype(np.uint16)
+
+
+def dequant_bf16(qweight: np.ndarray, qzeros: np.ndarray | None, scales_bf16: np.ndarray,
+                 group_size: int) -> np.ndarray:
+    """W[k, n] = bf16_RN((q[k, n] - z[k // g, n]) * s[k // g, n]) with bf16 scales; bf16 bits [K, N].
+
+    The product of a 5-bit integer and an 8-bit significand is exact in
+    float32, so one bf16 rounding of it is the one rounding step.
+    """
+    q = unpack(qweight).astype(np.int64)
+    k_dim, n_dim = q.shape
+    g = int(group_size)
+    if g <= 0 or k_dim % g != 0:
+        raise ValueError("group_size must divide K")
+    n_groups = k_dim // g
+    if scales_bf16.shape != (n_groups, n_dim):
+        raise ValueError("scales must have shape [K/group_size, N]")
+    z = np.full((n_groups, n_dim), 8, dtype=np.int64) if qzeros is None else unpack(qzeros).astype(np.int64)
+    group_of_row = np.arange(k_dim) // g
+    prod = (q - z[group_of_row, :]).astype(np.float64) * bf16_to_float(scales_bf16)[group_of_row, :]
+    return bf16_round(prod.astype(np.float32))
+
+
+def awq_linear_bf16(x_bf16: np.ndarray, qweight: np.ndarray, qzeros: np.ndarray | None,
+                    scales_bf16: np.ndarray, group_size: int) -> np.ndarray:
+    """The bf16 W4A16 layer: bf16 dequantization, then the float64 product (unrounded).
+
+    Every product of two bf16 values is exact in float64.
+    """
+    w = bf16_to_float(dequant_bf16(qweight, qzeros, scales_bf16, group_size))
+    return bf16_to_float(x_bf16) @ w
+
+
+# ---------------------------------------------------------------- W4A8 with per-group weight scales
+# "Support W4A8 quantization for vllm": HandH1998 says the per-channel kernel
+# only uses the channel scale fragment, while per-group weight quantization
+# needs both the group and the channel scale; the per-channel path turns an
+# int4 weight into an int8 by a shift of 4 (a factor 16) with the channel
+# scale on the output; the global reduction works on int32; the GEMM takes
+# s1 (per token), s2 and s3.  Reading: s3 is the per-group factor that turns
+# an int4 weight into an int8 one, an integer in [1, 16] (16 on every group
+# reproduces the per-channel kernel's shift), stored as fp16 [K/g, N]; the
+# accumulator stays an exact integer and s2 (per channel) is applied on the
+# output exactly like the per-channel scale.
+
+def w4a8_group_accumulate(xq: np.ndarray, wq_packed: np.ndarray, s3: np.ndarray,
+                          group_size: int) -> np.ndarray:
+    """acc[m, n] = sum_k xq[m, k] * ((u[k, n] - 8) * s3[k // g, n]), exact int64.
+
+    s3 must hold integers in [1, 16] (fp16 storage), so every weight
+    (u - 8) * s3 lies in [-128, 112], an int8.  Pins: brute-force integer sums
+    on tiny inputs; s3 = 16 everywhere equals 16 times the per-channel
+    accumulator.
+    """
+    s3f = np.asarray(s3, dtype=np.float16).astype(np.float64)
+    if np.any(s3f != np.round(s3f)) or np.any(s3f < 1) or np.any(s3f > 16):
+        raise ValueError("s3 must hold integers in [1, 16]")
+    q = unpack(wq_packed).astype(np.int64) - 8
+    k_dim, n_dim = q.shape
+    g = int(group_size)
+    if g <= 0 or k_dim % g != 0 or s3f.shape != (k_dim // g, n_dim):
+        raise ValueError("s3 must have shape [K/group_size, N] with group_size dividing K")
+    w8 = q * s3f.astype(np.int64)[np.arange(k_dim) // g, :]
+    acc = xq.astype(np.int64) @ w8
+    if acc.size and (acc.max() > np.iinfo(np.int32).max or acc.min() < np.iinfo(np.int32).min):
+        raise OverflowError("W4A8 accumulator does not fit in int32")
+    return acc
+
+
+def w4a8_group_linear(xq: np.ndarray, s_tok: np.ndarray, wq_packed: np.ndarray, s3: np.ndarray,
+                      s2: np.ndarray, group_size: int):
+    """Per-group W4A8 output y = fp16_RN((fp32(acc) * s_tok[m]) * fp32(s2[n])), acc from
+    ``w4a8_group_accumulate`` (the same epilogue as ``w4a8_linear``, s2 in place of s_ch).
+
+    Returns (y fp16 [M, N], acc int64 [M, N]).
+    """
+    acc = w4a8_group_accumulate(xq, wq_packed, s3, group_size)
+    y32 = (acc.astype(np.float32) * np.asarray(s_tok, dtype=np.float32)[:, None])
+    y32 = y32 * np.asarray(s2, dtype=np.float16).astype(np.float32)[None, :]
     return y32.astype(np.float16), acc

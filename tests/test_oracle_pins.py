@@ -321,3 +321,170 @@ def test_w4a8_epilogue_golden(golden_dir):
         y, acc = oracle.w4a8_linear(xq[None, :], st32, wq, sc16)
         assert np.all(acc == target)
         assert all(Fraction(float(v)) == want for v in y[0]), (line, y[0])
+
+
+# ---------------------------------------------------------------- bfloat16 variant
+def _bf16_value(bits: int) -> Fraction:
+    """Exact value of a bf16 bit pattern (finite), decoded field by field."""
+    sign = -1 if bits & 0x8000 else 1
+    exp = (bits >> 7) & 0xFF
+    frac = bits & 0x7F
+    if exp == 0:
+        return sign * Fraction(frac, 128) * Fraction(2) ** -126
+    return sign * (1 + Fraction(frac, 128)) * Fraction(2) ** (exp - 127)
+
+
+def test_bf16_golden(golden_dir):
+    n_round = n_deq = 0
+    for line in read_golden(golden_dir, "bf16_examples.txt"):
+        lhs, rhs = (s.strip() for s in line.split(":"))
+        want = int(rhs, 16)
+        parts = lhs.split()
+        if parts[0] == "round":
+            f = np.array([int(parts[1], 16)], dtype=np.uint32).view(np.float32)
+            assert int(oracle.bf16_round(f)[0]) == want, line
+            n_round += 1
+        else:
+            q, z, sbits = int(parts[1]), int(parts[2]), int(parts[3], 16)
+            codes = np.zeros((128, 8), dtype=np.uint8)
+            codes[:, 0] = q
+            zc = np.zeros((1, 8), dtype=np.uint8)
+            zc[0, 0] = z
+            scales = np.full((1, 8), sbits, dtype=np.uint16)
+            w = oracle.dequant_bf16(oracle.pack(codes), oracle.pack(zc), scales, 128)
+            assert np.all(w[:, 0] == want), line
+            n_deq += 1
+    assert n_round == 7 and n_deq == 4
+
+
+def test_bf16_round_is_the_nearest_bf16():
+    # brute force: for random finite float32 values, the result is the nearer of the two bf16 values
+    # around the input (exact rational distances), the one with an even last bit on a tie
+    rng = np.random.default_rng(11)
+    bits = rng.integers(0, 2 ** 32, size=3000, dtype=np.uint64).astype(np.uint32)
+    bits = bits[((bits >> 23) & 0xFF) < 0xFE]            # finite and below the top binade
+    ties = (rng.integers(0, 2 ** 16, size=200, dtype=np.uint64).astype(np.uint32) << 16) | 0x8000
+    ties = ties[((ties >> 23) & 0xFF) < 0xFE]
+    bits = np.concatenate([bits, ties]).astype(np.uint32)
+    got = oracle.bf16_round(bits.view(np.float32))
+    for b, g in zip(bits.tolist(), got.tolist()):
+        v = Fraction(float(np.array([b], dtype=np.uint32).view(np.float32)[0]))
+        lo = b >> 16                                      # same sign, magnitude truncated
+        cands = [lo, lo + 1]
+        dist = [abs(_bf16_value(c) - v) for c in cands]
+        if dist[0] < dist[1]:
+            best = cands[0]
+        elif dist[1] < dist[0]:
+            best = cands[1]
+        else:
+            best = cands[0] if cands[0] % 2 == 0 else cands[1]
+        assert g == best, hex(b)
+
+
+def test_dequant_bf16_exhaustive_against_exact_rounding():
+    # every (q, z) pair x bf16 scales spanning several binades: the exact product rounded to the nearest
+    # bf16 (ties to even) by a search over exact rationals
+    rng = np.random.default_rng(12)
+    sbits = np.concatenate([rng.integers(0x3A00, 0x3D80, size=6), [0x3F83, 0x3CA4]]).astype(np.uint16)
+    q = np.repeat(np.arange(16), 16).astype(np.uint8)        # 256 rows: every (q, z)
+    zz = np.tile(np.arange(16), 16).astype(np.uint8)
+    for sb in sbits.tolist():
+        codes = np.zeros((256, 8), dtype=np.uint8)
+        codes[:, 3] = q
+        # one group per row: group size 1 makes every row its own zero point
+        zc = np.zeros((256, 8), dtype=np.uint8)
+        zc[:, 3] = zz
+        scales = np.full((256, 8), sb, dtype=np.uint16)
+        w = oracle.dequant_bf16(oracle.pack(codes), oracle.pack(zc), scales, 1)
+        s = _bf16_value(sb)
+        for r in range(256):
+            exact = (int(q[r]) - int(zz[r])) * s
+            if exact == 0:
+                assert _bf16_value(int(w[r, 3])) == 0
+                continue
+            mag = abs(exact)
+            e = mag.numerator.bit_length() - mag.denominator.bit_length()
+            while Fraction(2) ** e > mag:
+                e -= 1
+            while Fraction(2) ** (e + 1) <= mag:
+                e += 1
+            ulp = Fraction(2) ** (e - 7)
+            m = mag / ulp
+            f = floor(m)
+            if m - f > Fraction(1, 2) or (m - f == Fraction(1, 2) and f % 2 == 1):
+                f += 1
+            want = (1 if exact > 0 else -1) * f * ulp
+            assert _bf16_value(int(w[r, 3])) == want, (sb, r)
+
+
+def test_dequant_bf16_symmetric_and_group_index():
+    # symmetric: z = 8; group g of rows [128 g, 128 g + 128) takes scale row g
+    codes = np.full((256, 8), 12, dtype=np.uint8)
+    scales = np.zeros((2, 8), dtype=np.uint16)
+    scales[0, :] = 0x3F80   # 1.0
+    scales[1, :] = 0x4000   # 2.0
+    w = oracle.bf16_to_float(oracle.dequant_bf16(oracle.pack(codes), None, scales, 128))
+    assert np.all(w[:128] == 4.0) and np.all(w[128:] == 8.0)
+
+
+def test_linear_bf16_bruteforce_exact_rationals():
+    p = synth.awq_problem_bf16(2, 8, 8, seed=13, group_size=8)
+    w = oracle.dequant_bf16(p["qweight"], p["qzeros"], p["scales"], 8)
+    y = oracle.awq_linear_bf16(p["x"], p["qweight"], p["qzeros"], p["scales"], 8)
+    for m in range(2):
+        for n in range(8):
+            exact = sum(_bf16_value(int(p["x"][m, k])) * _bf16_value(int(w[k, n])) for k in range(8))
+            assert abs(Fraction(float(y[m, n])) - exact) <= abs(exact) * Fraction(1, 2 ** 52) + Fraction(1, 2 ** 120)
+
+
+# ---------------------------------------------------------------- W4A8 with per-group weight scales
+def test_w4a8_group_accumulate_bruteforce():
+    p = synth.w4a8_group_problem(3, 16, 16, seed=14, group_size=8)
+    xq, _ = oracle.quant_act(p["x"])
+    acc = oracle.w4a8_group_accumulate(xq, p["wq"], p["s3"], 8)
+    words = p["wq"].view(np.uint32)
+    for m in range(3):
+        for n in range(16):
+            total = 0
+            for k in range(16):
+                slot = oracle.AWQ_ORDER.index(n % 8)
+                u = (int(words[k, n // 8]) >> (4 * slot)) & 0xF
+                total += int(xq[m, k]) * (u - 8) * int(p["s3"][k // 8, n])
+            assert acc[m, n] == total
+
+
+def test_w4a8_group_factor_16_is_the_per_channel_kernel():
+    # s3 = 16 on every group is the per-channel kernel's shift by 4: the accumulator is 16 times the
+    # per-channel one, and with s2 = s_ch / 16 (exact) the fp16 outputs are identical
+    p = synth.w4a8_problem(4, 256, 64, seed=15)
+    xq, s = oracle.quant_act(p["x"])
+    s3 = np.full((2, 64), 16, dtype=np.float16)
+    acc_g = oracle.w4a8_group_accumulate(xq, p["wq"], s3, 128)
+    assert np.array_equal(acc_g, 16 * oracle.w4a8_accumulate(xq, p["wq"]))
+    s2 = (p["s_ch"].astype(np.float32) / 16).astype(np.float16)
+    assert np.array_equal(s2.astype(np.float32) * 16, p["s_ch"].astype(np.float32))
+    y_g, _ = oracle.w4a8_group_linear(xq, s, p["wq"], s3, s2, 128)
+    y_c, _ = oracle.w4a8_linear(xq, s, p["wq"], p["s_ch"])
+    assert np.array_equal(y_g.view(np.uint16), y_c.view(np.uint16))
+
+
+def test_w4a8_group_rejects_non_integer_factors():
+    p = synth.w4a8_group_problem(1, 128, 8, seed=16)
+    xq, _ = oracle.quant_act(p["x"])
+    bad = p["s3"].copy()
+    bad[0, 0] = 1.5
+    for s3 in (bad, np.zeros_like(p["s3"]), np.full_like(p["s3"], 17)):
+        try:
+            oracle.w4a8_group_accumulate(xq, p["wq"], s3, 128)
+        except ValueError:
+            continue
+        raise AssertionError("accepted an s3 outside the integers 1..16")
+
+
+def test_new_order_map_round_trip_and_word():
+    # the new format's map: nibble slot i holds column 8c + i, so codes 0..7 pack to 0x76543210
+    q = np.arange(8, dtype=np.uint8)[None, :]
+    assert int(oracle.pack(q, oracle.AWQ_ORDER_NEW).view(np.uint32)[0, 0]) == 0x76543210
+    assert int(oracle.pack(q).view(np.uint32)[0, 0]) == 0x75316420
+    codes = synth.random_codes(5, 64, seed=17)
+    assert np.array_equal(oracle.unpack(oracle.pack(codes, oracle.AWQ_ORDER_NEW), oracle.AWQ_ORDER_NEW), codes)
