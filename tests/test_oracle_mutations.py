@@ -101,6 +101,39 @@ def _w4a8_linear_factory(kind):
     return w4a8_linear
 
 
+def _bf16_round_truncate(v):
+    f = np.ascontiguousarray(np.asarray(v, dtype=np.float32))
+    return (f.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+
+
+def _bf16_round_ties_away(v):
+    f = np.ascontiguousarray(np.asarray(v, dtype=np.float32))
+    return ((f.view(np.uint32).astype(np.uint64) + np.uint64(0x8000)) >> np.uint64(16)).astype(np.uint16)
+
+
+def _dequant_bf16_zero7(qweight, qzeros, scales_bf16, group_size):
+    q = O.unpack(qweight).astype(np.int64)
+    k_dim, n_dim = q.shape
+    g = int(group_size)
+    z = np.full((k_dim // g, n_dim), 7, np.int64) if qzeros is None else O.unpack(qzeros).astype(np.int64)
+    gi = np.arange(k_dim) // g
+    prod = (q - z[gi]).astype(np.float64) * O.bf16_to_float(scales_bf16)[gi]
+    return O.bf16_round(prod.astype(np.float32))
+
+
+def _group_acc_factory(kind):
+    def acc_fn(xq, wq_packed, s3, group_size):
+        q = O.unpack(wq_packed).astype(np.int64) - 8
+        k_dim, n_dim = q.shape
+        g = int(group_size)
+        s3i = np.asarray(s3, dtype=np.float16).astype(np.int64)
+        gi = (np.arange(k_dim) % (k_dim // g)) if kind == "group_mod" else (np.arange(k_dim) // g)
+        if kind == "offset7":
+            q = q + 1
+        return xq.astype(np.int64) @ (q * s3i[gi, :])
+    return acc_fn
+
+
 MUTANTS = [
     ("unpack", _unpack_inverse_map, ["test_unpack_pack_golden"]),
     ("pack", _pack_no_clamp, ["test_pack_clamps_codes_above_15"]),
@@ -117,6 +150,12 @@ MUTANTS = [
     ("w4a8_linear", _w4a8_linear_factory("product_first"), ["test_w4a8_epilogue_golden"]),
     ("w4a8_linear", _w4a8_linear_factory("fp16_intermediate"), ["test_w4a8_epilogue_golden"]),
     ("w4a8_linear", _w4a8_linear_factory("float64"), ["test_w4a8_epilogue_golden"]),
+    ("bf16_round", _bf16_round_truncate, ["test_bf16_golden", "test_bf16_round_is_the_nearest_bf16"]),
+    ("bf16_round", _bf16_round_ties_away, ["test_bf16_golden", "test_bf16_round_is_the_nearest_bf16"]),
+    ("dequant_bf16", _dequant_bf16_zero7, ["test_dequant_bf16_symmetric_and_group_index"]),
+    ("w4a8_group_accumulate", _group_acc_factory("group_mod"), ["test_w4a8_group_accumulate_bruteforce"]),
+    ("w4a8_group_accumulate", _group_acc_factory("offset7"), ["test_w4a8_group_accumulate_bruteforce",
+                                                               "test_w4a8_group_factor_16_is_the_per_channel_kernel"]),
 ]
 
 
