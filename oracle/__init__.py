@@ -30,4 +30,6 @@ from .awq_oracle import (  # noqa: F401
     awq_linear_bf16,
     w4a8_group_accumulate,
     w4a8_group_linear,
+    PREPACK_UNIT_BYTES,
+    prepack_gemv,
 )

@@ -299,3 +299,69 @@ def w4a8_group_linear(xq: np.ndarray, s_tok: np.ndarray, wq_packed: np.ndarray, 
     y32 = (acc.astype(np.float32) * np.asarray(s_tok, dtype=np.float32)[:, None])
     y32 = y32 * np.asarray(s2, dtype=np.float16).astype(np.float32)[None, :]
     return y32.astype(np.float16), acc
+
+
+# ---------------------------------------------------------------- decode prepack (a private layout)
+# "Support W4A8 quantization for vllm": the QQQ kernel shuffles the eight int4
+# weights of each int32 offline so that every thread of a warp fetches the
+# weights it needs.  The decode GEMV of this library takes an offline-prepared
+# copy of an AWQ layer in the layout restated below; the layout changes where
+# each code, zero point and scale sits, never its value.
+PREPACK_TILE_COLS = 256   # output columns per tile
+PREPACK_GROUP = 128       # rows per unit (one quantization group)
+PREPACK_UNIT_BYTES = PREPACK_GROUP * PREPACK_TILE_COLS // 2 + PREPACK_TILE_COLS // 2 + 2 * PREPACK_TILE_COLS
+
+
+def prepack_gemv(qweight: np.ndarray, qzeros: np.ndarray | None, scales: np.ndarray) -> np.ndarray:
+    """Prepared decode-GEMV copy of an AWQ layer (group size 128); returns uint8 bytes.
+
+    Units (tile T of 256 columns, group G of 128 rows) follow each other in the
+    order T-major, G-minor; each unit is 17024 bytes:
+      * 16384 bytes of codes: uint32 words [w 4][i 8][l 32][b 4].  Word
+        (w, i, l, b) with g = l // 4, t = l % 4, columns ce = 256 T + 64 w + 8 g + 2 b
+        and co = ce + 1, rows k = 128 G + 16 i + (2t, 2t+1, 2t+8, 2t+9) holds, from
+        the lowest nibble up: q[2t, ce], q[2t, co], q[2t+8, ce], q[2t+8, co],
+        q[2t+1, ce], q[2t+1, co], q[2t+9, ce], q[2t+9, co];
+      * 128 bytes of zero points: uint32 words [w 4][g 8]; nibble c of word (w, g)
+        is z of column 256 T + 64 w + 8 g + c (8 when ``qzeros`` is None);
+      * 512 bytes of scales: fp16 [w 4][g 8][c 8], the scale of the same column.
+    Columns at or beyond N get code 0, zero point 0 and scale 0.
+    Pins: every code, zero point and scale found again by decoding the layout
+    back (tests); the layout's defining cases worked by hand.
+    """
+    q = unpack(qweight)
+    k_dim, n_dim = q.shape
+    if k_dim % PREPACK_GROUP:
+        raise ValueError("K must be a multiple of 128")
+    groups = k_dim // PREPACK_GROUP
+    tiles = -(-n_dim // PREPACK_TILE_COLS)
+    n_pad = tiles * PREPACK_TILE_COLS
+    qp = np.zeros((k_dim, n_pad), dtype=np.uint32)
+    qp[:, :n_dim] = q
+    zp = np.zeros((groups, n_pad), dtype=np.uint32)
+    zp[:, :n_dim] = 8 if qzeros is None else unpack(qzeros)
+    sp = np.zeros((groups, n_pad), dtype=np.float16)
+    sp[:, :n_dim] = scales
+    out = np.zeros((tiles, groups, PREPACK_UNIT_BYTES), dtype=np.uint8)
+    # code words: index arrays over (T, G, w, i, l, b)
+    T, G, w, i, l, b = np.meshgrid(np.arange(tiles), np.arange(groups), np.arange(4), np.arange(8),
+                                   np.arange(32), np.arange(4), indexing="ij")
+    g, t = l // 4, l % 4
+    ce = 256 * T + 64 * w + 8 * g + 2 * b
+    co = ce + 1
+    k0 = 128 * G + 16 * i + 2 * t
+    nibbles = (qp[k0, ce], qp[k0, co], qp[k0 + 8, ce], qp[k0 + 8, co],
+               qp[k0 + 1, ce], qp[k0 + 1, co], qp[k0 + 9, ce], qp[k0 + 9, co])
+    words = np.zeros(T.shape, dtype=np.uint32)
+    for pos, nib in enumerate(nibbles):
+        words |= nib << np.uint32(4 * pos)
+    out[:, :, :16384] = words.reshape(tiles, groups, -1).view(np.uint8)
+    # zero-point words and scale vectors: [T][G][w][g][c]
+    zsel = zp.reshape(groups, tiles, 4, 8, 8).transpose(1, 0, 2, 3, 4)
+    zwords = np.zeros((tiles, groups, 4, 8), dtype=np.uint32)
+    for c in range(8):
+        zwords |= zsel[..., c] << np.uint32(4 * c)
+    out[:, :, 16384:16512] = zwords.reshape(tiles, groups, -1).view(np.uint8)
+    ssel = sp.reshape(groups, tiles, 4, 8, 8).transpose(1, 0, 2, 3, 4)
+    out[:, :, 16512:] = np.ascontiguousarray(ssel).reshape(tiles, groups, -1).view(np.uint8)
+    return out.reshape(-1)

@@ -134,6 +134,15 @@ def _group_acc_factory(kind):
     return acc_fn
 
 
+def _prepack_swapped_columns(qweight, qzeros, scales):
+    # even and odd columns of each block swapped
+    q = O.unpack(qweight)
+    q2 = q.reshape(q.shape[0], -1, 2)[:, :, ::-1].reshape(q.shape)
+    return _ORIGINAL_PREPACK(O.pack(q2), qzeros, scales)
+
+
+_ORIGINAL_PREPACK = O.prepack_gemv
+
 MUTANTS = [
     ("unpack", _unpack_inverse_map, ["test_unpack_pack_golden"]),
     ("pack", _pack_no_clamp, ["test_pack_clamps_codes_above_15"]),
@@ -156,6 +165,7 @@ MUTANTS = [
     ("w4a8_group_accumulate", _group_acc_factory("group_mod"), ["test_w4a8_group_accumulate_bruteforce"]),
     ("w4a8_group_accumulate", _group_acc_factory("offset7"), ["test_w4a8_group_accumulate_bruteforce",
                                                                "test_w4a8_group_factor_16_is_the_per_channel_kernel"]),
+    ("prepack_gemv", _prepack_swapped_columns, ["test_prepack_words_for_row_and_column_patterns"]),
 ]
 
 

@@ -488,3 +488,66 @@ def test_new_order_map_round_trip_and_word():
     assert int(oracle.pack(q).view(np.uint32)[0, 0]) == 0x75316420
     codes = synth.random_codes(5, 64, seed=17)
     assert np.array_equal(oracle.unpack(oracle.pack(codes, oracle.AWQ_ORDER_NEW), oracle.AWQ_ORDER_NEW), codes)
+
+
+# ---------------------------------------------------------------- decode prepack layout
+def _unit_words(buf, unit):
+    base = unit * oracle.PREPACK_UNIT_BYTES
+    return buf[base:base + 16384].view(np.uint32), buf[base + 16384:base + 16512].view(np.uint32), \
+        buf[base + 16512:base + oracle.PREPACK_UNIT_BYTES].view(np.float16)
+
+
+def _codes_to_qweight(q):
+    return oracle.pack(q.astype(np.uint8))
+
+
+def test_prepack_words_for_row_and_column_patterns():
+    # codes equal to the row index mod 16: word (w, i, l, b) holds rows 2t, 2t, 2t+8, 2t+8, 2t+1, 2t+1,
+    # 2t+9, 2t+9 (lowest nibble first), whatever w, i, b: lane 0 (t = 0) reads 0x99118800 and lane 1
+    # (t = 1) 0xBB33AA22
+    K, N = 256, 512
+    rows = (np.arange(K)[:, None] % 16 + np.zeros((1, N), int)).astype(np.uint8)
+    buf = oracle.prepack_gemv(_codes_to_qweight(rows), None, np.ones((K // 128, N), np.float16))
+    for unit in range(4):
+        words, _, _ = _unit_words(buf, unit)
+        w = words.reshape(4, 8, 32, 4)
+        assert np.all(w[:, :, 0, :] == 0x99118800) and np.all(w[:, :, 1, :] == 0xBB33AA22)
+    # codes equal to the column index mod 16: block b of lane g reads columns 8g + 2b (even positions)
+    # and 8g + 2b + 1 (odd positions): g = 0, b = 0 -> 0x10101010; b = 1 -> 0x32323232; g = 1, b = 0 ->
+    # 0x98989898
+    cols = (np.zeros((K, 1), int) + np.arange(N)[None, :] % 16).astype(np.uint8)
+    buf = oracle.prepack_gemv(_codes_to_qweight(cols), None, np.ones((K // 128, N), np.float16))
+    w = _unit_words(buf, 3)[0].reshape(4, 8, 32, 4)
+    assert np.all(w[:, :, 0:4, 0] == 0x10101010) and np.all(w[:, :, 0:4, 1] == 0x32323232)
+    assert np.all(w[:, :, 4:8, 0] == 0x98989898)
+
+
+def test_prepack_zero_and_scale_placement():
+    # zero point of column n = n mod 16: word (w, g) holds columns 64 w + 8 g + c in nibble c, so even g
+    # reads 0x76543210 and odd g 0xFEDCBA98; the symmetric layout holds 8 everywhere; scales sit in the
+    # same column order; columns beyond N hold zero point 0 and scale 0
+    K, N = 128, 480                                      # two tiles, the second one 224 columns wide
+    zc = (np.arange(N)[None, :] % 16).astype(np.uint8)
+    sc = (np.arange(N)[None, :] * 0.25).astype(np.float16)
+    buf = oracle.prepack_gemv(np.zeros((K, N // 8), np.int32), oracle.pack(zc), sc)
+    z0, s0 = _unit_words(buf, 0)[1].reshape(4, 8), _unit_words(buf, 0)[2].reshape(4, 8, 8)
+    assert np.all(z0[:, 0::2] == 0x76543210) and np.all(z0[:, 1::2] == 0xFEDCBA98)
+    assert np.array_equal(s0.reshape(-1), (np.arange(256) * 0.25).astype(np.float16))
+    z1, s1 = _unit_words(buf, 1)[1].reshape(-1), _unit_words(buf, 1)[2].reshape(-1)
+    assert np.all(z1[28:] == 0) and np.all(s1[224:] == 0)            # columns 480..511 are padding
+    assert np.array_equal(s1[:224], ((256 + np.arange(224)) * 0.25).astype(np.float16))
+    sym = oracle.prepack_gemv(np.zeros((K, N // 8), np.int32), None, sc)
+    assert np.all(_unit_words(sym, 0)[1] == 0x88888888)
+
+
+def test_prepack_is_a_permutation_of_the_codes():
+    # every unit holds exactly the codes of its 128 x 256 block, each once
+    p = synth.awq_problem(1, 256, 768, seed=18)
+    q = oracle.unpack(p["qweight"])
+    buf = oracle.prepack_gemv(p["qweight"], p["qzeros"], p["scales"])
+    for unit in range(6):
+        tile, grp = divmod(unit, 2)
+        words = _unit_words(buf, unit)[0]
+        nib = np.stack([(words >> np.uint32(4 * j)) & np.uint32(15) for j in range(8)]).ravel()
+        block = q[128 * grp:128 * grp + 128, 256 * tile:256 * tile + 256].ravel()
+        assert np.array_equal(np.bincount(nib, minlength=16), np.bincount(block, minlength=16))
