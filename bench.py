@@ -50,7 +50,7 @@ from bit_weight_only_awq_gb300 import synth  # noqa: E402
 
 WORKLOAD_FILTER = {"only": None, "ms": None}
 METRIC = "W4A16 group-quant GEMM TFLOP/s & HBM GB/s vs M; % of roofline on 1 GB300"
-WORKLOADS = ("decode", "prefill", "crossover", "crossover_sym", "w4a8")
+WORKLOADS = ("decode", "decode_awq", "prefill", "crossover", "crossover_sym", "w4a8")
 HEADLINE = "decode"
 L2_BYTES = 126 * 1024 * 1024  # GB300 L2 (the flush writes twice this)
 
@@ -92,6 +92,10 @@ def workload_calls(workload, only=None, ms=None):
 
 def _workload_calls(workload):
     if workload == "decode":
+        # the production decode path: weights prepared once at load time (awq_prepack_gemv)
+        return [("gemv_pp", n, m, k, nn) for n, k, nn in synth.LLAMA2_7B_DECODE for m in synth.DECODE_M]
+    if workload == "decode_awq":
+        # the same sweep on the AWQ-format words (awq_gemv), no preparation
         return [("gemv", n, m, k, nn) for n, k, nn in synth.LLAMA2_7B_DECODE for m in synth.DECODE_M]
     if workload == "prefill":
         return [("gemm", n, m, k, nn) for n, k, nn in synth.MISTRAL_7B_PREFILL for m in synth.PREFILL_M]
@@ -115,7 +119,7 @@ def call_bytes(kind, M, K, N, symmetric=False):
 
 def workload_unit(workload):
     """The sweep's own rate: GB/s where HBM bounds it (decode, crossover), TFLOP/s on the tensor cores."""
-    return "GB/s" if workload in ("decode", "crossover", "crossover_sym") else "TFLOP/s"
+    return "GB/s" if workload in ("decode", "decode_awq", "crossover", "crossover_sym") else "TFLOP/s"
 
 
 # ------------------------------------------------------------------ clocks
@@ -322,6 +326,9 @@ def build_inputs(torch, workload, device, only=None, ms=None):
             p = synth.awq_problem(M, K, N, seed=seed, symmetric=sym)
             b = {k: (None if p[k] is None else torch.from_numpy(p[k]).to(device))
                  for k in ("qweight", "qzeros", "scales")}
+            if kind == "gemv_pp":  # prepared once, as at model load; the AWQ words are not kept
+                b["pp"] = awq_module().awq_prepack_gemv(b["qweight"], b["qzeros"], b["scales"])
+                b.update(qweight=None, qzeros=None, scales=None)
         b["x_np"] = p["x"]
         b["meta"] = (kind, name, M, K, N)
         bufs.append(b)
@@ -366,12 +373,20 @@ def e2e_segments(torch, bufs, min_bytes):
     return segs
 
 
+def awq_module():
+    from bit_weight_only_awq_gb300 import awq
+    return awq
+
+
 def issue_step(awq, bufs, stream):
     """All calls of one step on `stream`; returns the number of kernels launched."""
     launches = 0
     for b in bufs:
         kind, _, M, K, N = b["meta"]
-        if kind == "gemv":
+        if kind == "gemv_pp":
+            awq.awq_gemv_prepacked(b["x"], b["pp"], out=b["y"], stream=stream)
+            launches += 1
+        elif kind == "gemv":
             awq.awq_gemv(b["x"], b["qweight"], b["qzeros"], b["scales"], out=b["y"], stream=stream)
             launches += 1
         elif kind == "gemm":
@@ -447,7 +462,8 @@ def gpu_workload(args, workload, world, torch, dist, awq, device, flush):
     # pre-size the shared workspace for the largest call, then warm every code path once
     for b in bufs:
         kind, _, M, K, N = b["meta"]
-        op = {"gemv": awq.OP_GEMV, "gemm": awq.OP_GEMM, "w4a8": awq.OP_W4A8_GEMM}[kind]
+        op = {"gemv": awq.OP_GEMV, "gemm": awq.OP_GEMM, "w4a8": awq.OP_W4A8_GEMM,
+              "gemv_pp": awq.OP_GEMV_PREPACKED}[kind]
         awq.device_workspace(awq.awq_workspace_bytes(op, M, K, N, 0), device)
     with torch.cuda.stream(stream):
         issue_step(awq, bufs, stream)
@@ -527,7 +543,8 @@ def gpu_workload(args, workload, world, torch, dist, awq, device, flush):
 
 
 def dominant_kernel(workload):
-    return {"decode": ("awq_gemv (gemv_kernel)", "hbm"), "prefill": ("awq_gemm (gemm_kernel)", "tensor"),
+    return {"decode": ("awq_gemv_prepacked (gemv_pp_kernel)", "hbm"),
+            "decode_awq": ("awq_gemv (gemv_kernel)", "hbm"), "prefill": ("awq_gemm (gemm_kernel)", "tensor"),
             "crossover": ("awq_gemv + awq_gemm", "hbm"), "crossover_sym": ("awq_gemv + awq_gemm", "hbm"),
             "w4a8": ("w4a8_linear (gemm_kernel<W4A8>)", "tensor")}[workload]
 

@@ -24,7 +24,7 @@ lib = ctypes.CDLL(_LIB_PATH)
 
 STATUS = {0: "AWQ_OK", -1: "AWQ_EINVAL", -2: "AWQ_EALIGN", -3: "AWQ_EARCH", -4: "AWQ_ECUDA",
           -5: "AWQ_ETIMEOUT", -6: "AWQ_EWORKSPACE", -7: "AWQ_ENULL"}
-OP_GEMV, OP_GEMM, OP_W4A8_GEMM = 0, 1, 2
+OP_GEMV, OP_GEMM, OP_W4A8_GEMM, OP_GEMV_PREPACKED = 0, 1, 2, 3
 GROUP_SIZE = 128
 
 _p = ctypes.c_void_p
@@ -44,6 +44,10 @@ _SIGS = {
     "w4a8_quant_act": (_i32, [_p, _p, _p, _i64, _i64, _p]),
     "w4a8_gemm": (_i32, [_p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _i32, _p, _sz, _p]),
     "w4a8_linear": (_i32, [_p, _p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _i32, _p, _sz, _p]),
+    "awq_prepacked_bytes": (_sz, [_i64, _i64]),
+    "awq_prepack_gemv": (_i32, [_p, _p, _p, _i64, _i64, _i32, _p, _sz, _p]),
+    "awq_unprepack_gemv": (_i32, [_p, _i64, _i64, _p, _p, _p, _p]),
+    "awq_gemv_prepacked": (_i32, [_p, _p, _p, _i64, _i64, _i64, _i32, _p, _sz, _p]),
     "awq_last_device_error": (_i32, [ctypes.POINTER(_i32)]),
     "awq_selftest_wait_timeout": (_i32, [_i64, _p]),
 }
@@ -171,6 +175,52 @@ def awq_gemv_noalloc(x, qweight, qzeros, scales, group_size: int = GROUP_SIZE, s
         out = torch.empty((M, N), dtype=torch.float16, device=x.device)
     _check("awq_gemv_noalloc", lib.awq_gemv_noalloc(_ptr(x), _ptr(qweight), _ptr(qzeros), _ptr(scales), _ptr(out),
                                                     M, K, N, group_size, split_k, _stream(stream)))
+    return out
+
+
+class Prepacked:
+    """A prepared decode copy of an AWQ layer (awq_prepack_gemv): the device bytes and the shape."""
+
+    def __init__(self, data: torch.Tensor, K: int, N: int):
+        self.data, self.K, self.N = data, K, N
+
+
+def awq_prepack_gemv(qweight, qzeros, scales, group_size: int = GROUP_SIZE, stream=None) -> Prepacked:
+    K, nw = qweight.shape
+    N = nw * 8
+    nbytes = int(lib.awq_prepacked_bytes(K, N))
+    if nbytes == 0:
+        raise AwqError("awq_prepack_gemv", -1)
+    data = torch.empty(nbytes, dtype=torch.uint8, device=qweight.device)
+    _check("awq_prepack_gemv", lib.awq_prepack_gemv(_ptr(qweight), _ptr(qzeros), _ptr(scales), K, N, group_size,
+                                                    _ptr(data), nbytes, _stream(stream)))
+    return Prepacked(data, K, N)
+
+
+def awq_unprepack_gemv(packed: Prepacked, with_zeros: bool = True, stream=None):
+    """The AWQ (qweight, qzeros or None, scales) that `packed` was made from."""
+    K, N = packed.K, packed.N
+    dev = packed.data.device
+    qweight = torch.empty((K, N // 8), dtype=torch.int32, device=dev)
+    qzeros = torch.empty((K // GROUP_SIZE, N // 8), dtype=torch.int32, device=dev) if with_zeros else None
+    scales = torch.empty((K // GROUP_SIZE, N), dtype=torch.float16, device=dev)
+    _check("awq_unprepack_gemv", lib.awq_unprepack_gemv(_ptr(packed.data), K, N, _ptr(qweight), _ptr(qzeros),
+                                                        _ptr(scales), _stream(stream)))
+    return qweight, qzeros, scales
+
+
+def awq_gemv_prepacked(x, packed: Prepacked, split_k: int = 0, out=None, workspace=None, stream=None):
+    M, K = x.shape
+    N = packed.N
+    if K != packed.K:
+        raise ValueError("x has K columns different from the prepared layer's")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    ws = workspace if workspace is not None else \
+        device_workspace(_workspace_need(OP_GEMV_PREPACKED, M, K, N, split_k, x.device), x.device)
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check("awq_gemv_prepacked", lib.awq_gemv_prepacked(_ptr(x), _ptr(packed.data), _ptr(out), M, K, N, split_k,
+                                                        _ptr(ws), nbytes, _stream(stream)))
     return out
 
 

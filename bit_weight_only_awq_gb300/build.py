@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG_DIR, "csrc")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libawq.so")
 
-SOURCES = ("awq_api.cu", "awq_elementwise.cu", "awq_gemv.cu", "awq_gemm_tc.cu", "w4a8_act.cu",
+SOURCES = ("awq_api.cu", "awq_elementwise.cu", "awq_gemv.cu", "awq_gemv_pp.cu", "awq_gemm_tc.cu", "w4a8_act.cu",
            "awq_noalloc.cu", "awq_selftest.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

@@ -142,6 +142,9 @@ size_t awq_workspace_bytes(awq_op op, int64_t M, int64_t K, int64_t N, int32_t s
     case AWQ_OP_GEMM:
       if (!gemm_shape_ok(M, K, N, split_k) || M == 0) return 0;
       return gemm_workspace_bytes(gemm_plan(M, K, N, split_k, kModeZeroPoint), M, K, N, kModeZeroPoint);
+    case AWQ_OP_GEMV_PREPACKED:
+      if (!gemv_shape_ok(M, K, N, kGroup, split_k) || M == 0 || M > 8) return 0;
+      return gemv_pp_workspace_bytes(gemv_pp_plan(M, K, N, split_k));
     case AWQ_OP_W4A8_GEMM: {
       if (!gemm_shape_ok(M, K, N, split_k) || M == 0) return 0;
       GemvPlan gp;
@@ -170,6 +173,53 @@ awq_status awq_gemv(const uint16_t* x, const int32_t* qweight, const int32_t* qz
   if (!err) return AWQ_ECUDA;
   return from_cuda(launch_gemv(x, reinterpret_cast<const uint32_t*>(qweight), reinterpret_cast<const uint32_t*>(qzeros),
                                scales, y, M, K, N, plan, workspace, err, (cudaStream_t)stream));
+}
+
+size_t awq_prepacked_bytes(int64_t K, int64_t N) {
+  if (!gemv_shape_ok(1, K, N, kGroup, 0)) return 0;
+  return prepacked_bytes(K, N);
+}
+
+awq_status awq_prepack_gemv(const int32_t* qweight, const int32_t* qzeros, const uint16_t* scales, int64_t K,
+                            int64_t N, int32_t group_size, void* packed, size_t packed_bytes, awq_stream_t stream) {
+  if (!gemv_shape_ok(1, K, N, group_size, 0)) return AWQ_EINVAL;
+  if (!qweight || !scales || !packed) return AWQ_ENULL;
+  if (!aligned16(qweight) || !aligned16(scales) || !aligned16(packed) || (qzeros && !aligned16(qzeros)))
+    return AWQ_EALIGN;
+  if (packed_bytes < prepacked_bytes(K, N)) return AWQ_EINVAL;
+  awq_status st = check_arch();
+  if (st != AWQ_OK) return st;
+  return from_cuda(launch_prepack(reinterpret_cast<const uint32_t*>(qweight), reinterpret_cast<const uint32_t*>(qzeros),
+                                  scales, K, N, static_cast<uint8_t*>(packed), (cudaStream_t)stream));
+}
+
+awq_status awq_unprepack_gemv(const void* packed, int64_t K, int64_t N, int32_t* qweight, int32_t* qzeros,
+                              uint16_t* scales, awq_stream_t stream) {
+  if (!gemv_shape_ok(1, K, N, kGroup, 0)) return AWQ_EINVAL;
+  if (!packed || !qweight || !scales) return AWQ_ENULL;
+  if (!aligned16(packed) || !aligned16(qweight) || !aligned16(scales) || (qzeros && !aligned16(qzeros)))
+    return AWQ_EALIGN;
+  awq_status st = check_arch();
+  if (st != AWQ_OK) return st;
+  return from_cuda(launch_unprepack(static_cast<const uint8_t*>(packed), K, N, reinterpret_cast<uint32_t*>(qweight),
+                                    reinterpret_cast<uint32_t*>(qzeros), scales, (cudaStream_t)stream));
+}
+
+awq_status awq_gemv_prepacked(const uint16_t* x, const void* packed, uint16_t* y, int64_t M, int64_t K, int64_t N,
+                              int32_t split_k, void* workspace, size_t workspace_bytes, awq_stream_t stream) {
+  if (!gemv_shape_ok(M, K, N, kGroup, split_k) || M > 8) return AWQ_EINVAL;
+  if (M == 0) return AWQ_OK;
+  if (!x || !packed || !y) return AWQ_ENULL;
+  if (!aligned16(x) || !aligned16(packed) || !aligned16(y)) return AWQ_EALIGN;
+  const GemvPlan plan = gemv_pp_plan(M, K, N, split_k);
+  awq_status st = check_workspace(gemv_pp_workspace_bytes(plan), workspace, workspace_bytes);
+  if (st != AWQ_OK) return st;
+  st = check_arch();
+  if (st != AWQ_OK) return st;
+  int* err = device_error_ptr();
+  if (!err) return AWQ_ECUDA;
+  return from_cuda(launch_gemv_prepacked(x, static_cast<const uint8_t*>(packed), y, M, K, N, plan, workspace, err,
+                                         (cudaStream_t)stream));
 }
 
 awq_status awq_gemm(const uint16_t* x, const int32_t* qweight, const int32_t* qzeros, const uint16_t* scales,

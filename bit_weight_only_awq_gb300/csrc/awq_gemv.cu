@@ -70,6 +70,7 @@
 #include "awq_internal.h"
 #include "awq_host.h"
 #include "awq_ptx.cuh"
+#include "awq_gemv_common.cuh"
 
 namespace awq {
 namespace {
@@ -111,29 +112,6 @@ struct Geo {
 };
 static_assert(kTileWords == kConsumers * 8, "one 8-word slice per consumer warp");
 
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-  uint32_t d;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
-  return d;
-}
-
-// (a & mask) | 0x64006400 in one LOP3
-template <uint32_t MASK>
-__device__ __forceinline__ uint32_t magic(uint32_t a) {
-  uint32_t d;
-  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "n"(MASK), "n"(0x64006400u));
-  return d;
-}
-
-
-__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};\n"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
 // PRMT selector: byte b of operand a -> result bytes 0,1; byte b of operand b -> bytes 2,3.
 __device__ __forceinline__ constexpr uint32_t byte_sel(int b) {
   return (uint32_t)(b | (b << 4) | ((b + 4) << 8) | ((b + 4) << 12));
@@ -155,10 +133,6 @@ __device__ __forceinline__ bool consumers_any(bool v) {
 __device__ __forceinline__ uint32_t q_offset(int row, int word) {
   return (uint32_t)((word >> 5) * kColStride + row * 128 + (((((word & 31) >> 2) ^ (row & 7))) << 4) +
                     (word & 3) * 4);
-}
-// Activation pair (k, k+1), k even (0..62), of token g in the 128-byte-swizzled 1 KB box.
-__device__ __forceinline__ uint32_t x_offset(int g, int k) {
-  return (uint32_t)(g * 128 + ((((k >> 3) ^ g)) << 4) + (k & 7) * 2);
 }
 
 // Lane-constant parts of the shared-memory addresses a consumer lane reads; every load of a

@@ -70,6 +70,23 @@ cudaError_t launch_gemv_w4a8(const uint16_t* x16, const uint32_t* wq, const floa
                              uint16_t* y, int32_t* acc_out, int64_t M, int64_t K, int64_t N, const GemvPlan& p,
                              void* ws, int* err, cudaStream_t s);
 
+// SMs of the current device (GB300's count when it cannot be queried)
+int device_sm_count();
+
+// ---- decode GEMV on the prepared layout (awq_gemv_pp.cu)
+constexpr int kPrepackTileCols = 256;   // output columns per unit
+constexpr int kPrepackUnitBytes = kGroup * kPrepackTileCols / 2 + kPrepackTileCols / 2 + 2 * kPrepackTileCols;
+static_assert(kPrepackUnitBytes == 17024 && kPrepackUnitBytes % 16 == 0, "prepared unit: codes | zeros | scales");
+size_t prepacked_bytes(int64_t K, int64_t N);
+cudaError_t launch_prepack(const uint32_t* qw, const uint32_t* qz, const uint16_t* sc, int64_t K, int64_t N,
+                           uint8_t* out, cudaStream_t s);
+cudaError_t launch_unprepack(const uint8_t* in, int64_t K, int64_t N, uint32_t* qw, uint32_t* qz, uint16_t* sc,
+                             cudaStream_t s);
+GemvPlan gemv_pp_plan(int64_t M, int64_t K, int64_t N, int split_k);
+size_t gemv_pp_workspace_bytes(const GemvPlan& p);
+cudaError_t launch_gemv_prepacked(const uint16_t* x, const uint8_t* packed, uint16_t* y, int64_t M, int64_t K,
+                                  int64_t N, const GemvPlan& p, void* ws, int* err, cudaStream_t s);
+
 // ---- tensor-core GEMM (awq_gemm_tc.cu)
 // kModeW4A8One is the W4A8 kernel for K slices of at most 16384 rows (kW4A8MaxKSlice): one exact
 // accumulator per M-block instead of two, which leaves tensor memory for two M-blocks of 256 tokens.

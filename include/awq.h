@@ -48,7 +48,12 @@ typedef enum {
 } awq_status;
 
 /* Operation selector for awq_workspace_bytes(). */
-typedef enum { AWQ_OP_GEMV = 0, AWQ_OP_GEMM = 1, AWQ_OP_W4A8_GEMM = 2 } awq_op;
+typedef enum {
+  AWQ_OP_GEMV = 0,
+  AWQ_OP_GEMM = 1,
+  AWQ_OP_W4A8_GEMM = 2,
+  AWQ_OP_GEMV_PREPACKED = 3
+} awq_op;
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char *awq_status_string(awq_status status);
@@ -154,6 +159,63 @@ awq_status awq_gemv(const uint16_t *x, const int32_t *qweight, const int32_t *qz
 awq_status awq_gemv_noalloc(const uint16_t *x, const int32_t *qweight, const int32_t *qzeros,
                             const uint16_t *scales, uint16_t *y, int64_t M, int64_t K, int64_t N,
                             int32_t group_size, int32_t split_k, awq_stream_t stream);
+
+/*
+ * Prepared decode weights.  The decode GEMV reads its weights fastest from a copy laid out for it,
+ * made once when the layer is loaded (the pages' W4A8 kernel shuffles its int4 weights offline in
+ * the same spirit: "Support W4A8 quantization for vllm", HandH1998 on the 8 INT4 weights of one
+ * INT32 shuffled offline so that every thread of a warp fetches the right weights).  The copy holds
+ * exactly the codes, zero points and scales of the AWQ layer, rearranged: for each 256-column tile
+ * (tile-major) and each 128-row group, one 17024-byte unit of
+ *   - codes as uint32 words [warp w: 4][16-row step i: 8][lane l: 32][column pair b: 4]; word
+ *     (w, i, l, b), with g = l / 4, t = l % 4, even column ce = 256 T + 64 w + 8 g + 2 b, odd column
+ *     co = ce + 1 and rows k = 128 G + 16 i + (2t, 2t+1, 2t+8, 2t+9), holds from the lowest nibble
+ *     up q[2t, ce], q[2t, co], q[2t+8, ce], q[2t+8, co], q[2t+1, ce], q[2t+1, co], q[2t+9, ce],
+ *     q[2t+9, co];
+ *   - zero points as uint32 words [w: 4][g: 8], nibble c = z of column 256 T + 64 w + 8 g + c
+ *     (8 for the symmetric variant);
+ *   - scales as fp16 [w: 4][g: 8][c: 8] of the same columns.
+ * Columns at or beyond N hold code 0, zero point 0 and scale 0.
+ *
+ * awq_prepacked_bytes -- bytes of the prepared copy: ceil(N / 256) * (K / 128) * 17024
+ * (0 for a shape the GEMV does not take: K % 128 != 0 or N % 32 != 0).
+ */
+size_t awq_prepacked_bytes(int64_t K, int64_t N);
+
+/*
+ * awq_prepack_gemv -- writes the prepared copy of an AWQ layer (group size 128) into `packed`
+ * (device memory of at least awq_prepacked_bytes(K, N) bytes, 16-byte aligned, caller-owned).
+ * qweight int32 [K, N/8]; qzeros int32 [K/128, N/8] or NULL (symmetric, z = 8); scales fp16
+ * [K/128, N].  K % 128 == 0, N % 32 == 0.  AWQ_EINVAL for a shape outside that or a `packed_bytes`
+ * below the size needed.  Bit-exact and reversible (awq_unprepack_gemv).
+ */
+awq_status awq_prepack_gemv(const int32_t *qweight, const int32_t *qzeros, const uint16_t *scales,
+                            int64_t K, int64_t N, int32_t group_size, void *packed,
+                            size_t packed_bytes, awq_stream_t stream);
+
+/*
+ * awq_unprepack_gemv -- the inverse: the AWQ words, zero points (packed like AWQ qzeros; pass NULL
+ * to skip them, e.g. for a symmetric layer) and scales that `packed` was made from.
+ */
+awq_status awq_unprepack_gemv(const void *packed, int64_t K, int64_t N, int32_t *qweight,
+                              int32_t *qzeros, uint16_t *scales, awq_stream_t stream);
+
+/*
+ * awq_gemv_prepacked -- y = x * W for M <= 8 tokens on the prepared copy: the same result as
+ * awq_gemv (the same fold of zero point and scale into fp32 sums, one rounding of the output; the
+ * fp32 summation order differs).  x fp16 [M, K], packed from awq_prepack_gemv, y fp16 [M, N].
+ * 1 <= M <= 8 (0 = no-op), K % 128 == 0, N % 32 == 0.  split_k as for awq_gemv, over 256-column
+ * tiles: a tile shared by several CTAs is completed by the CTA holding its first group, which waits
+ * (bounded) for the other contributors, so the call assumes its CTAs can all be resident at once.
+ * Needs a workspace when a tile is shared (awq_workspace_bytes(AWQ_OP_GEMV_PREPACKED, ...) > 0;
+ * same contract as awq_gemv's).  Two of its CTAs fit on one SM, so with programmatic dependent launch
+ * the next call's CTAs stream their weights while this call finishes.
+ * Source: as awq_gemv (the M <= 8 branch of the dispatch snippet in "Speed up AWQ 2.5x with updated
+ * kernel").
+ */
+awq_status awq_gemv_prepacked(const uint16_t *x, const void *packed, uint16_t *y, int64_t M,
+                              int64_t K, int64_t N, int32_t split_k, void *workspace,
+                              size_t workspace_bytes, awq_stream_t stream);
 
 /*
  * awq_gemm -- y = x * W on the tensor cores (tcgen05, fp16 x fp16 -> fp32 in

@@ -171,3 +171,27 @@ def test_binding_has_no_fallback(awq):
     src = open(awq.__file__).read()
     assert "oracle" not in src
     assert "numpy" not in src
+
+
+def test_prepared_layout_entry_points_check_arguments(awq):
+    lib = awq.lib
+    # size of the prepared copy: ceil(N / 256) tiles x K / 128 groups x 17024 bytes
+    assert lib.awq_prepacked_bytes(4096, 4096) == 16 * 32 * 17024
+    assert lib.awq_prepacked_bytes(4096, 4128) == 17 * 32 * 17024
+    assert lib.awq_prepacked_bytes(100, 4096) == 0 and lib.awq_prepacked_bytes(4096, 40) == 0
+    need = lib.awq_prepacked_bytes(256, 512)
+    assert lib.awq_prepack_gemv(FAKE, FAKE, FAKE, 256, 512, 128, FAKE, need - 16, None) == EINVAL
+    assert lib.awq_prepack_gemv(FAKE, FAKE, FAKE, 256, 512, 64, FAKE, need, None) == EINVAL
+    assert lib.awq_prepack_gemv(None, FAKE, FAKE, 256, 512, 128, FAKE, need, None) == ENULL
+    assert lib.awq_prepack_gemv(FAKE, FAKE, FAKE, 256, 512, 128, FAKE_MISALIGNED, need, None) == EALIGN
+    assert lib.awq_unprepack_gemv(FAKE, 256, 500, FAKE, FAKE, FAKE, None) == EINVAL
+    gp = lib.awq_gemv_prepacked
+    assert gp(FAKE, FAKE, FAKE, 9, 4096, 4096, 0, None, 0, None) == EINVAL      # up to 8 tokens
+    assert gp(FAKE, FAKE, FAKE, 0, 4096, 4096, 0, None, 0, None) == 0           # empty batch: no-op
+    assert gp(FAKE, None, FAKE, 4, 4096, 4096, 0, None, 0, None) == ENULL
+    assert gp(FAKE_MISALIGNED, FAKE, FAKE, 4, 4096, 4096, 0, None, 0, None) == EALIGN
+    # shared tiles need a workspace; split 1 (one CTA per tile) needs none
+    ws = awq.awq_workspace_bytes(awq.OP_GEMV_PREPACKED, 4, 4096, 4096, 0)
+    assert ws > 65536 and gp(FAKE, FAKE, FAKE, 4, 4096, 4096, 0, None, 0, None) == EWORKSPACE
+    assert awq.awq_workspace_bytes(awq.OP_GEMV_PREPACKED, 4, 4096, 4096, 1) == 0
+    assert awq.awq_workspace_bytes(awq.OP_GEMV_PREPACKED, 9, 4096, 4096, 0) == 0

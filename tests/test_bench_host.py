@@ -18,7 +18,9 @@ import bench  # noqa: E402
 def test_decode_workload_is_the_llama2_sweep():
     calls = bench.workload_calls("decode")
     assert len(calls) == 16
-    assert {c[0] for c in calls} == {"gemv"}
+    assert {c[0] for c in calls} == {"gemv_pp"}        # the prepared-weight decode GEMV
+    awq_layout = bench.workload_calls("decode_awq")   # the same calls on the AWQ words
+    assert [c[1:] for c in awq_layout] == [c[1:] for c in calls] and {c[0] for c in awq_layout} == {"gemv"}
     shapes = {(c[1], c[3], c[4]) for c in calls}
     assert shapes == {("qkv", 4096, 12288), ("o_proj", 4096, 4096), ("gate_up", 4096, 22016),
                       ("down", 11008, 4096)}
@@ -44,7 +46,7 @@ def test_crossover_routes_by_token_count():
 
 def test_filters():
     calls = bench.workload_calls("decode", only="qkv", ms=[8])
-    assert calls == [("gemv", "qkv", 8, 4096, 12288)]
+    assert calls == [("gemv_pp", "qkv", 8, 4096, 12288)]
     with pytest.raises(ValueError):
         bench.workload_calls("decode", only="nope")
 
