@@ -50,7 +50,8 @@ from bit_weight_only_awq_gb300 import synth  # noqa: E402
 
 WORKLOAD_FILTER = {"only": None, "ms": None}
 METRIC = "W4A16 group-quant GEMM TFLOP/s & HBM GB/s vs M; % of roofline on 1 GB300"
-WORKLOADS = ("decode", "decode_awq", "prefill", "crossover", "crossover_sym", "w4a8")
+WORKLOADS = ("decode", "decode_awq", "prefill", "crossover", "crossover_sym", "w4a8", "decode_bf16",
+             "prefill_bf16")
 HEADLINE = "decode"
 L2_BYTES = 126 * 1024 * 1024  # GB300 L2 (the flush writes twice this)
 
@@ -78,6 +79,10 @@ def is_symmetric(workload):
     return workload.endswith("_sym")
 
 
+def is_bf16(workload):
+    return workload.endswith("_bf16")
+
+
 def workload_calls(workload, only=None, ms=None):
     """List of (kind, name, M, K, N) for one step (optionally filtered by shape name / M)."""
     calls = _workload_calls(workload)
@@ -99,6 +104,10 @@ def _workload_calls(workload):
         return [("gemv", n, m, k, nn) for n, k, nn in synth.LLAMA2_7B_DECODE for m in synth.DECODE_M]
     if workload == "prefill":
         return [("gemm", n, m, k, nn) for n, k, nn in synth.MISTRAL_7B_PREFILL for m in synth.PREFILL_M]
+    if workload == "decode_bf16":
+        return [("gemv_bf16", n, m, k, nn) for n, k, nn in synth.LLAMA2_7B_DECODE for m in synth.DECODE_M]
+    if workload == "prefill_bf16":
+        return [("gemm_bf16", n, m, k, nn) for n, k, nn in synth.MISTRAL_7B_PREFILL for m in synth.PREFILL_M]
     if workload in ("crossover", "crossover_sym"):
         out = []
         for n, k, nn in synth.LLAMA31_8B_STACK:
@@ -119,7 +128,7 @@ def call_bytes(kind, M, K, N, symmetric=False):
 
 def workload_unit(workload):
     """The sweep's own rate: GB/s where HBM bounds it (decode, crossover), TFLOP/s on the tensor cores."""
-    return "GB/s" if workload in ("decode", "decode_awq", "crossover", "crossover_sym") else "TFLOP/s"
+    return "GB/s" if workload in ("decode", "decode_awq", "decode_bf16", "crossover", "crossover_sym") else "TFLOP/s"
 
 
 # ------------------------------------------------------------------ clocks
@@ -185,6 +194,8 @@ def _oracle_problems(workload, cols, seed):
     for i, (kind, name, M, K, N) in enumerate(workload_calls(workload)):
         if kind == "w4a8":
             problems.append((kind, M, K, synth.w4a8_problem(M, K, cols, seed=seed + i)))
+        elif is_bf16(workload):
+            problems.append((kind, M, K, synth.awq_problem_bf16(M, K, cols, seed=seed + i)))
         else:
             problems.append((kind, M, K, synth.awq_problem(M, K, cols, seed=seed + i, symmetric=sym)))
     return problems
@@ -217,6 +228,8 @@ def _oracle_passes(workload, budget_s, seed):
             if kind == "w4a8":
                 xq, s = oracle.quant_act(p["x"])
                 oracle.w4a8_linear(xq, s, p["wq"], p["s_ch"])
+            elif kind.endswith("_bf16"):
+                oracle.awq_linear_bf16(p["x"], p["qweight"], p["qzeros"], p["scales"], 128)
             else:
                 oracle.awq_linear(p["x"], p["qweight"], p["qzeros"], p["scales"], 128)
             spent += time.perf_counter() - t0
@@ -322,6 +335,11 @@ def build_inputs(torch, workload, device, only=None, ms=None):
             p = synth.w4a8_problem(M, K, N, seed=seed)
             b = {"wq": torch.from_numpy(p["wq"]).to(device), "s_ch": torch.from_numpy(p["s_ch"]).to(device)}
             b["s_tok"] = torch.empty((M,), dtype=torch.float32, device=device)
+        elif kind.endswith("_bf16"):
+            p = synth.awq_problem_bf16(M, K, N, seed=seed)
+            b = {k: torch.from_numpy(p[k]).to(device) for k in ("qweight", "qzeros")}
+            b["scales"] = torch.from_numpy(p["scales"].view(np.int16)).to(device).view(torch.bfloat16)
+            p["x"] = p["x"].view(np.int16)
         else:
             p = synth.awq_problem(M, K, N, seed=seed, symmetric=sym)
             b = {k: (None if p[k] is None else torch.from_numpy(p[k]).to(device))
@@ -335,14 +353,17 @@ def build_inputs(torch, workload, device, only=None, ms=None):
     # every view starts on a 16-byte boundary: M * K and M * N are multiples of 8 halves
     nx = sum(b["meta"][2] * b["meta"][3] for b in bufs)
     ny = sum(b["meta"][2] * b["meta"][4] for b in bufs)
-    packed = {"x": torch.empty(nx, dtype=torch.float16, device=device),
-              "x_host": torch.empty(nx, dtype=torch.float16).pin_memory(),
-              "y": torch.empty(ny, dtype=torch.float16, device=device),
-              "y_host": torch.empty(ny, dtype=torch.float16).pin_memory()}
+    dt = torch.bfloat16 if is_bf16(workload) else torch.float16
+    packed = {"x": torch.empty(nx, dtype=dt, device=device),
+              "x_host": torch.empty(nx, dtype=dt).pin_memory(),
+              "y": torch.empty(ny, dtype=dt, device=device),
+              "y_host": torch.empty(ny, dtype=dt).pin_memory()}
     ox = oy = 0
     for b in bufs:
         _, _, M, K, N = b["meta"]
         xh = torch.from_numpy(b.pop("x_np")).reshape(-1)
+        if dt == torch.bfloat16:
+            xh = xh.view(torch.bfloat16)
         packed["x_host"][ox:ox + M * K].copy_(xh)
         b["x"] = packed["x"][ox:ox + M * K].view(M, K)
         b["x"].copy_(xh.view(M, K))
@@ -385,6 +406,12 @@ def issue_step(awq, bufs, stream):
         kind, _, M, K, N = b["meta"]
         if kind == "gemv_pp":
             awq.awq_gemv_prepacked(b["x"], b["pp"], out=b["y"], stream=stream)
+            launches += 1
+        elif kind == "gemv_bf16":
+            awq.awq_gemv_bf16(b["x"], b["qweight"], b["qzeros"], b["scales"], out=b["y"], stream=stream)
+            launches += 1
+        elif kind == "gemm_bf16":
+            awq.awq_gemm_bf16(b["x"], b["qweight"], b["qzeros"], b["scales"], out=b["y"], stream=stream)
             launches += 1
         elif kind == "gemv":
             awq.awq_gemv(b["x"], b["qweight"], b["qzeros"], b["scales"], out=b["y"], stream=stream)
@@ -463,7 +490,7 @@ def gpu_workload(args, workload, world, torch, dist, awq, device, flush):
     for b in bufs:
         kind, _, M, K, N = b["meta"]
         op = {"gemv": awq.OP_GEMV, "gemm": awq.OP_GEMM, "w4a8": awq.OP_W4A8_GEMM,
-              "gemv_pp": awq.OP_GEMV_PREPACKED}[kind]
+              "gemv_pp": awq.OP_GEMV_PREPACKED, "gemv_bf16": awq.OP_GEMV_BF16, "gemm_bf16": awq.OP_GEMM_BF16}[kind]
         awq.device_workspace(awq.awq_workspace_bytes(op, M, K, N, 0), device)
     with torch.cuda.stream(stream):
         issue_step(awq, bufs, stream)
@@ -546,7 +573,9 @@ def dominant_kernel(workload):
     return {"decode": ("awq_gemv_prepacked (gemv_pp_kernel)", "hbm"),
             "decode_awq": ("awq_gemv (gemv_kernel)", "hbm"), "prefill": ("awq_gemm (gemm_kernel)", "tensor"),
             "crossover": ("awq_gemv + awq_gemm", "hbm"), "crossover_sym": ("awq_gemv + awq_gemm", "hbm"),
-            "w4a8": ("w4a8_linear (gemm_kernel<W4A8>)", "tensor")}[workload]
+            "w4a8": ("w4a8_linear (gemm_kernel<W4A8>)", "tensor"),
+            "decode_bf16": ("awq_gemv_bf16 (gemv_kernel<16, bf16>)", "hbm"),
+            "prefill_bf16": ("awq_gemm_bf16 (gemm_kernel<bf16>)", "tensor")}[workload]
 
 
 def load_traffic(workload, algorithmic_bytes_per_launch):
@@ -613,6 +642,7 @@ def workload_record(workload, r, args, world):
               "M": sorted({c[2] for c in calls}), "group_size": 128,
               "weights": "symmetric (zero 8, no qzeros)" if sym else ("per-channel int4, u = q + 8" if workload == "w4a8"
                                                                         else "zero-point (packed qzeros)"),
+              "activations": "bf16 (bf16 scales and output)" if is_bf16(workload) else "fp16",
               "kernels": sorted({c[0] for c in calls}), "calls_per_step": len(calls),
               "l2": "inputs larger than L2: every call of a step has its own weights "
                     f"({sum(c[3] * c[4] / 2 for c in calls) / 1e6:.0f} MB packed per step); per-M rates flush L2 "
@@ -698,7 +728,7 @@ def main():
         records[w] = workload_record(w, r, args, world)
     if rank == 0 and not args.no_cpu_baseline:
         for i, w in enumerate([head] + others):
-            budget = args.cpu_budget if i == 0 else max(1.0, args.cpu_budget / 2)
+            budget = args.cpu_budget if i == 0 else max(1.0, args.cpu_budget / 4)
             records[w]["cpu_baseline"] = cpu_baseline(w, budget, records[w]["unit"])
 
     if rank == 0:

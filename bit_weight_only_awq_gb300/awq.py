@@ -24,7 +24,7 @@ lib = ctypes.CDLL(_LIB_PATH)
 
 STATUS = {0: "AWQ_OK", -1: "AWQ_EINVAL", -2: "AWQ_EALIGN", -3: "AWQ_EARCH", -4: "AWQ_ECUDA",
           -5: "AWQ_ETIMEOUT", -6: "AWQ_EWORKSPACE", -7: "AWQ_ENULL"}
-OP_GEMV, OP_GEMM, OP_W4A8_GEMM, OP_GEMV_PREPACKED = 0, 1, 2, 3
+OP_GEMV, OP_GEMM, OP_W4A8_GEMM, OP_GEMV_PREPACKED, OP_GEMV_BF16, OP_GEMM_BF16 = 0, 1, 2, 3, 4, 5
 GROUP_SIZE = 128
 
 _p = ctypes.c_void_p
@@ -44,6 +44,9 @@ _SIGS = {
     "w4a8_quant_act": (_i32, [_p, _p, _p, _i64, _i64, _p]),
     "w4a8_gemm": (_i32, [_p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _i32, _p, _sz, _p]),
     "w4a8_linear": (_i32, [_p, _p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _i32, _p, _sz, _p]),
+    "awq_dequant_bf16": (_i32, [_p, _p, _p, _i64, _i64, _i32, _p, _p]),
+    "awq_gemv_bf16": (_i32, [_p, _p, _p, _p, _p, _i64, _i64, _i64, _i32, _i32, _p, _sz, _p]),
+    "awq_gemm_bf16": (_i32, [_p, _p, _p, _p, _p, _i64, _i64, _i64, _i32, _i32, _p, _sz, _p]),
     "awq_prepacked_bytes": (_sz, [_i64, _i64]),
     "awq_prepack_gemv": (_i32, [_p, _p, _p, _i64, _i64, _i32, _p, _sz, _p]),
     "awq_unprepack_gemv": (_i32, [_p, _i64, _i64, _p, _p, _p, _p]),
@@ -148,7 +151,7 @@ def _gemm_like(name, op, x, qweight, qzeros, scales, group_size, split_k, out, w
     M, K = x.shape
     N = qweight.shape[1] * 8
     if out is None:
-        out = torch.empty((M, N), dtype=torch.float16, device=x.device)
+        out = torch.empty((M, N), dtype=x.dtype, device=x.device)
     if ws is None:
         ws = device_workspace(_workspace_need(op, M, K, N, split_k, x.device), x.device)
     nbytes = 0 if ws is None else ws.numel() * ws.element_size()
@@ -227,6 +230,36 @@ def awq_gemv_prepacked(x, packed: Prepacked, split_k: int = 0, out=None, workspa
 def awq_gemm(x, qweight, qzeros, scales, group_size: int = GROUP_SIZE, split_k: int = 0, out=None,
              workspace=None, stream=None) -> torch.Tensor:
     return _gemm_like("awq_gemm", OP_GEMM, x, qweight, qzeros, scales, group_size, split_k, out, workspace, stream)
+
+
+def _need_bf16(*tensors):
+    for t in tensors:
+        if t is not None and t.dtype != torch.bfloat16:
+            raise TypeError("the bf16 entry points take bf16 activations and scales")
+
+
+def awq_dequant_bf16(qweight, qzeros, scales, group_size: int = GROUP_SIZE, out=None, stream=None):
+    _need_bf16(scales)
+    K, nw = qweight.shape
+    if out is None:
+        out = torch.empty((K, nw * 8), dtype=torch.bfloat16, device=qweight.device)
+    _check("awq_dequant_bf16", lib.awq_dequant_bf16(_ptr(qweight), _ptr(qzeros), _ptr(scales), K, nw * 8,
+                                                    group_size, _ptr(out), _stream(stream)))
+    return out
+
+
+def awq_gemv_bf16(x, qweight, qzeros, scales, group_size: int = GROUP_SIZE, split_k: int = 0, out=None,
+                  workspace=None, stream=None) -> torch.Tensor:
+    _need_bf16(x, scales)
+    return _gemm_like("awq_gemv_bf16", OP_GEMV_BF16, x, qweight, qzeros, scales, group_size, split_k, out,
+                      workspace, stream)
+
+
+def awq_gemm_bf16(x, qweight, qzeros, scales, group_size: int = GROUP_SIZE, split_k: int = 0, out=None,
+                  workspace=None, stream=None) -> torch.Tensor:
+    _need_bf16(x, scales)
+    return _gemm_like("awq_gemm_bf16", OP_GEMM_BF16, x, qweight, qzeros, scales, group_size, split_k, out,
+                      workspace, stream)
 
 
 GEMV_MAX_M = 16

@@ -112,6 +112,21 @@ awq_status awq_dequant(const int32_t* qweight, const int32_t* qzeros, const uint
                                   (cudaStream_t)stream));
 }
 
+awq_status awq_dequant_bf16(const int32_t* qweight, const int32_t* qzeros, const uint16_t* scales, int64_t K,
+                            int64_t N, int32_t group_size, uint16_t* w, awq_stream_t stream) {
+  if (group_size != 32 && group_size != 64 && group_size != 128 && group_size != 256) return AWQ_EINVAL;
+  if (K < 0 || N < 0 || K % group_size != 0 || N % 8 != 0) return AWQ_EINVAL;
+  if (K == 0 || N == 0) return AWQ_OK;
+  if (!qweight || !scales || !w) return AWQ_ENULL;
+  if (!aligned16(qweight) || !aligned16(scales) || !aligned16(w) || (qzeros && !aligned16(qzeros)))
+    return AWQ_EALIGN;
+  awq_status st = check_arch();
+  if (st != AWQ_OK) return st;
+  return from_cuda(launch_dequant(reinterpret_cast<const uint32_t*>(qweight),
+                                  reinterpret_cast<const uint32_t*>(qzeros), scales, K, N, group_size, w,
+                                  (cudaStream_t)stream, true));
+}
+
 static bool gemv_shape_ok(int64_t M, int64_t K, int64_t N, int32_t group_size, int32_t split_k) {
   return M >= 0 && M <= kGemvMaxM && K > 0 && K % kGroup == 0 && N > 0 && N % 32 == 0 && group_size == kGroup &&
          split_k >= 0 && K <= (int64_t)1 << 30 && N <= (int64_t)1 << 30;
@@ -142,6 +157,12 @@ size_t awq_workspace_bytes(awq_op op, int64_t M, int64_t K, int64_t N, int32_t s
     case AWQ_OP_GEMM:
       if (!gemm_shape_ok(M, K, N, split_k) || M == 0) return 0;
       return gemm_workspace_bytes(gemm_plan(M, K, N, split_k, kModeZeroPoint), M, K, N, kModeZeroPoint);
+    case AWQ_OP_GEMV_BF16:  // the 16-token instance: partials of 16 token rows
+      if (!gemv_shape_ok(M, K, N, kGroup, split_k) || M == 0) return 0;
+      return gemv_workspace_bytes(gemv_plan(M, K, N, split_k), 16, N);
+    case AWQ_OP_GEMM_BF16:
+      if (!gemm_shape_ok(M, K, N, split_k) || M == 0) return 0;
+      return gemm_workspace_bytes(gemm_plan(M, K, N, split_k, kModeZeroPointBF16), M, K, N, kModeZeroPointBF16);
     case AWQ_OP_GEMV_PREPACKED:
       if (!gemv_shape_ok(M, K, N, kGroup, split_k) || M == 0 || M > 8) return 0;
       return gemv_pp_workspace_bytes(gemv_pp_plan(M, K, N, split_k));
@@ -220,6 +241,53 @@ awq_status awq_gemv_prepacked(const uint16_t* x, const void* packed, uint16_t* y
   if (!err) return AWQ_ECUDA;
   return from_cuda(launch_gemv_prepacked(x, static_cast<const uint8_t*>(packed), y, M, K, N, plan, workspace, err,
                                          (cudaStream_t)stream));
+}
+
+awq_status awq_gemv_bf16(const uint16_t* x, const int32_t* qweight, const int32_t* qzeros, const uint16_t* scales,
+                         uint16_t* y, int64_t M, int64_t K, int64_t N, int32_t group_size, int32_t split_k,
+                         void* workspace, size_t workspace_bytes, awq_stream_t stream) {
+  if (!gemv_shape_ok(M, K, N, group_size, split_k)) return AWQ_EINVAL;
+  if (M == 0) return AWQ_OK;
+  if (!x || !qweight || !scales || !y) return AWQ_ENULL;
+  if (!aligned16(x) || !aligned16(qweight) || !aligned16(scales) || !aligned16(y) || (qzeros && !aligned16(qzeros)))
+    return AWQ_EALIGN;
+  const GemvPlan plan = gemv_plan(M, K, N, split_k);
+  awq_status st = check_workspace(gemv_workspace_bytes(plan, 16, N), workspace, workspace_bytes);
+  if (st != AWQ_OK) return st;
+  st = check_arch();
+  if (st != AWQ_OK) return st;
+  int* err = device_error_ptr();
+  if (!err) return AWQ_ECUDA;
+  return from_cuda(launch_gemv(x, reinterpret_cast<const uint32_t*>(qweight), reinterpret_cast<const uint32_t*>(qzeros),
+                               scales, y, M, K, N, plan, workspace, err, (cudaStream_t)stream, true));
+}
+
+awq_status awq_gemm_bf16(const uint16_t* x, const int32_t* qweight, const int32_t* qzeros, const uint16_t* scales,
+                         uint16_t* y, int64_t M, int64_t K, int64_t N, int32_t group_size, int32_t split_k,
+                         void* workspace, size_t workspace_bytes, awq_stream_t stream) {
+  if (!gemm_shape_ok(M, K, N, split_k) || group_size != kGroup) return AWQ_EINVAL;
+  if (M == 0) return AWQ_OK;
+  if (!x || !qweight || !scales || !y) return AWQ_ENULL;
+  if (!aligned16(x) || !aligned16(qweight) || !aligned16(scales) || !aligned16(y) || (qzeros && !aligned16(qzeros)))
+    return AWQ_EALIGN;
+  const int mode = qzeros ? kModeZeroPointBF16 : kModeSymmetricBF16;
+  const GemmPlan plan = gemm_plan(M, K, N, split_k, mode);
+  awq_status st = check_workspace(gemm_workspace_bytes(plan, M, K, N, mode), workspace, workspace_bytes);
+  if (st != AWQ_OK) return st;
+  st = check_arch();
+  if (st != AWQ_OK) return st;
+  int* err = device_error_ptr();
+  if (!err) return AWQ_ECUDA;
+  void* part = nullptr;
+  int* counters = nullptr;
+  if (plan.split > 1) {
+    if ((int64_t)plan.n_tiles * plan.m_tiles > kMaxCounters) return AWQ_EINVAL;
+    counters = static_cast<int*>(workspace);
+    part = static_cast<char*>(workspace) + kCounterBytes;
+  }
+  return from_cuda(launch_gemm(mode, x, reinterpret_cast<const uint32_t*>(qweight),
+                               reinterpret_cast<const uint32_t*>(qzeros), scales, nullptr, nullptr, y, nullptr, M,
+                               K, N, plan, part, counters, err, (cudaStream_t)stream));
 }
 
 awq_status awq_gemm(const uint16_t* x, const int32_t* qweight, const int32_t* qzeros, const uint16_t* scales,

@@ -3,6 +3,7 @@
 // Packing follows the older AWQ format ("Speed up AWQ 2.5x with updated kernel",
 // casper-hansen's format differences): nibble slot i of word c holds logical
 // column 8c + map[i], map = [0, 2, 4, 6, 1, 3, 5, 7].
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include "awq_internal.h"
@@ -49,12 +50,13 @@ __global__ void unpack_kernel(const uint32_t* __restrict__ packed, int64_t words
   }
 }
 
-// One thread per packed word (k, c): eight fp16 outputs W[k, 8c..8c+7].
-// (q - z) is an exact small integer and (q - z) * s is exact in fp32 (at most
-// 5 + 11 significant bits), so __float2half_rn performs the single rounding.
+// One thread per packed word (k, c): eight outputs W[k, 8c..8c+7], fp16 or (BF16) bf16 like the scales.
+// (q - z) is an exact small integer and (q - z) * s is exact in fp32 (at most 5 + 11 significant bits), so
+// the conversion to the output format (round to nearest even) performs the single rounding.
+template <bool BF16>
 __global__ void dequant_kernel(const uint32_t* __restrict__ qw, const uint32_t* __restrict__ qz,
-                               const __half* __restrict__ scales, int64_t K, int64_t nw, int group,
-                               __half* __restrict__ w) {
+                               const uint16_t* __restrict__ scales, int64_t K, int64_t nw, int group,
+                               uint16_t* __restrict__ w) {
   const int64_t words = K * nw;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < words;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -74,9 +76,14 @@ __global__ void dequant_kernel(const uint32_t* __restrict__ qw, const uint32_t* 
         const int col = 2 * pair + e;
         const int sh = 4 * slot_of_col(col);
         const int d = (int)((word >> sh) & 0xFu) - (int)((zword >> sh) & 0xFu);
-        const __half s = __ushort_as_half((unsigned short)(sw[pair] >> (16 * e)));
-        const __half r = __float2half_rn((float)d * __half2float(s));
-        halves |= (uint32_t)__half_as_ushort(r) << (16 * e);
+        const unsigned short sbits = (unsigned short)(sw[pair] >> (16 * e));
+        unsigned short r;
+        if constexpr (BF16) {
+          r = __bfloat16_as_ushort(__float2bfloat16_rn((float)d * __bfloat162float(__ushort_as_bfloat16(sbits))));
+        } else {
+          r = __half_as_ushort(__float2half_rn((float)d * __half2float(__ushort_as_half(sbits))));
+        }
+        halves |= (uint32_t)r << (16 * e);
       }
       outw[pair] = halves;
     }
@@ -101,11 +108,11 @@ cudaError_t launch_unpack(const uint32_t* packed, int64_t rows, int64_t n, uint8
 }
 
 cudaError_t launch_dequant(const uint32_t* qw, const uint32_t* qz, const uint16_t* scales, int64_t K,
-                           int64_t N, int group, uint16_t* w, cudaStream_t s) {
+                           int64_t N, int group, uint16_t* w, cudaStream_t s, bool bf16) {
   const int64_t words = K * (N / 8);
   if (words == 0) return cudaSuccess;
-  dequant_kernel<<<grid_for(words), kThreads, 0, s>>>(qw, qz, reinterpret_cast<const __half*>(scales), K,
-                                                      N / 8, group, reinterpret_cast<__half*>(w));
+  if (bf16) dequant_kernel<true><<<grid_for(words), kThreads, 0, s>>>(qw, qz, scales, K, N / 8, group, w);
+  else dequant_kernel<false><<<grid_for(words), kThreads, 0, s>>>(qw, qz, scales, K, N / 8, group, w);
   return cudaGetLastError();
 }
 

@@ -35,6 +35,7 @@
 //    slice spans at most 16384 rows, so every fp32 partial sum is an exact integer.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include "awq_internal.h"
@@ -56,6 +57,10 @@ constexpr int kWBlockBytes = kBK * kBN * 2;     // dequantized tile of one M-blo
 
 template <int MODE>
 constexpr bool kIsW4A8 = MODE == kModeW4A8 || MODE == kModeW4A8One;
+template <int MODE>
+constexpr bool kIsBF16 = MODE == kModeZeroPointBF16 || MODE == kModeSymmetricBF16;
+template <int MODE>
+constexpr bool kHasZeros = MODE == kModeZeroPoint || MODE == kModeZeroPointBF16;
 
 // NB M-blocks of 128 weight columns share every activation tile: with NB = 2 a CTA owns 256 columns
 // and the activation bytes per flop halve (the ring that feeds them was the measured limit at NB = 1).
@@ -90,8 +95,10 @@ struct Cfg {
   static constexpr bool kSoloMma = BT <= 64;
   static constexpr int kWarps = kSoloMma ? 24 : 3 + kDqWarps;
   static constexpr int kThreads = kWarps * 32;
-  // tcgen05 instruction descriptor, kind::f16: D f32, A/B f16, A MN-major, B K-major, M=128, N=BT
-  static constexpr uint32_t kIdesc = (1u << 4) | (1u << 15) | ((uint32_t)(BT >> 3) << 17) |
+  // tcgen05 instruction descriptor, kind::f16: D f32, A/B both f16 or both bf16 (bits 7-9 / 10-12),
+  // A MN-major, B K-major, M=128, N=BT
+  static constexpr uint32_t kAB = kIsBF16<MODE> ? ((1u << 7) | (1u << 10)) : 0u;
+  static constexpr uint32_t kIdesc = (1u << 4) | kAB | (1u << 15) | ((uint32_t)(BT >> 3) << 17) |
                                      ((uint32_t)(kBN >> 4) << 24);
   static_assert(kXStages >= 2 * kXSub, "activation ring");
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
@@ -129,6 +136,26 @@ __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
 // pair j of a packed word: (col 2j, col 2j+1) = nibble slots (j, j+4) as fp16 1024 + code
 __device__ __forceinline__ uint32_t pair_magic(uint32_t w, int j) {
   return ((w >> (4 * j)) & 0x000F000Fu) | 0x64006400u;
+}
+// the same pair as bf16 128 + code (exact: 128..143 needs 8 significant bits)
+__device__ __forceinline__ uint32_t pair_magic_bf16(uint32_t w, int j) {
+  return ((w >> (4 * j)) & 0x000F000Fu) | 0x43004300u;
+}
+__device__ __forceinline__ uint32_t bsub2(uint32_t a, uint32_t b) {  // exact here: (128 + q) - (128 + z)
+  uint32_t d;
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b) {  // one rounding to nearest even
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// fp32 output value -> the layer's output format (fp16 or bf16), round to nearest even
+template <int MODE>
+__device__ __forceinline__ __half out_cvt(float v) {
+  if constexpr (kIsBF16<MODE>) return __ushort_as_half(__bfloat16_as_ushort(__float2bfloat16_rn(v)));
+  else return __float2half_rn(v);
 }
 
 // ------------------------------------------------------------------ kernel
@@ -214,7 +241,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
       const bool is_x = warp == 0;
       const int S = is_x ? SX : kQStages;
       const uint32_t tx = is_x ? (uint32_t)C::kXSlotBytes
-                               : (uint32_t)(kQBytes + (MODE == kModeZeroPoint ? C::kZBytes : 0) +
+                               : (uint32_t)(kQBytes + (kHasZeros<MODE> ? C::kZBytes : 0) +
                                             (!kIsW4A8<MODE> ? C::kSBytes : 0));
       const int units = is_x ? nsteps * C::kXSub : nsteps;  // x: (k-step, 32-k half) slots
       int issued = 0;
@@ -231,7 +258,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
           uint8_t* qb = qring + st * kQStage;
           mbar_arrive_tx(fullq(st), tx);
           tma_load_2d(smem_u32(qb), &tm_q, n0 / 8, kb, fullq(st));
-          if (MODE == kModeZeroPoint) tma_load_2d(smem_u32(qb + kQBytes), &tm_z, n0 / 8, grp, fullq(st));
+          if (kHasZeros<MODE>) tma_load_2d(smem_u32(qb + kQBytes), &tm_z, n0 / 8, grp, fullq(st));
           if (!kIsW4A8<MODE>) tma_load_2d(smem_u32(qb + kQBytes + 128), &tm_s, n0, grp, fullq(st));
         }
       }
@@ -318,12 +345,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
       uint8_t* wt = wring + ws * kWBytes;
       uint32_t zp[4], sp[4];
       if (!kIsW4A8<MODE>) {
-        const uint32_t zword = MODE == kModeZeroPoint ? reinterpret_cast<const uint32_t*>(qb + kQBytes)[c]
-                                                      : 0x88888888u;
+        const uint32_t zword = kHasZeros<MODE> ? reinterpret_cast<const uint32_t*>(qb + kQBytes)[c]
+                                               : 0x88888888u;
         const uint4 sv = reinterpret_cast<const uint4*>(qb + kQBytes + 128)[c];
         sp[0] = sv.x; sp[1] = sv.y; sp[2] = sv.z; sp[3] = sv.w;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) zp[j] = pair_magic(zword, j);
+        for (int j = 0; j < 4; ++j) zp[j] = kIsBF16<MODE> ? pair_magic_bf16(zword, j) : pair_magic(zword, j);
       }
       uint32_t words[kPasses];
 #pragma unroll
@@ -336,9 +363,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         uint32_t o[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const uint32_t h = pair_magic(words[jr], j);
-          o[j] = kIsW4A8<MODE> ? hsub2(h, 0x64086408u) /* u - 8, exact */
-                                     : hmul2(hsub2(h, zp[j]), sp[j]);
+          if constexpr (kIsBF16<MODE>) {
+            o[j] = bmul2(bsub2(pair_magic_bf16(words[jr], j), zp[j]), sp[j]);
+          } else {
+            const uint32_t h = pair_magic(words[jr], j);
+            o[j] = kIsW4A8<MODE> ? hsub2(h, 0x64086408u) /* u - 8, exact */
+                                 : hmul2(hsub2(h, zp[j]), sp[j]);
+          }
         }
         const uint32_t off =
             blk_off + (uint32_t)((r >> 3) * 2048 + (cw >> 3) * 1024 + (r & 7) * 128 + (((cw & 7) ^ (r & 7)) << 4));
@@ -399,7 +430,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
               reinterpret_cast<int32_t*>(part)[(size_t)blockIdx.z * M * N + o] = a;
             }
           } else {
-            if (split == 1) y[o] = __float2half_rn(v[j]);
+            if (split == 1) y[o] = out_cvt<MODE>(v[j]);
             else reinterpret_cast<float*>(part)[(size_t)blockIdx.z * M * N + o] = v[j];
           }
         }
@@ -449,7 +480,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
               if (acc_out) acc_out[o] = a[j];
               y[o] = __float2half_rn(__fmul_rn(__fmul_rn((float)a[j], s_tok[m]), sch));
             } else {
-              y[o] = __float2half_rn(a[j]);
+              y[o] = out_cvt<MODE>(a[j]);
             }
           }
         }
@@ -478,7 +509,9 @@ cudaError_t launch_t(const uint16_t* x16, const uint32_t* qw, const uint32_t* qz
   constexpr int kQWords = C::kQWords;
   CUtensorMap tx, tq, tz, ts;
   const uint64_t nw = (uint64_t)N / 8, ng = (uint64_t)K / kGroup;
-  bool ok = make_map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x16, (uint64_t)K, (uint64_t)M, C::kXK, BT,
+  constexpr CUtensorMapDataType kHalfType = kIsBF16<MODE> ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                          : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  bool ok = make_map_2d(&tx, kHalfType, 2, x16, (uint64_t)K, (uint64_t)M, C::kXK, BT,
                         C::kXK == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B) &&
             make_map_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, qw, nw, (uint64_t)K, kQWords, kBK,
                         CU_TENSOR_MAP_SWIZZLE_NONE);
@@ -488,7 +521,7 @@ cudaError_t launch_t(const uint16_t* x16, const uint32_t* qw, const uint32_t* qz
   ok = ok && (kIsW4A8<MODE>
                   ? make_map_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, qw, nw, (uint64_t)K, kQWords, 1,
                                 CU_TENSOR_MAP_SWIZZLE_NONE)
-                  : make_map_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, sc, (uint64_t)N, ng, NB * kBN, 1,
+                  : make_map_2d(&ts, kHalfType, 2, sc, (uint64_t)N, ng, NB * kBN, 1,
                                 CU_TENSOR_MAP_SWIZZLE_NONE));
   if (!ok) return cudaErrorInvalidValue;
   auto kern = gemm_kernel<BT, NB, MODE>;
@@ -612,6 +645,12 @@ cudaError_t launch_gemm(int mode, const uint16_t* x16, const uint32_t* qw, const
       return launch_mode<kModeSymmetric>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters, err, s);
     case kModeW4A8:
       return launch_mode<kModeW4A8>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters, err, s);
+    case kModeZeroPointBF16:
+      return launch_mode<kModeZeroPointBF16>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters,
+                                             err, s);
+    case kModeSymmetricBF16:
+      return launch_mode<kModeSymmetricBF16>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters,
+                                             err, s);
     default:
       return cudaErrorInvalidValue;
   }

@@ -63,6 +63,7 @@
 //    free of bank conflicts, and every address is a lane constant plus an immediate.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include <type_traits>
@@ -267,10 +268,73 @@ __device__ __forceinline__ void group_consts_h(uint32_t zword, const uint4& sv, 
   }
 }
 
+// bf16 variant: 128 + q is exact in bf16 but 128 + 16 q does not fit its 8 significant bits' magic form
+// (the high nibble would reach the exponent), so high nibbles are shifted down first; both nibbles then
+// give 128 + code, zero points 128 + z, and the scale is s for both.
+__device__ __forceinline__ uint32_t magic_bf16(uint32_t a) {  // (a & 0x000F000F) | 0x43004300
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "n"(0x000F000Fu), "n"(0x43004300u));
+  return d;
+}
+__device__ __forceinline__ uint32_t bsub2(uint32_t a, uint32_t b) {  // exact here: (128 + q) - (128 + z)
+  uint32_t d;
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b) {  // one rounding to nearest even
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ void mma16816_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void group_consts_bf16(uint32_t zword, const uint4& sv, GroupConstsH& c) {
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    const uint32_t zb = prmt(zword, zword, byte_sel(b));
+    c.zlo[b] = magic_bf16(zb);       // 128 + z(slot 2b)
+    c.zhi[b] = magic_bf16(zb >> 4);  // 128 + z(slot 2b+1)
+    c.slo[b] = bcast_half(sv, order_map(2 * b));
+    c.shi[b] = bcast_half(sv, order_map(2 * b + 1));
+  }
+}
+
 // acc[h] += W^T x_h over the 64 rows held in `sr`, for the two 8-token halves h.  HSUB2 of the zero
-// (exact) then HMUL2 by the scale (s / 16 for the 16 q of the high nibble) give W = fp16_RN((q - z) s).
+// (exact) then HMUL2 by the scale (s / 16 for the 16 q of the high nibble) give W = fp16_RN((q - z) s);
+// BF16: the bf16 forms, W = bf16_RN((q - z) s).
+template <bool BF16 = false>
 __device__ __forceinline__ void compute_stage16(const StageRegs<16>& sr, const GroupConstsH& c,
                                                 float (&acc)[2][4][4]) {
+  if constexpr (BF16) {
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+      uint32_t p01[4], p23[4], a[4][4];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        p01[b] = prmt(sr.r[it][0], sr.r[it][1], byte_sel(b));
+        p23[b] = prmt(sr.r[it][2], sr.r[it][3], byte_sel(b));
+      }
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        a[b][0] = bmul2(bsub2(magic_bf16(p01[b]), c.zlo[b]), c.slo[b]);
+        a[b][1] = bmul2(bsub2(magic_bf16(p01[b] >> 4), c.zhi[b]), c.shi[b]);
+        a[b][2] = bmul2(bsub2(magic_bf16(p23[b]), c.zlo[b]), c.slo[b]);
+        a[b][3] = bmul2(bsub2(magic_bf16(p23[b] >> 4), c.zhi[b]), c.shi[b]);
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+          mma16816_bf16(acc[h][b], a[b][0], a[b][1], a[b][2], a[b][3], sr.b[h][it][0], sr.b[h][it][1]);
+    }
+    return;
+  }
 #pragma unroll
   for (int it = 0; it < 4; ++it) {
     uint32_t p01[4], p23[4], a[4][4];
@@ -291,6 +355,18 @@ __device__ __forceinline__ void compute_stage16(const StageRegs<16>& sr, const G
 #pragma unroll
       for (int b = 0; b < 4; ++b)
         mma16816(acc[h][b], a[b][0], a[b][1], a[b][2], a[b][3], sr.b[h][it][0], sr.b[h][it][1]);
+  }
+}
+
+// two fp32 outputs rounded (to nearest even) to the layer's output format, fp16 or bf16, as one word
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (BF16) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  } else {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
   }
 }
 
@@ -362,7 +438,8 @@ static_assert(kMaxRegs == 168, "9 warps: three on one sub-partition");
 // fp32 partial sum is an exact integer (the host keeps a CTA's rows of a tile at or below 16384, so
 // |sum| <= 1024 * 16384 = 2^24); partials are added as int32 and the output is
 // fp16((acc * s_tok[m]) * s_ch[n]), with acc also stored to acc_out when given.
-template <int T, bool EXACT>
+// BF16 (16 tokens only): bf16 activations, scales and output, W = bf16_RN((q - z) s) made exactly.
+template <int T, bool EXACT, bool BF16 = false>
 __global__ void __maxnreg__(kMaxRegs)
 gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_x,
             const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_s, int has_z,
@@ -370,6 +447,7 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             int M, int N, int RB, int tiles, int maxc, const float* __restrict__ s_tok,
             const __half* __restrict__ s_ch, int32_t* __restrict__ acc_out) {
   static_assert(!EXACT || T == 16, "the exact product uses the 16-token instance");
+  static_assert(!BF16 || (T == 16 && !EXACT), "the bf16 variant is the 16-token W4A16 instance");
   // RB = K / 64 row blocks per tile; unit u = (tile u / RB, row block u % RB); units < 2^31 (host check)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -512,6 +590,7 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
           const uint4 sv = EXACT ? make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u)  // 1.0
                                  : reinterpret_cast<const uint4*>(sb + kSOff)[word];
           if constexpr (T == 8) group_consts(zword, sv, gc);
+          else if constexpr (BF16) group_consts_bf16(zword, sv, gc);
           else group_consts_h(zword, sv, gc);
           cached_grp = grp;
         }
@@ -542,12 +621,12 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
           StageRegs<16> sr;
           load_stage<16>(sb, 0, lo, sr);
           if (nh == 2) {
-            compute_stage16(sr, gc, acc);
+            compute_stage16<BF16>(sr, gc, acc);
             load_stage<16>(sb, 1, lo, sr);
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(empty_bar(st));  // slot free before the last unit's arithmetic
-          compute_stage16(sr, gc, acc);
+          compute_stage16<BF16>(sr, gc, acc);
         }
       }
       if (failed) break;
@@ -582,8 +661,7 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 #pragma unroll
             for (int c = 0; c < 8; c += 2) {
               const int s0 = slot_of_col(c), s1 = slot_of_col(c + 1);
-              __half2 v = __floats2half2_rn(acc[hf][s0 >> 1][(s0 & 1) * 2 + par], acc[hf][s1 >> 1][(s1 & 1) * 2 + par]);
-              h[c / 2] = *reinterpret_cast<uint32_t*>(&v);
+              h[c / 2] = pack2<BF16>(acc[hf][s0 >> 1][(s0 & 1) * 2 + par], acc[hf][s1 >> 1][(s1 & 1) * 2 + par]);
             }
             *reinterpret_cast<uint4*>(y + (size_t)m * N + n0) = make_uint4(h[0], h[1], h[2], h[3]);
           }
@@ -752,9 +830,9 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             const int m = it / kQuads;
             const int n = own_tile * kTileCols + (it - m * kQuads) * 4;
             if (n < N) {  // N % 32 == 0: all four outputs are in range
-              __half2* dst = reinterpret_cast<__half2*>(y + (size_t)m * N + n);
-              dst[0] = __floats2half2_rn(s4[k].x, s4[k].y);
-              dst[1] = __floats2half2_rn(s4[k].z, s4[k].w);
+              uint32_t* dst = reinterpret_cast<uint32_t*>(y + (size_t)m * N + n);
+              dst[0] = pack2<BF16>(s4[k].x, s4[k].y);
+              dst[1] = pack2<BF16>(s4[k].z, s4[k].w);
             }
           }
         }
@@ -819,13 +897,13 @@ GemvPlan gemv_plan(int64_t M, int64_t K, int64_t N, int split_k) {
 size_t gemv_workspace_bytes(const GemvPlan& p, int64_t M, int64_t N) {
   (void)N;
   if (p.maxc <= 1) return 0;
-  const size_t tokens = M <= 8 ? 8 : 16;  // token rows of a partial: the kernel's T
+  const size_t tokens = M <= 8 ? 8 : 16;  // token rows of a partial: the kernel's T (bf16 always runs T = 16)
   return kCounterBytes + align256((size_t)p.tiles * p.maxc * tokens * kTileCols * sizeof(float));
 }
 
 namespace {
 
-template <int T, bool EXACT>
+template <int T, bool EXACT, bool BF16 = false>
 cudaError_t launch_gemv_t(const uint16_t* x, const uint32_t* qw, const uint32_t* qz, const uint16_t* sc,
                           uint16_t* y, int64_t M, int64_t K, int64_t N, const GemvPlan& p, void* ws, int* err,
                           cudaStream_t s, const float* s_tok = nullptr, const uint16_t* s_ch = nullptr,
@@ -842,8 +920,8 @@ cudaError_t launch_gemv_t(const uint16_t* x, const uint32_t* qw, const uint32_t*
   const bool ok =
       make_map_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, qw, nw, (uint64_t)K, kBoxWords, kRows,
                   CU_TENSOR_MAP_SWIZZLE_128B) &&
-      make_map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x, (uint64_t)K, (uint64_t)M, kRows, T,
-                  CU_TENSOR_MAP_SWIZZLE_128B) &&
+      make_map_2d(&tx, BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x, (uint64_t)K,
+                  (uint64_t)M, kRows, T, CU_TENSOR_MAP_SWIZZLE_128B) &&
       make_map_2d(&tz, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, qz ? (const void*)qz : (const void*)qw, nw,
                   qz ? ng : (uint64_t)K, kTileWords, 1, CU_TENSOR_MAP_SWIZZLE_NONE) &&
       (EXACT || make_map_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, sc, (uint64_t)N / 2, ng, kTileCols / 2, 1,
@@ -851,7 +929,7 @@ cudaError_t launch_gemv_t(const uint16_t* x, const uint32_t* qw, const uint32_t*
   if (!ok) return cudaErrorInvalidValue;
   if (EXACT) ts = tq;  // no scale rows are copied
   constexpr int kSmemBytes = Geo<T>::kSmemBytes;
-  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(gemv_kernel<T, EXACT>), kSmemBytes);
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(gemv_kernel<T, EXACT, BF16>), kSmemBytes);
   if (e != cudaSuccess) return e;
 
   cudaLaunchConfig_t cfg = {};
@@ -864,7 +942,7 @@ cudaError_t launch_gemv_t(const uint16_t* x, const uint32_t* qw, const uint32_t*
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, gemv_kernel<T, EXACT>, tq, tx, tz, ts, qz ? 1 : 0, reinterpret_cast<__half*>(y), part,
+  e = cudaLaunchKernelEx(&cfg, gemv_kernel<T, EXACT, BF16>, tq, tx, tz, ts, qz ? 1 : 0, reinterpret_cast<__half*>(y), part,
                          counters, err, (int)M, (int)N, (int)(K / kRows), p.tiles, p.maxc, s_tok,
                          reinterpret_cast<const __half*>(s_ch), acc_out);
   if (e != cudaSuccess) return e;
@@ -875,9 +953,10 @@ cudaError_t launch_gemv_t(const uint16_t* x, const uint32_t* qw, const uint32_t*
 
 cudaError_t launch_gemv(const uint16_t* x, const uint32_t* qw, const uint32_t* qz, const uint16_t* sc,
                         uint16_t* y, int64_t M, int64_t K, int64_t N, const GemvPlan& p, void* ws,
-                        int* err, cudaStream_t s) {
+                        int* err, cudaStream_t s, bool bf16) {
   // the kernel counts (tile, 64-row block) units in 32 bits; any tensor that fits a GPU stays far below
   if ((int64_t)p.tiles * p.groups >= ((int64_t)1 << 31)) return cudaErrorInvalidValue;
+  if (bf16) return launch_gemv_t<16, false, true>(x, qw, qz, sc, y, M, K, N, p, ws, err, s);
   if (M <= 8) return launch_gemv_t<8, false>(x, qw, qz, sc, y, M, K, N, p, ws, err, s);
   return launch_gemv_t<16, false>(x, qw, qz, sc, y, M, K, N, p, ws, err, s);
 }

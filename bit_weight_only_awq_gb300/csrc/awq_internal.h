@@ -35,8 +35,9 @@ int* device_error_ptr();  // nullptr if the symbol address could not be obtained
 // ---- elementwise kernels (awq_elementwise.cu)
 cudaError_t launch_pack(const uint8_t* q, int64_t rows, int64_t n, uint32_t* packed, cudaStream_t s);
 cudaError_t launch_unpack(const uint32_t* packed, int64_t rows, int64_t n, uint8_t* q, cudaStream_t s);
+// bf16: bf16 scales and output (else fp16)
 cudaError_t launch_dequant(const uint32_t* qw, const uint32_t* qz, const uint16_t* scales, int64_t K,
-                           int64_t N, int group, uint16_t* w, cudaStream_t s);
+                           int64_t N, int group, uint16_t* w, cudaStream_t s, bool bf16 = false);
 
 // ---- decode GEMV (awq_gemv.cu)
 constexpr int kNumSMs = 152;  // GB300
@@ -60,9 +61,10 @@ struct GemvPlan {
 };
 GemvPlan gemv_plan(int64_t M, int64_t K, int64_t N, int split_k);
 size_t gemv_workspace_bytes(const GemvPlan& p, int64_t M, int64_t N);
+// bf16: bf16 activations, scales and output on the 16-token instance (workspace rows as for M = 16)
 cudaError_t launch_gemv(const uint16_t* x, const uint32_t* qw, const uint32_t* qz, const uint16_t* sc,
                         uint16_t* y, int64_t M, int64_t K, int64_t N, const GemvPlan& p, void* ws,
-                        int* err, cudaStream_t s);
+                        int* err, cudaStream_t s, bool bf16 = false);
 // W4A8 on the 16-token GEMV (M <= 16): x16 = the int8 codes widened to fp16, wq = AWQ-packed u = q + 8,
 // exact int32 accumulators.  gemv_w4a8_ok: the plan keeps every CTA's rows of a tile within 16384.
 bool gemv_w4a8_ok(const GemvPlan& p, int64_t M);
@@ -91,7 +93,15 @@ cudaError_t launch_gemv_prepacked(const uint16_t* x, const uint8_t* packed, uint
 // kModeW4A8One is the W4A8 kernel for K slices of at most 16384 rows (kW4A8MaxKSlice): one exact
 // accumulator per M-block instead of two, which leaves tensor memory for two M-blocks of 256 tokens.
 // The plan picks it; callers pass kModeW4A8.
-enum GemmMode { kModeZeroPoint = 0, kModeSymmetric = 1, kModeW4A8 = 2, kModeW4A8One = 3 };
+// kModeZeroPointBF16 / kModeSymmetricBF16: the W4A16 modes with bf16 activations, scales and output.
+enum GemmMode {
+  kModeZeroPoint = 0,
+  kModeSymmetric = 1,
+  kModeW4A8 = 2,
+  kModeW4A8One = 3,
+  kModeZeroPointBF16 = 4,
+  kModeSymmetricBF16 = 5
+};
 struct GemmPlan {
   int bt;        // token tile (MMA N): 16, 32, 64, 128 or 256
   int split;     // K slices (grid.z)

@@ -52,7 +52,9 @@ typedef enum {
   AWQ_OP_GEMV = 0,
   AWQ_OP_GEMM = 1,
   AWQ_OP_W4A8_GEMM = 2,
-  AWQ_OP_GEMV_PREPACKED = 3
+  AWQ_OP_GEMV_PREPACKED = 3,
+  AWQ_OP_GEMV_BF16 = 4,
+  AWQ_OP_GEMM_BF16 = 5
 } awq_op;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -230,6 +232,37 @@ awq_status awq_gemm(const uint16_t *x, const int32_t *qweight, const int32_t *qz
                     const uint16_t *scales, uint16_t *y, int64_t M, int64_t K, int64_t N,
                     int32_t group_size, int32_t split_k, void *workspace,
                     size_t workspace_bytes, awq_stream_t stream);
+
+/*
+ * bf16 variant of the W4A16 layer.  Many models are trained in bf16 ("Support W4A8 quantization for
+ * vllm": brisker's question on bf16 support and HandH1998's answer that the W4A8 kernel there does not
+ * support it).  These entry points take bf16 activations and scales (raw bf16 bits in uint16_t, the
+ * upper half of an IEEE binary32) and write bf16 outputs; codes and zero points are packed as for the
+ * fp16 entry points.
+ *
+ * awq_dequant_bf16 -- W[k, n] = bf16_RN((q[k, n] - z[k / g, n]) * s[k / g, n]); same arguments and
+ * checks as awq_dequant, bf16 scales and output.  Bit-identical to the correctly rounded product.
+ *
+ * awq_gemv_bf16 -- y = x * W for M <= 16 tokens, bf16 x [M, K], scales, y [M, N].  Every weight is
+ * made exactly as awq_dequant_bf16 makes it and multiplied on the tensor pipe with fp32 accumulation;
+ * the output is rounded once.  Runs the 16-token instance of the decode kernel for every M (its
+ * workspace: awq_workspace_bytes(AWQ_OP_GEMV_BF16, ...)); split_k and the residency assumption as for
+ * awq_gemv.
+ *
+ * awq_gemm_bf16 -- the tensor-core GEMM (tcgen05 kind::f16 with bf16 A and B) for any M >= 1, bf16
+ * x, scales and y; workspace awq_workspace_bytes(AWQ_OP_GEMM_BF16, ...); otherwise as awq_gemm.
+ */
+awq_status awq_dequant_bf16(const int32_t *qweight, const int32_t *qzeros, const uint16_t *scales,
+                            int64_t K, int64_t N, int32_t group_size, uint16_t *w,
+                            awq_stream_t stream);
+awq_status awq_gemv_bf16(const uint16_t *x, const int32_t *qweight, const int32_t *qzeros,
+                         const uint16_t *scales, uint16_t *y, int64_t M, int64_t K, int64_t N,
+                         int32_t group_size, int32_t split_k, void *workspace,
+                         size_t workspace_bytes, awq_stream_t stream);
+awq_status awq_gemm_bf16(const uint16_t *x, const int32_t *qweight, const int32_t *qzeros,
+                         const uint16_t *scales, uint16_t *y, int64_t M, int64_t K, int64_t N,
+                         int32_t group_size, int32_t split_k, void *workspace,
+                         size_t workspace_bytes, awq_stream_t stream);
 
 /*
  * w4a8_quant_act -- per-token dynamic int8 quantization of activations.
