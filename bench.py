@@ -50,8 +50,8 @@ from bit_weight_only_awq_gb300 import synth  # noqa: E402
 
 WORKLOAD_FILTER = {"only": None, "ms": None}
 METRIC = "W4A16 group-quant GEMM TFLOP/s & HBM GB/s vs M; % of roofline on 1 GB300"
-WORKLOADS = ("decode", "decode_awq", "prefill", "crossover", "crossover_sym", "w4a8", "decode_bf16",
-             "prefill_bf16")
+WORKLOADS = ("decode", "decode_awq", "prefill", "crossover", "crossover_sym", "w4a8", "w4a8_grouped",
+             "decode_bf16", "prefill_bf16")
 HEADLINE = "decode"
 L2_BYTES = 126 * 1024 * 1024  # GB300 L2 (the flush writes twice this)
 
@@ -68,6 +68,11 @@ def w4a16_sym_bytes(M, K, N):
 
 def w4a8_bytes(M, K, N):
     return K * N / 2 + 2 * N + M * K + 4 * M + 2 * M * N
+
+
+def w4a8_grouped_bytes(M, K, N):
+    """Per-group W4A8: the per-channel bytes plus the fp16 group factors s3 [K/128, N]."""
+    return w4a8_bytes(M, K, N) + 2 * (K / 128) * N
 
 
 def awq_linear_gemv_max():
@@ -117,12 +122,17 @@ def _workload_calls(workload):
     if workload == "w4a8":
         k, nn = synth.W4A8_SHAPE
         return [("w4a8", "w4a8", m, k, nn) for m in synth.W4A8_M]
+    if workload == "w4a8_grouped":
+        k, nn = synth.W4A8_SHAPE
+        return [("w4a8g", "w4a8_grouped", m, k, nn) for m in synth.W4A8_M]
     raise ValueError(workload)
 
 
 def call_bytes(kind, M, K, N, symmetric=False):
     if kind == "w4a8":
         return w4a8_bytes(M, K, N)
+    if kind == "w4a8g":
+        return w4a8_grouped_bytes(M, K, N)
     return w4a16_sym_bytes(M, K, N) if symmetric else w4a16_bytes(M, K, N)
 
 
@@ -194,6 +204,8 @@ def _oracle_problems(workload, cols, seed):
     for i, (kind, name, M, K, N) in enumerate(workload_calls(workload)):
         if kind == "w4a8":
             problems.append((kind, M, K, synth.w4a8_problem(M, K, cols, seed=seed + i)))
+        elif kind == "w4a8g":
+            problems.append((kind, M, K, synth.w4a8_group_problem(M, K, cols, seed=seed + i)))
         elif is_bf16(workload):
             problems.append((kind, M, K, synth.awq_problem_bf16(M, K, cols, seed=seed + i)))
         else:
@@ -228,6 +240,9 @@ def _oracle_passes(workload, budget_s, seed):
             if kind == "w4a8":
                 xq, s = oracle.quant_act(p["x"])
                 oracle.w4a8_linear(xq, s, p["wq"], p["s_ch"])
+            elif kind == "w4a8g":
+                xq, s = oracle.quant_act(p["x"])
+                oracle.w4a8_group_linear(xq, s, p["wq"], p["s3"], p["s2"], 128)
             elif kind.endswith("_bf16"):
                 oracle.awq_linear_bf16(p["x"], p["qweight"], p["qzeros"], p["scales"], 128)
             else:
@@ -335,6 +350,10 @@ def build_inputs(torch, workload, device, only=None, ms=None):
             p = synth.w4a8_problem(M, K, N, seed=seed)
             b = {"wq": torch.from_numpy(p["wq"]).to(device), "s_ch": torch.from_numpy(p["s_ch"]).to(device)}
             b["s_tok"] = torch.empty((M,), dtype=torch.float32, device=device)
+        elif kind == "w4a8g":
+            p = synth.w4a8_group_problem(M, K, N, seed=seed)
+            b = {k: torch.from_numpy(p[k]).to(device) for k in ("wq", "s3", "s2")}
+            b["s_tok"] = torch.empty((M,), dtype=torch.float32, device=device)
         elif kind.endswith("_bf16"):
             p = synth.awq_problem_bf16(M, K, N, seed=seed)
             b = {k: torch.from_numpy(p[k]).to(device) for k in ("qweight", "qzeros")}
@@ -419,6 +438,9 @@ def issue_step(awq, bufs, stream):
         elif kind == "gemm":
             awq.awq_gemm(b["x"], b["qweight"], b["qzeros"], b["scales"], out=b["y"], stream=stream)
             launches += 1
+        elif kind == "w4a8g":
+            awq.w4a8_linear_grouped(b["x"], b["wq"], b["s3"], b["s2"], out=b["y"], s_tok=b["s_tok"], stream=stream)
+            launches += 2  # quantize (fp16 codes into the workspace), then the tensor-core GEMM
         else:
             awq.w4a8_linear(b["x"], b["wq"], b["s_ch"], out=b["y"], s_tok=b["s_tok"], stream=stream)
             launches += 2  # quantize (fp16 codes into the workspace), then the GEMV or the tensor-core GEMM
@@ -490,7 +512,8 @@ def gpu_workload(args, workload, world, torch, dist, awq, device, flush):
     for b in bufs:
         kind, _, M, K, N = b["meta"]
         op = {"gemv": awq.OP_GEMV, "gemm": awq.OP_GEMM, "w4a8": awq.OP_W4A8_GEMM,
-              "gemv_pp": awq.OP_GEMV_PREPACKED, "gemv_bf16": awq.OP_GEMV_BF16, "gemm_bf16": awq.OP_GEMM_BF16}[kind]
+              "gemv_pp": awq.OP_GEMV_PREPACKED, "gemv_bf16": awq.OP_GEMV_BF16, "gemm_bf16": awq.OP_GEMM_BF16,
+              "w4a8g": awq.OP_W4A8_GROUPED}[kind]
         awq.device_workspace(awq.awq_workspace_bytes(op, M, K, N, 0), device)
     with torch.cuda.stream(stream):
         issue_step(awq, bufs, stream)
@@ -574,6 +597,7 @@ def dominant_kernel(workload):
             "decode_awq": ("awq_gemv (gemv_kernel)", "hbm"), "prefill": ("awq_gemm (gemm_kernel)", "tensor"),
             "crossover": ("awq_gemv + awq_gemm", "hbm"), "crossover_sym": ("awq_gemv + awq_gemm", "hbm"),
             "w4a8": ("w4a8_linear (gemm_kernel<W4A8>)", "tensor"),
+            "w4a8_grouped": ("w4a8_linear_grouped (gemm_kernel<W4A8, group factors>)", "tensor"),
             "decode_bf16": ("awq_gemv_bf16 (gemv_kernel<16, bf16>)", "hbm"),
             "prefill_bf16": ("awq_gemm_bf16 (gemm_kernel<bf16>)", "tensor")}[workload]
 
@@ -640,8 +664,10 @@ def workload_record(workload, r, args, world):
                      "TFLOP/s": round(t, 2), "frac_hbm": round(g / hbm, 4), "frac_tensor": round(t / bf16, 4)})
     config = {"workload": f"{workload}: " + ", ".join(sorted({f'{n} K={k} N={nn}' for _, n, _, k, nn in calls})),
               "M": sorted({c[2] for c in calls}), "group_size": 128,
-              "weights": "symmetric (zero 8, no qzeros)" if sym else ("per-channel int4, u = q + 8" if workload == "w4a8"
-                                                                        else "zero-point (packed qzeros)"),
+              "weights": "symmetric (zero 8, no qzeros)" if sym else (
+                  "per-channel int4, u = q + 8" if workload == "w4a8" else
+                  "int4 u = q + 8 with integer group factors s3 (g=128) and channel scales s2" if workload == "w4a8_grouped"
+                  else "zero-point (packed qzeros)"),
               "activations": "bf16 (bf16 scales and output)" if is_bf16(workload) else "fp16",
               "kernels": sorted({c[0] for c in calls}), "calls_per_step": len(calls),
               "l2": "inputs larger than L2: every call of a step has its own weights "

@@ -24,7 +24,7 @@ lib = ctypes.CDLL(_LIB_PATH)
 
 STATUS = {0: "AWQ_OK", -1: "AWQ_EINVAL", -2: "AWQ_EALIGN", -3: "AWQ_EARCH", -4: "AWQ_ECUDA",
           -5: "AWQ_ETIMEOUT", -6: "AWQ_EWORKSPACE", -7: "AWQ_ENULL"}
-OP_GEMV, OP_GEMM, OP_W4A8_GEMM, OP_GEMV_PREPACKED, OP_GEMV_BF16, OP_GEMM_BF16 = 0, 1, 2, 3, 4, 5
+OP_GEMV, OP_GEMM, OP_W4A8_GEMM, OP_GEMV_PREPACKED, OP_GEMV_BF16, OP_GEMM_BF16, OP_W4A8_GROUPED = 0, 1, 2, 3, 4, 5, 6
 GROUP_SIZE = 128
 
 _p = ctypes.c_void_p
@@ -51,6 +51,8 @@ _SIGS = {
     "awq_prepack_gemv": (_i32, [_p, _p, _p, _i64, _i64, _i32, _p, _sz, _p]),
     "awq_unprepack_gemv": (_i32, [_p, _i64, _i64, _p, _p, _p, _p]),
     "awq_gemv_prepacked": (_i32, [_p, _p, _p, _i64, _i64, _i64, _i32, _p, _sz, _p]),
+    "w4a8_gemm_grouped": (_i32, [_p, _p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _i32, _i32, _p, _sz, _p]),
+    "w4a8_linear_grouped": (_i32, [_p, _p, _p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _i32, _i32, _p, _sz, _p]),
     "awq_last_device_error": (_i32, [ctypes.POINTER(_i32)]),
     "awq_selftest_wait_timeout": (_i32, [_i64, _p]),
 }
@@ -310,6 +312,40 @@ def w4a8_linear(x, wq, s_ch, split_k: int = 0, out=None, acc_out=None, xq_out=No
     nbytes = 0 if ws is None else ws.numel() * ws.element_size()
     _check("w4a8_linear", lib.w4a8_linear(_ptr(x), _ptr(wq), _ptr(s_ch), _ptr(out), _ptr(acc_out), _ptr(xq_out),
                                           _ptr(s_tok), M, K, N, split_k, _ptr(ws), nbytes, _stream(stream)))
+    return out, s_tok
+
+
+def w4a8_gemm_grouped(xq, s_tok, wq, s3, s2, split_k: int = 0, out=None, acc_out=None, workspace=None,
+                      stream=None):
+    """Per-group W4A8 from int8 codes (s3: integer group factors 1..16, s2: channel scales)."""
+    M, K = xq.shape
+    N = wq.shape[1] * 8
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=xq.device)
+    need = awq_workspace_bytes(OP_W4A8_GROUPED, M, K, N, split_k)
+    ws = workspace if workspace is not None else device_workspace(need, xq.device)
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check("w4a8_gemm_grouped", lib.w4a8_gemm_grouped(_ptr(xq), _ptr(s_tok), _ptr(wq), _ptr(s3), _ptr(s2), _ptr(out),
+                                                      _ptr(acc_out), M, K, N, GROUP_SIZE, split_k, _ptr(ws), nbytes,
+                                                      _stream(stream)))
+    return out
+
+
+def w4a8_linear_grouped(x, wq, s3, s2, split_k: int = 0, out=None, acc_out=None, xq_out=None, s_tok=None,
+                        workspace=None, stream=None):
+    """Per-group W4A8 from fp16 activations in one call (quantization included); returns (y, s_tok)."""
+    M, K = x.shape
+    N = wq.shape[1] * 8
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    if s_tok is None:
+        s_tok = torch.empty((M,), dtype=torch.float32, device=x.device)
+    need = awq_workspace_bytes(OP_W4A8_GROUPED, M, K, N, split_k)
+    ws = workspace if workspace is not None else device_workspace(need, x.device)
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check("w4a8_linear_grouped", lib.w4a8_linear_grouped(_ptr(x), _ptr(wq), _ptr(s3), _ptr(s2), _ptr(out),
+                                                          _ptr(acc_out), _ptr(xq_out), _ptr(s_tok), M, K, N,
+                                                          GROUP_SIZE, split_k, _ptr(ws), nbytes, _stream(stream)))
     return out, s_tok
 
 

@@ -163,6 +163,9 @@ size_t awq_workspace_bytes(awq_op op, int64_t M, int64_t K, int64_t N, int32_t s
     case AWQ_OP_GEMM_BF16:
       if (!gemm_shape_ok(M, K, N, split_k) || M == 0) return 0;
       return gemm_workspace_bytes(gemm_plan(M, K, N, split_k, kModeZeroPointBF16), M, K, N, kModeZeroPointBF16);
+    case AWQ_OP_W4A8_GROUPED:
+      if (!gemm_shape_ok(M, K, N, split_k) || M == 0) return 0;
+      return gemm_workspace_bytes(gemm_plan(M, K, N, split_k, kModeW4A8G), M, K, N, kModeW4A8G);
     case AWQ_OP_GEMV_PREPACKED:
       if (!gemv_shape_ok(M, K, N, kGroup, split_k) || M == 0 || M > 8) return 0;
       return gemv_pp_workspace_bytes(gemv_pp_plan(M, K, N, split_k));
@@ -388,6 +391,69 @@ awq_status w4a8_linear(const uint16_t* x, const int32_t* wq, const uint16_t* s_c
     return AWQ_EALIGN;
   auto quantize = [&](uint16_t* x16, cudaStream_t s) { return launch_quant_act(x, xq_out, s_tok, M, K, s, x16); };
   return w4a8_product(quantize, s_tok, wq, s_ch, y, acc_out, M, K, N, split_k, workspace, workspace_bytes, stream);
+}
+
+}  // extern "C"
+
+// The per-group W4A8 product once `fill` has written the fp16 codes of the activations into the workspace:
+// the tensor-core GEMM with 1024-row exact chunks (every token count).
+template <class Fill>
+static awq_status w4a8_grouped_product(Fill fill, const float* s_tok, const int32_t* wq, const uint16_t* s3,
+                                       const uint16_t* s2, uint16_t* y, int32_t* acc_out, int64_t M, int64_t K,
+                                       int64_t N, int32_t split_k, void* workspace, size_t workspace_bytes,
+                                       awq_stream_t stream) {
+  const GemmPlan plan = gemm_plan(M, K, N, split_k, kModeW4A8G);
+  awq_status st = check_workspace(gemm_workspace_bytes(plan, M, K, N, kModeW4A8G), workspace, workspace_bytes);
+  if (st != AWQ_OK) return st;
+  if (plan.split > 1 && (int64_t)plan.n_tiles * plan.m_tiles > kMaxCounters) return AWQ_EINVAL;
+  st = check_arch();
+  if (st != AWQ_OK) return st;
+  int* err = device_error_ptr();
+  if (!err) return AWQ_ECUDA;
+  char* ws = static_cast<char*>(workspace);
+  uint16_t* x16 = reinterpret_cast<uint16_t*>(ws + kCounterBytes);
+  const cudaStream_t s = (cudaStream_t)stream;
+  if (fill(x16, s) != cudaSuccess) return AWQ_ECUDA;
+  void* part = nullptr;
+  int* counters = nullptr;
+  if (plan.split > 1) {
+    counters = reinterpret_cast<int*>(ws);
+    part = ws + kCounterBytes + align256((size_t)M * (size_t)K * 2);
+  }
+  return from_cuda(launch_gemm(kModeW4A8G, x16, reinterpret_cast<const uint32_t*>(wq), nullptr, s3, s_tok, s2, y,
+                               acc_out, M, K, N, plan, part, counters, err, s));
+}
+
+extern "C" {
+
+awq_status w4a8_gemm_grouped(const int8_t* xq, const float* s_tok, const int32_t* wq, const uint16_t* s3,
+                             const uint16_t* s2, uint16_t* y, int32_t* acc_out, int64_t M, int64_t K, int64_t N,
+                             int32_t group_size, int32_t split_k, void* workspace, size_t workspace_bytes,
+                             awq_stream_t stream) {
+  if (!gemm_shape_ok(M, K, N, split_k) || group_size != kGroup) return AWQ_EINVAL;
+  if (M == 0) return AWQ_OK;
+  if (!xq || !s_tok || !wq || !s3 || !s2 || !y) return AWQ_ENULL;
+  if (!aligned16(xq) || !aligned16(wq) || !aligned16(s3) || !aligned16(s2) || !aligned16(y) ||
+      (acc_out && !aligned16(acc_out)))
+    return AWQ_EALIGN;
+  auto widen = [&](uint16_t* x16, cudaStream_t s) { return launch_i8_to_f16(xq, x16, M * K, s); };
+  return w4a8_grouped_product(widen, s_tok, wq, s3, s2, y, acc_out, M, K, N, split_k, workspace, workspace_bytes,
+                              stream);
+}
+
+awq_status w4a8_linear_grouped(const uint16_t* x, const int32_t* wq, const uint16_t* s3, const uint16_t* s2,
+                               uint16_t* y, int32_t* acc_out, int8_t* xq_out, float* s_tok, int64_t M, int64_t K,
+                               int64_t N, int32_t group_size, int32_t split_k, void* workspace,
+                               size_t workspace_bytes, awq_stream_t stream) {
+  if (!gemm_shape_ok(M, K, N, split_k) || group_size != kGroup) return AWQ_EINVAL;
+  if (M == 0) return AWQ_OK;
+  if (!x || !s_tok || !wq || !s3 || !s2 || !y) return AWQ_ENULL;
+  if (!aligned16(x) || !aligned16(wq) || !aligned16(s3) || !aligned16(s2) || !aligned16(y) ||
+      (acc_out && !aligned16(acc_out)) || (xq_out && !aligned16(xq_out)))
+    return AWQ_EALIGN;
+  auto quantize = [&](uint16_t* x16, cudaStream_t s) { return launch_quant_act(x, xq_out, s_tok, M, K, s, x16); };
+  return w4a8_grouped_product(quantize, s_tok, wq, s3, s2, y, acc_out, M, K, N, split_k, workspace, workspace_bytes,
+                              stream);
 }
 
 awq_status awq_last_device_error(int32_t* code) {

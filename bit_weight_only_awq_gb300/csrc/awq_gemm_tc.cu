@@ -56,7 +56,13 @@ __device__ __forceinline__ int dq_rank_solo(int w) { return (w - 3) - ((w + 2) /
 constexpr int kWBlockBytes = kBK * kBN * 2;     // dequantized tile of one M-block, 16 KB
 
 template <int MODE>
-constexpr bool kIsW4A8 = MODE == kModeW4A8 || MODE == kModeW4A8One;
+constexpr bool kIsW4A8 = MODE == kModeW4A8 || MODE == kModeW4A8One || MODE == kModeW4A8G;
+// modes whose k-step stage carries a row of per-(group, column) scales: W4A16 and W4A8 with group factors
+template <int MODE>
+constexpr bool kHasScales = !kIsW4A8<MODE> || MODE == kModeW4A8G;
+// modes with several exact-integer accumulators per K slice (one per chunk of chunk_steps k-steps)
+template <int MODE>
+constexpr bool kChunked = MODE == kModeW4A8 || MODE == kModeW4A8G;
 template <int MODE>
 constexpr bool kIsBF16 = MODE == kModeZeroPointBF16 || MODE == kModeSymmetricBF16;
 template <int MODE>
@@ -86,7 +92,9 @@ struct Cfg {
   static constexpr int kFit = (227 * 1024 - 1024 - kFixed) / kXSlotBytes;
   static constexpr int kXStages = kFit > 16 ? 16 : kFit;   // slots
   static constexpr int kSmem = kXStages * kXSlotBytes + kFixed + 1024;
-  static constexpr int kAccs = MODE == kModeW4A8 ? 2 : 1;  // W4A8: one accumulator per exact K chunk (two)
+  // W4A8: one accumulator per exact K chunk (two of 16384 rows); with group factors as many 1024-row
+  // chunks as tensor memory holds (512 columns)
+  static constexpr int kAccs = MODE == kModeW4A8 ? 2 : MODE == kModeW4A8G ? 512 / (NB * BT) : 1;
   static constexpr int kTmemCols = NB * kAccs * BT < 32 ? 32 : NB * kAccs * BT;
   // Warps: 0 copies activations, 1 issues the mmas (one thread), 2 copies packed weights, 16 dequantize.
   // With tiles of at most 64 tokens the mmas are short and their issue rate limits the k-step, so
@@ -242,7 +250,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
       const int S = is_x ? SX : kQStages;
       const uint32_t tx = is_x ? (uint32_t)C::kXSlotBytes
                                : (uint32_t)(kQBytes + (kHasZeros<MODE> ? C::kZBytes : 0) +
-                                            (!kIsW4A8<MODE> ? C::kSBytes : 0));
+                                            (kHasScales<MODE> ? C::kSBytes : 0));
       const int units = is_x ? nsteps * C::kXSub : nsteps;  // x: (k-step, 32-k half) slots
       int issued = 0;
       for (int j = 0; j < units; ++j, ++issued) {
@@ -259,7 +267,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
           mbar_arrive_tx(fullq(st), tx);
           tma_load_2d(smem_u32(qb), &tm_q, n0 / 8, kb, fullq(st));
           if (kHasZeros<MODE>) tma_load_2d(smem_u32(qb + kQBytes), &tm_z, n0 / 8, grp, fullq(st));
-          if (!kIsW4A8<MODE>) tma_load_2d(smem_u32(qb + kQBytes + 128), &tm_s, n0, grp, fullq(st));
+          if (kHasScales<MODE>) tma_load_2d(smem_u32(qb + kQBytes + 128), &tm_s, n0, grp, fullq(st));
         }
       }
       // never leave the CTA with copies in flight
@@ -312,7 +320,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
           wph ^= 1u;
         }
         ++within;  // k-steps accumulated into the current chunk (W4A16: one chunk)
-        if (MODE == kModeW4A8 && within == chunk_steps) {
+        if (kChunked<MODE> && within == chunk_steps) {
           within = 0;
           ++chunk;
         }
@@ -344,7 +352,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
       const uint32_t* qw = reinterpret_cast<const uint32_t*>(qb);
       uint8_t* wt = wring + ws * kWBytes;
       uint32_t zp[4], sp[4];
-      if (!kIsW4A8<MODE>) {
+      if (kHasScales<MODE>) {
         const uint32_t zword = kHasZeros<MODE> ? reinterpret_cast<const uint32_t*>(qb + kQBytes)[c]
                                                : 0x88888888u;
         const uint4 sv = reinterpret_cast<const uint4*>(qb + kQBytes + 128)[c];
@@ -367,8 +375,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             o[j] = bmul2(bsub2(pair_magic_bf16(words[jr], j), zp[j]), sp[j]);
           } else {
             const uint32_t h = pair_magic(words[jr], j);
-            o[j] = kIsW4A8<MODE> ? hsub2(h, 0x64086408u) /* u - 8, exact */
-                                 : hmul2(hsub2(h, zp[j]), sp[j]);
+            if constexpr (MODE == kModeW4A8G) o[j] = hmul2(hsub2(h, 0x64086408u), sp[j]);  // (u - 8) s3, exact
+            else o[j] = kIsW4A8<MODE> ? hsub2(h, 0x64086408u) /* u - 8, exact */
+                                      : hmul2(hsub2(h, zp[j]), sp[j]);
           }
         }
         const uint32_t off =
@@ -409,9 +418,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         if (kIsW4A8<MODE>) {
 #pragma unroll
           for (int j = 0; j < 8; ++j) vi[j] = __float2int_rn(v[j]);  // exact integers
-          if (MODE == kModeW4A8 && nsteps > chunk_steps) {
+          // the other chunks' accumulators, each an exact integer, added as int32
+          for (int ch = 1; kChunked<MODE> && ch < C::kAccs && ch * chunk_steps < nsteps; ++ch) {
             float v2[8];
-            tmem_ld8(tmem + ((uint32_t)(lq * 32) << 16) + dcol + (uint32_t)(NB * BT + cb), v2);
+            tmem_ld8(tmem + ((uint32_t)(lq * 32) << 16) + dcol + (uint32_t)(ch * NB * BT + cb), v2);
 #pragma unroll
             for (int j = 0; j < 8; ++j) vi[j] += __float2int_rn(v2[j]);
           }
@@ -518,7 +528,7 @@ cudaError_t launch_t(const uint16_t* x16, const uint32_t* qw, const uint32_t* qz
   // zero-point and scale maps: dummies (the weight map) when the mode does not read them
   ok = ok && make_map_2d(&tz, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, qz ? (const void*)qz : (const void*)qw, nw,
                          qz ? ng : (uint64_t)K, kQWords, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
-  ok = ok && (kIsW4A8<MODE>
+  ok = ok && (!kHasScales<MODE>
                   ? make_map_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, qw, nw, (uint64_t)K, kQWords, 1,
                                 CU_TENSOR_MAP_SWIZZLE_NONE)
                   : make_map_2d(&ts, kHalfType, 2, sc, (uint64_t)N, ng, NB * kBN, 1,
@@ -530,7 +540,8 @@ cudaError_t launch_t(const uint16_t* x16, const uint32_t* qw, const uint32_t* qz
   dim3 grid(p.n_tiles, p.m_tiles, p.split);
   kern<<<grid, C::kThreads, C::kSmem, s>>>(tx, tq, tz, ts, reinterpret_cast<__half*>(y), acc_out, s_tok,
                                        reinterpret_cast<const __half*>(s_ch), part, counters, err, (int)M,
-                                       (int)N, (int)K, p.ksteps, kW4A8MaxKSlice / kBK);
+                                       (int)N, (int)K, p.ksteps,
+                                       (MODE == kModeW4A8G ? kW4A8GroupChunk : kW4A8MaxKSlice) / kBK);
   return cudaGetLastError();
 }
 
@@ -550,6 +561,15 @@ cudaError_t launch_mode(const uint16_t* x16, const uint32_t* qw, const uint32_t*
     }
   }
   if (p.nb != 1) return cudaErrorInvalidValue;
+  if constexpr (MODE == kModeW4A8G) {  // token tiles of at most 64: 8 to 32 chunk accumulators
+    if ((int64_t)p.ksteps * kBK > (int64_t)(512 / p.bt) * kW4A8GroupChunk) return cudaErrorInvalidValue;
+    switch (p.bt) {
+      case 16: return launch_t<16, 1, MODE>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters, err, s);
+      case 32: return launch_t<32, 1, MODE>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters, err, s);
+      case 64: return launch_t<64, 1, MODE>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters, err, s);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (p.bt) {
     case 16: return launch_t<16, 1, MODE>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters, err, s);
     case 32: return launch_t<32, 1, MODE>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters, err, s);
@@ -588,11 +608,12 @@ GemmPlan gemm_plan(int64_t M, int64_t K, int64_t N, int split_k, int mode) {
   p.nb = 1;
   p.bt = bt0;
   while (p.bt > 64 && tiles(p.bt, 1) < 114) p.bt /= 2;
+  if (mode == kModeW4A8G && p.bt > 64) p.bt = 64;  // 512 / 64 = 8 exact chunks of 1024 rows per K slice
   // >= 128-token tiles: 256 weight columns per CTA (two M-blocks on one activation tile) whenever that
   // still fills about a wave.  W4A8 then has one exact accumulator per M-block, which holds K slices of
   // at most 16384 rows: taken only when K fits one slice (at K = 21760 and 4096 tokens, two M-blocks
   // with a K split of two measured 1375 us against 1150 us for one M-block with two accumulators)
-  if (bt0 >= 128 && (mode != kModeW4A8 || K <= kW4A8MaxKSlice)) {
+  if (bt0 >= 128 && mode != kModeW4A8G && (mode != kModeW4A8 || K <= kW4A8MaxKSlice)) {
     int bt = bt0;
     while (bt > 128 && tiles(bt, 2) < 114) bt /= 2;
     // under a wave, a K split with slices of at least 32 k-steps may fill it (M = 256, K = 14336,
@@ -612,10 +633,12 @@ GemmPlan gemm_plan(int64_t M, int64_t K, int64_t N, int split_k, int mode) {
   // fill the 152 SMs: largest split (<= 8, >= 8 k-steps per slice) whose CTA count stays <= one wave,
   // if the unsplit grid is under one wave
   int split = split_k > 0 ? split_k : fill_split((int64_t)p.n_tiles * p.m_tiles, total, 8);
-  if (mode == kModeW4A8) {
+  if (mode == kModeW4A8 || mode == kModeW4A8G) {
     // exact accumulators: each K slice spans at most 2 x 16384 rows with one M-block (two
-    // accumulators), at most 16384 with two M-blocks (one each)
-    const int64_t slice = p.nb == 2 ? kW4A8MaxKSlice : 2 * kW4A8MaxKSlice;
+    // accumulators), at most 16384 with two M-blocks (one each); with group factors 512 / bt chunks of
+    // 1024 rows
+    const int64_t slice = mode == kModeW4A8G ? (int64_t)(512 / p.bt) * kW4A8GroupChunk
+                                             : (p.nb == 2 ? kW4A8MaxKSlice : 2 * kW4A8MaxKSlice);
     const int min_split = (int)((K + slice - 1) / slice);
     if (split < min_split) split = min_split;
   }
@@ -628,7 +651,7 @@ GemmPlan gemm_plan(int64_t M, int64_t K, int64_t N, int split_k, int mode) {
 
 // Workspace: [tile counters, kCounterBytes] [W4A8: fp16 copy of the codes] [split partials]
 size_t gemm_workspace_bytes(const GemmPlan& p, int64_t M, int64_t K, int64_t N, int mode) {
-  const size_t x16 = mode == kModeW4A8 ? align256((size_t)M * (size_t)K * 2) : 0;
+  const size_t x16 = (mode == kModeW4A8 || mode == kModeW4A8G) ? align256((size_t)M * (size_t)K * 2) : 0;
   const size_t part = p.split > 1 ? align256((size_t)p.split * (size_t)M * (size_t)N * 4) : 0;
   if (x16 == 0 && part == 0) return 0;
   return kCounterBytes + x16 + part;
@@ -645,6 +668,8 @@ cudaError_t launch_gemm(int mode, const uint16_t* x16, const uint32_t* qw, const
       return launch_mode<kModeSymmetric>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters, err, s);
     case kModeW4A8:
       return launch_mode<kModeW4A8>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters, err, s);
+    case kModeW4A8G:
+      return launch_mode<kModeW4A8G>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters, err, s);
     case kModeZeroPointBF16:
       return launch_mode<kModeZeroPointBF16>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters,
                                              err, s);

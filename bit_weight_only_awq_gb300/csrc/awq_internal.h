@@ -100,8 +100,12 @@ enum GemmMode {
   kModeW4A8 = 2,
   kModeW4A8One = 3,
   kModeZeroPointBF16 = 4,
-  kModeSymmetricBF16 = 5
+  kModeSymmetricBF16 = 5,
+  kModeW4A8G = 6  // W4A8 with per-group integer weight factors s3: weights (u - 8) * s3
 };
+// W4A8 with per-group factors: |code| <= 128 times |weight| <= 128, so an fp32 sum stays an exact integer
+// over 1024 rows (2^24); each tensor-memory accumulator holds one such chunk.
+constexpr int kW4A8GroupChunk = 1024;
 struct GemmPlan {
   int bt;        // token tile (MMA N): 16, 32, 64, 128 or 256
   int split;     // K slices (grid.z)

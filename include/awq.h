@@ -54,7 +54,8 @@ typedef enum {
   AWQ_OP_W4A8_GEMM = 2,
   AWQ_OP_GEMV_PREPACKED = 3,
   AWQ_OP_GEMV_BF16 = 4,
-  AWQ_OP_GEMM_BF16 = 5
+  AWQ_OP_GEMM_BF16 = 5,
+  AWQ_OP_W4A8_GROUPED = 6
 } awq_op;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -329,6 +330,39 @@ awq_status w4a8_linear(const uint16_t *x, const int32_t *wq, const uint16_t *s_c
                        int32_t *acc_out, int8_t *xq_out, float *s_tok, int64_t M, int64_t K,
                        int64_t N, int32_t split_k, void *workspace, size_t workspace_bytes,
                        awq_stream_t stream);
+
+/*
+ * W4A8 with per-group weight factors.  The per-channel W4A8 kernel widens an int4 weight to int8 by a
+ * shift of 4 and applies the channel scale to the output; per-group weight quantization needs a group
+ * scale as well as the channel scale, and the reduction stays on int32 ("Support W4A8 quantization for
+ * vllm": HandH1998 on FragS_GROUP and FragS_CHANNEL, on dequant_per_channel as a shift of 4 bits, alexm
+ * on the int32 global reduce; marlin_qqq_gemm(a, b_q_weight, s1, s2, s3, ...)).  Reading of the group
+ * scale: s3 [K/128, N] holds integers in [1, 16] (fp16 storage), the per-group factor that turns the
+ * int4 weight into an int8 one; s3 = 16 everywhere is the per-channel kernel.
+ *   acc[m, n] = sum_k xq[m, k] * ((u[k, n] - 8) * s3[k / 128, n])   (exact, int32)
+ *   y[m, n]   = fp16_RN((fp32(acc) * s_tok[m]) * fp32(s2[n]))
+ * Factors outside the integers 1..16 give unspecified (but memory-safe) results.
+ *
+ * w4a8_gemm_grouped -- from int8 codes: xq int8 [M, K], s_tok fp32 [M], wq int32 [K, N/8] (AWQ-packed
+ * u = q + 8), s3 fp16 [K/128, N], s2 fp16 [N], y fp16 [M, N], acc_out int32 [M, N] (optional).  Runs the
+ * tensor-core GEMM for every M: weights (u - 8) * s3 made exactly in fp16, codes widened to fp16 in the
+ * workspace, each 1024 rows in their own fp32 tensor-memory accumulator (an exact integer: |code| <= 128,
+ * |weight| <= 128), token tiles of at most 64, K beyond one slice of 512 / tile * 1024 rows reduced across
+ * CTAs in int32.  K % 128 == 0, N % 32 == 0, group_size == 128.  Workspace:
+ * awq_workspace_bytes(AWQ_OP_W4A8_GROUPED, ...).
+ *
+ * w4a8_linear_grouped -- the same from fp16 activations, quantized per token as w4a8_quant_act does
+ * (s_tok fp32 [M] output, required; xq_out int8 [M, K] optional), one call.
+ */
+awq_status w4a8_gemm_grouped(const int8_t *xq, const float *s_tok, const int32_t *wq,
+                             const uint16_t *s3, const uint16_t *s2, uint16_t *y, int32_t *acc_out,
+                             int64_t M, int64_t K, int64_t N, int32_t group_size, int32_t split_k,
+                             void *workspace, size_t workspace_bytes, awq_stream_t stream);
+awq_status w4a8_linear_grouped(const uint16_t *x, const int32_t *wq, const uint16_t *s3,
+                               const uint16_t *s2, uint16_t *y, int32_t *acc_out, int8_t *xq_out,
+                               float *s_tok, int64_t M, int64_t K, int64_t N, int32_t group_size,
+                               int32_t split_k, void *workspace, size_t workspace_bytes,
+                               awq_stream_t stream);
 
 /*
  * awq_last_device_error -- reads and clears the device-side error word of the

@@ -114,3 +114,10 @@ def test_workload_record_from_fabricated_timings():
     flops = sum(2.0 * M * K * N for _, _, M, K, N in pcalls)
     assert rec2["unit"] == "TFLOP/s" and rec2["value"] == pytest.approx(flops / 0.2e-3 / 1e12, rel=1e-4)
     assert rec2["roofline"]["bound"] == "tensor" and "frac_of_burst" in rec2["roofline"]
+
+
+def test_w4a8_grouped_workload_and_bytes():
+    calls = bench.workload_calls("w4a8_grouped")
+    assert [c[2] for c in calls] == [1, 16, 64, 256, 1024, 4096] and {c[0] for c in calls} == {"w4a8g"}
+    # the per-channel bytes plus fp16 group factors: 2 * 170 groups * 8192 columns
+    assert bench.call_bytes("w4a8g", 1, 21760, 8192) == bench.w4a8_bytes(1, 21760, 8192) + 2 * 170 * 8192

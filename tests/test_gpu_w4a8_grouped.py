@@ -1,0 +1,117 @@
+"""GPU parity of W4A8 with per-group weight factors (through the C ABI) against the CPU oracle.
+
+acc[m, n] = sum_k xq[m, k] (u[k, n] - 8) s3[k / 128, n] is an exact integer and y =
+fp16((fp32(acc) s_tok[m]) s2[n]): both are compared bit for bit (the oracle's
+w4a8_group_linear), on small ragged shapes spanning several 1024-row chunks and K slices, on
+the W4A8 configuration's shape with sampled columns, and on extreme codes where every chunk's
+sum reaches 2^24.
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+from bit_weight_only_awq_gb300 import synth
+from tests.test_gpu_parity import sample_word_cols
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def awq():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from bit_weight_only_awq_gb300 import build as awq_build
+    awq_build.build()
+    from bit_weight_only_awq_gb300 import awq as mod
+    return mod
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def host(t):
+    torch.cuda.synchronize()
+    return t.cpu().numpy()
+
+
+def run(awq, p, split_k=0, xq=None):
+    """The library's quantization + grouped product; returns (xq, s_tok, y, acc)."""
+    M, K = p["x"].shape
+    N = p["wq"].shape[1] * 8
+    if xq is None:
+        xq_t, s_t = awq.w4a8_quant_act(dev(p["x"]))
+    else:
+        xq_t, s_t = dev(xq), dev(np.ones(M, np.float32))
+    acc = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    y = awq.w4a8_gemm_grouped(xq_t, s_t, dev(p["wq"]), dev(p["s3"]), dev(p["s2"]), split_k=split_k, acc_out=acc)
+    return host(xq_t), host(s_t), host(y), host(acc)
+
+
+@pytest.mark.parametrize("split_k", [1, 2, 0])
+@pytest.mark.parametrize("M", [1, 5, 16, 40, 64, 100])
+def test_w4a8_grouped_small_bitexact(awq, M, split_k):
+    # K = 2560: 20 groups, 2.5 chunks of 1024 rows; N = 288: a ragged last 128-column tile
+    p = synth.w4a8_group_problem(M, 2560, 288, seed=9000 + M + 10 * split_k)
+    xq, s, y, acc = run(awq, p, split_k)
+    want_y, want_acc = oracle.w4a8_group_linear(xq, s, p["wq"], p["s3"], p["s2"], 128)
+    assert np.array_equal(acc, want_acc)
+    assert np.array_equal(y.view(np.uint16), want_y.view(np.uint16))
+
+
+@pytest.mark.parametrize("M", [1, 16, 64, 256, 1000])
+def test_w4a8_grouped_config_shape_sampled(awq, M):
+    K, N = synth.W4A8_SHAPE
+    p = synth.w4a8_group_problem(M, K, N, seed=9100 + M)
+    xq, s, y, acc = run(awq, p)
+    wc = sample_word_cols(N // 8, seed=M + 9, count=6)
+    cols = (8 * wc[:, None] + np.arange(8)[None, :]).ravel()
+    want_y, want_acc = oracle.w4a8_group_linear(xq, s, p["wq"][:, wc], p["s3"][:, cols], p["s2"][cols], 128)
+    assert np.array_equal(acc[:, cols], want_acc)
+    assert np.array_equal(y[:, cols].view(np.uint16), want_y.view(np.uint16))
+
+
+@pytest.mark.parametrize("split_k", [0, 1])
+def test_w4a8_grouped_extreme_chunks(awq, split_k):
+    # codes -128 against weights (0 - 8) * 16 = -128: every product is 2^14 and every 1024-row chunk sums
+    # to exactly 2^24; across K = 21760 the accumulator reaches 356 million (int32, exact)
+    M, K, N = 2, 21760, 256
+    xq = np.full((M, K), -128, dtype=np.int8)
+    xq[1, 1::2] = 127
+    wq = np.zeros((K, N // 8), dtype=np.int32)            # every nibble 0: u - 8 = -8
+    p = {"x": np.zeros((M, K), np.float16), "wq": wq, "s3": np.full((K // 128, N), 16, np.float16),
+         "s2": np.full(N, 1e-6, np.float16)}
+    _, s, y, acc = run(awq, p, split_k, xq=xq)
+    want_y, want_acc = oracle.w4a8_group_linear(xq, s, wq, p["s3"], p["s2"], 128)
+    assert want_acc[0, 0] == K * 16384
+    assert np.array_equal(acc, want_acc)
+    assert np.array_equal(y.view(np.uint16), want_y.view(np.uint16))
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 21760, 8192), (300, 4096, 1024)])
+def test_w4a8_linear_grouped_matches_two_calls(awq, M, K, N):
+    p = synth.w4a8_group_problem(M, K, N, seed=9200 + M)
+    xq, s, y2, acc2 = run(awq, p)
+    acc = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    xq_out = torch.empty((M, K), dtype=torch.int8, device="cuda")
+    y, s_tok = awq.w4a8_linear_grouped(dev(p["x"]), dev(p["wq"]), dev(p["s3"]), dev(p["s2"]), acc_out=acc,
+                                       xq_out=xq_out)
+    assert np.array_equal(host(xq_out), xq)
+    assert np.array_equal(host(s_tok).view(np.uint32), s.view(np.uint32))
+    assert np.array_equal(host(acc), acc2)
+    assert np.array_equal(host(y).view(np.uint16), y2.view(np.uint16))
+
+
+def test_w4a8_grouped_factor_16_is_the_per_channel_kernel(awq):
+    # s3 = 16 everywhere with s2 = s_ch / 16 (exact) gives the per-channel kernel's outputs bit for bit
+    M, K, N = 40, 4096, 512
+    p = synth.w4a8_problem(M, K, N, seed=9300)
+    xq_t, s_t = awq.w4a8_quant_act(dev(p["x"]))
+    y_c = awq.w4a8_gemm(xq_t, s_t, dev(p["wq"]), dev(p["s_ch"]))
+    s3 = np.full((K // 128, N), 16, np.float16)
+    s2 = (p["s_ch"].astype(np.float32) / 16).astype(np.float16)
+    y_g = awq.w4a8_gemm_grouped(xq_t, s_t, dev(p["wq"]), dev(s3), dev(s2))
+    assert np.array_equal(host(y_g).view(np.uint16), host(y_c).view(np.uint16))
+    assert awq.awq_last_device_error() == 0
