@@ -311,11 +311,13 @@ def oracle_rate_in_unit(v_bytes, unit, calls, symmetric=False):
     return v_bytes * fb / 1e12
 
 
-def cpu_baseline(workload, budget_s, unit):
+def cpu_baseline(workload, budget_s, unit, all_cores_too=True):
     calls = workload_calls(workload)
     sym = is_symmetric(workload)
     out = {}
     for label, all_cores in (("one_core", False), ("all_cores", True)):
+        if all_cores and not all_cores_too:
+            continue
         try:
             v, desc, cores = run_oracle_subprocess(workload, budget_s, all_cores=all_cores)
             out[label] = {"value": oracle_rate_in_unit(v, unit, calls, sym), "unit": unit, "cores": cores,
@@ -323,7 +325,8 @@ def cpu_baseline(workload, budget_s, unit):
         except Exception as exc:  # the baseline is reported, never required
             out[label] = {"value": None, "unit": unit, "cores": 0, "kind": "oracle", "sample": f"failed: {exc}"[:200]}
     rec = dict(out["one_core"])
-    rec["all_cores"] = out["all_cores"]
+    if "all_cores" in out:
+        rec["all_cores"] = out["all_cores"]
     rec["nproc"] = host_cores()
     return rec
 
@@ -341,32 +344,34 @@ def load_peaks():
 def build_inputs(torch, workload, device, only=None, ms=None):
     """Per-call device buffers (weights distinct per call).  The activations and outputs of all calls
     are views into one device buffer each, mirrored by one pinned host buffer each, so that the e2e
-    step moves them with one host-to-device and one device-to-host copy."""
+    step moves them with one host-to-device and one device-to-host copy.
+
+    Weights, zero points and scales come from the seeded generators of `synth`; the activations,
+    N(0, 1) rounded to the layer's 16-bit format, are drawn on the device from a CUDA generator seeded
+    per workload (the host-side normal generator takes tens of seconds for the prefill sweeps)."""
     sym = is_symmetric(workload)
     bufs = []
     for i, (kind, name, M, K, N) in enumerate(workload_calls(workload, only, ms)):
         seed = 10_000 + i
         if kind == "w4a8":
-            p = synth.w4a8_problem(M, K, N, seed=seed)
+            p = synth.w4a8_problem(M, K, N, seed=seed, with_x=False)
             b = {"wq": torch.from_numpy(p["wq"]).to(device), "s_ch": torch.from_numpy(p["s_ch"]).to(device)}
             b["s_tok"] = torch.empty((M,), dtype=torch.float32, device=device)
         elif kind == "w4a8g":
-            p = synth.w4a8_group_problem(M, K, N, seed=seed)
+            p = synth.w4a8_group_problem(M, K, N, seed=seed, with_x=False)
             b = {k: torch.from_numpy(p[k]).to(device) for k in ("wq", "s3", "s2")}
             b["s_tok"] = torch.empty((M,), dtype=torch.float32, device=device)
         elif kind.endswith("_bf16"):
-            p = synth.awq_problem_bf16(M, K, N, seed=seed)
+            p = synth.awq_problem_bf16(M, K, N, seed=seed, with_x=False)
             b = {k: torch.from_numpy(p[k]).to(device) for k in ("qweight", "qzeros")}
             b["scales"] = torch.from_numpy(p["scales"].view(np.int16)).to(device).view(torch.bfloat16)
-            p["x"] = p["x"].view(np.int16)
         else:
-            p = synth.awq_problem(M, K, N, seed=seed, symmetric=sym)
+            p = synth.awq_problem(M, K, N, seed=seed, symmetric=sym, with_x=False)
             b = {k: (None if p[k] is None else torch.from_numpy(p[k]).to(device))
                  for k in ("qweight", "qzeros", "scales")}
             if kind == "gemv_pp":  # prepared once, as at model load; the AWQ words are not kept
                 b["pp"] = awq_module().awq_prepack_gemv(b["qweight"], b["qzeros"], b["scales"])
                 b.update(qweight=None, qzeros=None, scales=None)
-        b["x_np"] = p["x"]
         b["meta"] = (kind, name, M, K, N)
         bufs.append(b)
     # every view starts on a 16-byte boundary: M * K and M * N are multiples of 8 halves
@@ -377,15 +382,14 @@ def build_inputs(torch, workload, device, only=None, ms=None):
               "x_host": torch.empty(nx, dtype=dt).pin_memory(),
               "y": torch.empty(ny, dtype=dt, device=device),
               "y_host": torch.empty(ny, dtype=dt).pin_memory()}
+    gen = torch.Generator(device=device)
+    gen.manual_seed(20_000 + WORKLOADS.index(workload))
+    packed["x"].copy_(torch.randn(nx, generator=gen, device=device, dtype=torch.float32))
+    packed["x_host"].copy_(packed["x"])
     ox = oy = 0
     for b in bufs:
         _, _, M, K, N = b["meta"]
-        xh = torch.from_numpy(b.pop("x_np")).reshape(-1)
-        if dt == torch.bfloat16:
-            xh = xh.view(torch.bfloat16)
-        packed["x_host"][ox:ox + M * K].copy_(xh)
         b["x"] = packed["x"][ox:ox + M * K].view(M, K)
-        b["x"].copy_(xh.view(M, K))
         b["y"] = packed["y"][oy:oy + M * N].view(M, N)
         ox += M * K
         oy += M * N
@@ -698,7 +702,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="all", choices=("all",) + WORKLOADS)
     ap.add_argument("--min-seconds", type=float, default=1.0, help="device time each workload is timed for")
-    ap.add_argument("--per-m-reps", type=int, default=30, help="L2-flushed replays per token count")
+    ap.add_argument("--per-m-reps", type=int, default=15, help="L2-flushed replays per token count")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work per CPU-baseline run")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default=None, help="comma-separated shape names to keep (profiling small cases)")
@@ -753,9 +757,12 @@ def main():
         r = gpu_workload(args, w, world, torch, dist, awq, device, flush)
         records[w] = workload_record(w, r, args, world)
     if rank == 0 and not args.no_cpu_baseline:
+        # one core and all host cores for the headline and the prefill sweep (the two halves of the metric);
+        # one core for the other sweeps, on a shorter sample
         for i, w in enumerate([head] + others):
             budget = args.cpu_budget if i == 0 else max(1.0, args.cpu_budget / 4)
-            records[w]["cpu_baseline"] = cpu_baseline(w, budget, records[w]["unit"])
+            records[w]["cpu_baseline"] = cpu_baseline(w, budget, records[w]["unit"],
+                                                      all_cores_too=w in (head, "prefill"))
 
     if rank == 0:
         top = records[head]

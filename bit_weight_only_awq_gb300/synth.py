@@ -14,7 +14,8 @@ pages benchmark but which are not available here):
   32-bit integers directly.
 * scales fp16, uniform on [0.002, 0.02] (W4A16) or [0.001, 0.01] (W4A8
   per-channel), rounded to fp16.
-* activations fp16, standard normal, rounded to fp16.
+* activations fp16, standard normal, rounded to fp16 (``with_x=False`` leaves them out, for a caller
+  that draws them itself).
 """
 
 from __future__ import annotations
@@ -60,8 +61,8 @@ def rng_for(seed: int) -> np.random.Generator:
 
 
 def random_words(rng: np.random.Generator, rows: int, cols: int) -> np.ndarray:
-    """Uniform 32-bit words viewed as int32 (eight independent uniform nibbles each)."""
-    return rng.integers(0, 2 ** 32, size=(rows, cols), dtype=np.uint64).astype(np.uint32).view(np.int32)
+    """Uniform 32-bit words viewed as int32 (eight independent uniform nibbles each), from random bytes."""
+    return np.frombuffer(rng.bytes(rows * cols * 4), dtype=np.int32).reshape(rows, cols).copy()
 
 
 def random_codes(rows: int, cols: int, seed: int, high: int = 16) -> np.ndarray:
@@ -74,7 +75,7 @@ def activations(rng: np.random.Generator, m: int, k: int) -> np.ndarray:
 
 
 def awq_problem(m: int, k: int, n: int, seed: int, group_size: int = GROUP_SIZE,
-                symmetric: bool = False) -> dict:
+                symmetric: bool = False, with_x: bool = True) -> dict:
     """Inputs of one W4A16 AWQ linear call.
 
     Returns a dict with ``x`` fp16 [M, K], ``qweight`` int32 [K, N/8],
@@ -86,19 +87,19 @@ def awq_problem(m: int, k: int, n: int, seed: int, group_size: int = GROUP_SIZE,
     qweight = random_words(rng, k, n // 8)
     qzeros = None if symmetric else random_words(rng, k // group_size, n // 8)
     scales = rng.uniform(0.002, 0.02, size=(k // group_size, n)).astype(np.float16)
-    x = activations(rng, m, k)
+    x = activations(rng, m, k) if with_x else None
     return {"x": x, "qweight": qweight, "qzeros": qzeros, "scales": scales,
             "group_size": group_size}
 
 
-def w4a8_problem(m: int, k: int, n: int, seed: int) -> dict:
+def w4a8_problem(m: int, k: int, n: int, seed: int, with_x: bool = True) -> dict:
     """Inputs of one W4A8 call: fp16 activations, packed u = q + 8 weights, fp16 channel scales."""
     if n % 8:
         raise ValueError("N must be a multiple of 8")
     rng = rng_for(seed)
     wq = random_words(rng, k, n // 8)
     s_ch = rng.uniform(0.001, 0.01, size=(n,)).astype(np.float16)
-    x = activations(rng, m, k)
+    x = activations(rng, m, k) if with_x else None
     return {"x": x, "wq": wq, "s_ch": s_ch}
 
 
@@ -112,7 +113,7 @@ def to_bf16_bits(a: np.ndarray) -> np.ndarray:
 
 
 def awq_problem_bf16(m: int, k: int, n: int, seed: int, group_size: int = GROUP_SIZE,
-                     symmetric: bool = False) -> dict:
+                     symmetric: bool = False, with_x: bool = True) -> dict:
     """Inputs of one bf16 W4A16 AWQ linear call: the W4A16 recipe with bf16 activations
     (N(0, 1)) and bf16 scales (U[0.002, 0.02]), both as uint16 bit patterns."""
     if n % 8 or k % group_size:
@@ -121,11 +122,12 @@ def awq_problem_bf16(m: int, k: int, n: int, seed: int, group_size: int = GROUP_
     qweight = random_words(rng, k, n // 8)
     qzeros = None if symmetric else random_words(rng, k // group_size, n // 8)
     scales = to_bf16_bits(rng.uniform(0.002, 0.02, size=(k // group_size, n)))
-    x = to_bf16_bits(rng.standard_normal((m, k), dtype=np.float32))
+    x = to_bf16_bits(rng.standard_normal((m, k), dtype=np.float32)) if with_x else None
     return {"x": x, "qweight": qweight, "qzeros": qzeros, "scales": scales, "group_size": group_size}
 
 
-def w4a8_group_problem(m: int, k: int, n: int, seed: int, group_size: int = GROUP_SIZE) -> dict:
+def w4a8_group_problem(m: int, k: int, n: int, seed: int, group_size: int = GROUP_SIZE,
+                       with_x: bool = True) -> dict:
     """Inputs of one per-group W4A8 call: fp16 activations, packed u = q + 8 weights, integer group
     factors s3 uniform on 1..16 (fp16 [K/g, N]) and fp16 channel scales s2 uniform on [1e-4, 1e-3]."""
     if n % 8 or k % group_size:
@@ -134,5 +136,5 @@ def w4a8_group_problem(m: int, k: int, n: int, seed: int, group_size: int = GROU
     wq = random_words(rng, k, n // 8)
     s3 = rng.integers(1, 17, size=(k // group_size, n)).astype(np.float16)
     s2 = rng.uniform(0.0001, 0.001, size=(n,)).astype(np.float16)
-    x = activations(rng, m, k)
+    x = activations(rng, m, k) if with_x else None
     return {"x": x, "wq": wq, "s3": s3, "s2": s2, "group_size": group_size}
