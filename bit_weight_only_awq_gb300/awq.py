@@ -36,6 +36,8 @@ _SIGS = {
     "awq_status_string": (ctypes.c_char_p, [_i32]),
     "awq_pack": (_i32, [_p, _i64, _i64, _p, _p]),
     "awq_unpack": (_i32, [_p, _i64, _i64, _p, _p]),
+    "awq_pack_order": (_i32, [_p, _i64, _i64, _i32, _p, _p]),
+    "awq_unpack_order": (_i32, [_p, _i64, _i64, _i32, _p, _p]),
     "awq_dequant": (_i32, [_p, _p, _p, _i64, _i64, _i32, _p, _p]),
     "awq_workspace_bytes": (_sz, [_i32, _i64, _i64, _i64, _i32]),
     "awq_gemv": (_i32, [_p, _p, _p, _p, _p, _i64, _i64, _i64, _i32, _i32, _p, _sz, _p]),
@@ -137,6 +139,25 @@ def awq_unpack(packed: torch.Tensor, out: torch.Tensor | None = None, stream=Non
     if out is None:
         out = torch.empty((rows, nw * 8), dtype=torch.uint8, device=packed.device)
     _check("awq_unpack", lib.awq_unpack(_ptr(packed), rows, nw * 8, _ptr(out), _stream(stream)))
+    return out
+
+
+ORDER_OLD, ORDER_NEW = 0, 1
+
+
+def awq_pack_order(q: torch.Tensor, order: int, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    rows, n = q.shape
+    if out is None:
+        out = torch.empty((rows, n // 8), dtype=torch.int32, device=q.device)
+    _check("awq_pack_order", lib.awq_pack_order(_ptr(q), rows, n, order, _ptr(out), _stream(stream)))
+    return out
+
+
+def awq_unpack_order(packed: torch.Tensor, order: int, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    rows, nw = packed.shape
+    if out is None:
+        out = torch.empty((rows, nw * 8), dtype=torch.uint8, device=packed.device)
+    _check("awq_unpack_order", lib.awq_unpack_order(_ptr(packed), rows, nw * 8, order, _ptr(out), _stream(stream)))
     return out
 
 

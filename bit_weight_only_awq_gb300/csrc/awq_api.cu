@@ -97,6 +97,32 @@ awq_status awq_unpack(const int32_t* packed, int64_t rows, int64_t n, uint8_t* q
   return from_cuda(launch_unpack(reinterpret_cast<const uint32_t*>(packed), rows, n, q, (cudaStream_t)stream));
 }
 
+awq_status awq_pack_order(const uint8_t* q, int64_t rows, int64_t n, awq_order order, int32_t* packed,
+                          awq_stream_t stream) {
+  if (order != AWQ_ORDER_OLD && order != AWQ_ORDER_NEW) return AWQ_EINVAL;
+  if (rows < 0 || n < 0 || n % 8 != 0) return AWQ_EINVAL;
+  if (rows == 0 || n == 0) return AWQ_OK;
+  if (!q || !packed) return AWQ_ENULL;
+  if (!aligned16(q) || !aligned16(packed)) return AWQ_EALIGN;
+  awq_status st = check_arch();
+  if (st != AWQ_OK) return st;
+  return from_cuda(launch_pack(q, rows, n, reinterpret_cast<uint32_t*>(packed), (cudaStream_t)stream,
+                               order == AWQ_ORDER_NEW));
+}
+
+awq_status awq_unpack_order(const int32_t* packed, int64_t rows, int64_t n, awq_order order, uint8_t* q,
+                            awq_stream_t stream) {
+  if (order != AWQ_ORDER_OLD && order != AWQ_ORDER_NEW) return AWQ_EINVAL;
+  if (rows < 0 || n < 0 || n % 8 != 0) return AWQ_EINVAL;
+  if (rows == 0 || n == 0) return AWQ_OK;
+  if (!q || !packed) return AWQ_ENULL;
+  if (!aligned16(q) || !aligned16(packed)) return AWQ_EALIGN;
+  awq_status st = check_arch();
+  if (st != AWQ_OK) return st;
+  return from_cuda(launch_unpack(reinterpret_cast<const uint32_t*>(packed), rows, n, q, (cudaStream_t)stream,
+                                 order == AWQ_ORDER_NEW));
+}
+
 awq_status awq_dequant(const int32_t* qweight, const int32_t* qzeros, const uint16_t* scales, int64_t K,
                        int64_t N, int32_t group_size, uint16_t* w, awq_stream_t stream) {
   if (group_size != 32 && group_size != 64 && group_size != 128 && group_size != 256) return AWQ_EINVAL;

@@ -20,6 +20,11 @@ inline int grid_for(int64_t work) {
   return (int)(blocks < 1 ? 1 : (blocks > cap ? cap : blocks));
 }
 
+// slot of logical column `col` in a packed word: the older format's map, or (NEW) the new format's [0..7]
+template <bool NEW>
+__device__ __forceinline__ int slot_for(int col) { return NEW ? col : slot_of_col(col); }
+
+template <bool NEW>
 __global__ void pack_kernel(const uint8_t* __restrict__ q, int64_t words, uint32_t* __restrict__ out) {
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < words;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -29,12 +34,13 @@ __global__ void pack_kernel(const uint8_t* __restrict__ q, int64_t words, uint32
     for (int col = 0; col < 8; ++col) {
       uint32_t code = ((col < 4 ? b.x : b.y) >> (8 * (col & 3))) & 0xFFu;
       code = code > 15u ? 15u : code;  // clamp (packer fix on the W4A8 page)
-      w |= code << (4 * slot_of_col(col));
+      w |= code << (4 * slot_for<NEW>(col));
     }
     out[i] = w;
   }
 }
 
+template <bool NEW>
 __global__ void unpack_kernel(const uint32_t* __restrict__ packed, int64_t words, uint8_t* __restrict__ q) {
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < words;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -42,7 +48,7 @@ __global__ void unpack_kernel(const uint32_t* __restrict__ packed, int64_t words
     uint32_t lo = 0, hi = 0;
 #pragma unroll
     for (int col = 0; col < 8; ++col) {
-      const uint32_t code = (w >> (4 * slot_of_col(col))) & 0xFu;
+      const uint32_t code = (w >> (4 * slot_for<NEW>(col))) & 0xFu;
       if (col < 4) lo |= code << (8 * col);
       else hi |= code << (8 * (col - 4));
     }
@@ -93,17 +99,20 @@ __global__ void dequant_kernel(const uint32_t* __restrict__ qw, const uint32_t* 
 
 }  // namespace
 
-cudaError_t launch_pack(const uint8_t* q, int64_t rows, int64_t n, uint32_t* packed, cudaStream_t s) {
+cudaError_t launch_pack(const uint8_t* q, int64_t rows, int64_t n, uint32_t* packed, cudaStream_t s, bool new_order) {
   const int64_t words = rows * (n / 8);
   if (words == 0) return cudaSuccess;
-  pack_kernel<<<grid_for(words), kThreads, 0, s>>>(q, words, packed);
+  if (new_order) pack_kernel<true><<<grid_for(words), kThreads, 0, s>>>(q, words, packed);
+  else pack_kernel<false><<<grid_for(words), kThreads, 0, s>>>(q, words, packed);
   return cudaGetLastError();
 }
 
-cudaError_t launch_unpack(const uint32_t* packed, int64_t rows, int64_t n, uint8_t* q, cudaStream_t s) {
+cudaError_t launch_unpack(const uint32_t* packed, int64_t rows, int64_t n, uint8_t* q, cudaStream_t s,
+                          bool new_order) {
   const int64_t words = rows * (n / 8);
   if (words == 0) return cudaSuccess;
-  unpack_kernel<<<grid_for(words), kThreads, 0, s>>>(packed, words, q);
+  if (new_order) unpack_kernel<true><<<grid_for(words), kThreads, 0, s>>>(packed, words, q);
+  else unpack_kernel<false><<<grid_for(words), kThreads, 0, s>>>(packed, words, q);
   return cudaGetLastError();
 }
 

@@ -33,8 +33,11 @@ inline size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
 int* device_error_ptr();  // nullptr if the symbol address could not be obtained
 
 // ---- elementwise kernels (awq_elementwise.cu)
-cudaError_t launch_pack(const uint8_t* q, int64_t rows, int64_t n, uint32_t* packed, cudaStream_t s);
-cudaError_t launch_unpack(const uint32_t* packed, int64_t rows, int64_t n, uint8_t* q, cudaStream_t s);
+// new_order: the new format's order map [0..7] (else the older [0, 2, 4, 6, 1, 3, 5, 7])
+cudaError_t launch_pack(const uint8_t* q, int64_t rows, int64_t n, uint32_t* packed, cudaStream_t s,
+                        bool new_order = false);
+cudaError_t launch_unpack(const uint32_t* packed, int64_t rows, int64_t n, uint8_t* q, cudaStream_t s,
+                          bool new_order = false);
 // bf16: bf16 scales and output (else fp16)
 cudaError_t launch_dequant(const uint32_t* qw, const uint32_t* qz, const uint16_t* scales, int64_t K,
                            int64_t N, int group, uint16_t* w, cudaStream_t s, bool bf16 = false);

@@ -78,6 +78,22 @@ awq_status awq_unpack(const int32_t *packed, int64_t rows, int64_t n, uint8_t *q
                       awq_stream_t stream);
 
 /*
+ * Order maps of the two AWQ formats: the older one (map [0, 2, 4, 6, 1, 3, 5, 7], the format every
+ * other entry point takes) and the new one (map [0, 1, ..., 7]: nibble slot i holds column 8c + i).
+ * Source: "Speed up AWQ 2.5x with updated kernel", casper-hansen's list of format differences.  The
+ * new format's other differences (skipped zeros, calculate_zeros_width) are not specified there and
+ * are not supported.
+ */
+typedef enum { AWQ_ORDER_OLD = 0, AWQ_ORDER_NEW = 1 } awq_order;
+
+/* awq_pack_order / awq_unpack_order -- awq_pack / awq_unpack with the order map chosen by `order`
+ * (AWQ_EINVAL for another value).  Codes above 15 are clamped as by awq_pack. */
+awq_status awq_pack_order(const uint8_t *q, int64_t rows, int64_t n, awq_order order, int32_t *packed,
+                          awq_stream_t stream);
+awq_status awq_unpack_order(const int32_t *packed, int64_t rows, int64_t n, awq_order order,
+                            uint8_t *q, awq_stream_t stream);
+
+/*
  * awq_dequant -- W[k, n] = fp16_RN((q[k, n] - z[k / g, n]) * s[k / g, n]).
  * qweight int32 [K, N/8]; qzeros int32 [K/g, N/8] or NULL for the symmetric
  * variant (z = 8); scales fp16 [K/g, N]; w fp16 [K, N] (output).

@@ -195,3 +195,12 @@ def test_prepared_layout_entry_points_check_arguments(awq):
     assert ws > 65536 and gp(FAKE, FAKE, FAKE, 4, 4096, 4096, 0, None, 0, None) == EWORKSPACE
     assert awq.awq_workspace_bytes(awq.OP_GEMV_PREPACKED, 4, 4096, 4096, 1) == 0
     assert awq.awq_workspace_bytes(awq.OP_GEMV_PREPACKED, 9, 4096, 4096, 0) == 0
+
+
+def test_order_map_entry_points_check_arguments(awq):
+    lib = awq.lib
+    assert lib.awq_pack_order(FAKE, 4, 16, 2, FAKE, None) == EINVAL     # no third order map
+    assert lib.awq_unpack_order(FAKE, 4, 12, 1, FAKE, None) == EINVAL   # n % 8
+    assert lib.awq_pack_order(None, 4, 16, 1, FAKE, None) == ENULL
+    assert lib.awq_unpack_order(FAKE, 4, 16, 0, FAKE_MISALIGNED, None) == EALIGN
+    assert lib.awq_pack_order(FAKE, 0, 16, 1, FAKE, None) == 0          # nothing to pack

@@ -98,6 +98,17 @@ def test_pack_unpack_bitexact(awq, rows, n):
     assert np.array_equal(host(awq.awq_unpack(dev(words))), oracle.unpack(words))
 
 
+@pytest.mark.parametrize("order", [0, 1])
+@pytest.mark.parametrize("rows,n", [(37, 200), (256, 4096)])
+def test_pack_unpack_both_order_maps_bitexact(awq, rows, n, order):
+    # the older map [0, 2, 4, 6, 1, 3, 5, 7] and the new format's [0..7]
+    omap = oracle.AWQ_ORDER_NEW if order else oracle.AWQ_ORDER
+    codes = synth.random_codes(rows, n, seed=rows + 3 * n, high=32)
+    assert np.array_equal(host(awq.awq_pack_order(dev(codes), order)), oracle.pack(codes, omap))
+    words = synth.random_words(np.random.default_rng(rows + 1), rows, n // 8)
+    assert np.array_equal(host(awq.awq_unpack_order(dev(words), order)), oracle.unpack(words, omap))
+
+
 @pytest.mark.parametrize("symmetric", [False, True])
 @pytest.mark.parametrize("K,N,g", [(512, 512, 128), (384, 264, 128), (256, 64, 64)])
 def test_dequant_bitexact(awq, K, N, g, symmetric):
