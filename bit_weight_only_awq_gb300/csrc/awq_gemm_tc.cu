@@ -173,7 +173,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_s,
             __half* __restrict__ y, int32_t* __restrict__ acc_out, const float* __restrict__ s_tok,
             const __half* __restrict__ s_ch, void* __restrict__ part, int* __restrict__ counters,
-            int* __restrict__ err, int M, int N, int K, int ksteps_per_split, int chunk_steps) {
+            int* __restrict__ err, int M, int N, int K, int ksteps_per_split, int chunk_steps, int m_tiles,
+            int band) {
   using C = Cfg<BT, NB, MODE>;
   // Accumulators in tensor memory: M-block b of K chunk c at column (c * NB + b) * BT.  W4A8 keeps one
   // per chunk of at most chunk_steps k-steps (16384 rows), each an exact integer in fp32; W4A16 uses
@@ -187,7 +188,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
   constexpr int kWBytes = C::kWBytes;
   constexpr int SX = C::kXStages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint8_t* smem = align_smem_1024(smem_raw);
   uint8_t* xring = smem;                                   // SX slots of BT x 32 fp16 (1024-aligned)
   uint8_t* wring = xring + SX * C::kXSlotBytes;            // kWStages x NB x 16 KB (1024-aligned)
   uint8_t* qring = wring + kWStages * kWBytes;             // kQStages x kQStage (128-aligned)
@@ -199,8 +200,18 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * (NB * kBN);
-  const int m0 = blockIdx.y * BT;
+  // output tile of this CTA: bands of `band` token tiles, weight tiles in order within a band and the
+  // band's token tiles fastest, so that the CTAs running at once share a few weight tiles and one
+  // band of activation tiles (which stays in L2 while the band's weight tiles stream past)
+  const int n_tiles = (int)(gridDim.x / (unsigned)m_tiles);
+  const int band_id = (int)blockIdx.x / (band * n_tiles);
+  const int in_band = (int)blockIdx.x - band_id * band * n_tiles;
+  const int band_rows = min(band, m_tiles - band_id * band);
+  const int tile_n = in_band / band_rows;
+  const int tile_m = band_id * band + (in_band - tile_n * band_rows);
+  const int tile_id = tile_m * n_tiles + tile_n;
+  const int n0 = tile_n * (NB * kBN);
+  const int m0 = tile_m * BT;
   const int total_steps = K / kBK;
   const int step0 = blockIdx.z * ksteps_per_split;
   const int nsteps = min(ksteps_per_split, total_steps - step0);
@@ -434,13 +445,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
           if (kIsW4A8<MODE>) {
             const int a = vi[j];
             if (split == 1) {
-              if (acc_out) acc_out[o] = a;
-              y[o] = __float2half_rn(__fmul_rn(__fmul_rn((float)a, s_tok[m]), sch));
+              if (acc_out) __stcs(acc_out + o, a);
+              __stcs(y + o, __float2half_rn(__fmul_rn(__fmul_rn((float)a, s_tok[m]), sch)));
             } else {
               reinterpret_cast<int32_t*>(part)[(size_t)blockIdx.z * M * N + o] = a;
             }
           } else {
-            if (split == 1) y[o] = out_cvt<MODE>(v[j]);
+            if (split == 1) __stcs(y + o, out_cvt<MODE>(v[j]));
             else reinterpret_cast<float*>(part)[(size_t)blockIdx.z * M * N + o] = v[j];
           }
         }
@@ -450,7 +461,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
       __threadfence();
       asm volatile("bar.sync 1, %0;" ::"r"(NB * kDqGroupWarps * 32) : "memory");  // the epilogue groups
       if (group == 0 && d == 0) {
-        const int ctr = blockIdx.y * gridDim.x + blockIdx.x;
+        const int ctr = tile_id;
         *last_flag = (atomicAdd(counters + ctr, 1) == split - 1);
       }
       asm volatile("bar.sync 1, %0;" ::"r"(NB * kDqGroupWarps * 32) : "memory");
@@ -487,14 +498,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             if (m >= M) break;
             const size_t o = (size_t)m * N + n;
             if constexpr (kIsW4A8<MODE>) {
-              if (acc_out) acc_out[o] = a[j];
-              y[o] = __float2half_rn(__fmul_rn(__fmul_rn((float)a[j], s_tok[m]), sch));
+              if (acc_out) __stcs(acc_out + o, a[j]);
+              __stcs(y + o, __float2half_rn(__fmul_rn(__fmul_rn((float)a[j], s_tok[m]), sch)));
             } else {
-              y[o] = out_cvt<MODE>(a[j]);
+              __stcs(y + o, out_cvt<MODE>(a[j]));
             }
           }
         }
-        if (group == 0 && d == 0) atomicExch(counters + blockIdx.y * gridDim.x + blockIdx.x, 0);
+        if (group == 0 && d == 0) atomicExch(counters + tile_id, 0);
       }
     }
   }
@@ -537,11 +548,12 @@ cudaError_t launch_t(const uint16_t* x16, const uint32_t* qw, const uint32_t* qz
   auto kern = gemm_kernel<BT, NB, MODE>;
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), C::kSmem);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.n_tiles, p.m_tiles, p.split);
+  dim3 grid((unsigned)(p.n_tiles * p.m_tiles), 1, p.split);
   kern<<<grid, C::kThreads, C::kSmem, s>>>(tx, tq, tz, ts, reinterpret_cast<__half*>(y), acc_out, s_tok,
                                        reinterpret_cast<const __half*>(s_ch), part, counters, err, (int)M,
                                        (int)N, (int)K, p.ksteps,
-                                       (MODE == kModeW4A8G ? kW4A8GroupChunk : kW4A8MaxKSlice) / kBK);
+                                       (MODE == kModeW4A8G ? kW4A8GroupChunk : kW4A8MaxKSlice) / kBK,
+                                       p.m_tiles, p.band);
   return cudaGetLastError();
 }
 
@@ -646,6 +658,13 @@ GemmPlan gemm_plan(int64_t M, int64_t K, int64_t N, int split_k, int mode) {
   if (split < 1) split = 1;
   p.ksteps = (total + split - 1) / split;
   p.split = (total + p.ksteps - 1) / p.ksteps;
+  // raster band: as many token tiles as keep their activation tiles (fp16, a K slice each) within about
+  // a third of the 126 MB L2, so that they stay resident while the weight tiles stream past
+  const int64_t x_tile = (int64_t)p.bt * p.ksteps * kBK * 2;
+  int64_t band = kRasterBandBytes / (x_tile > 0 ? x_tile : 1);
+  if (band > p.m_tiles) band = p.m_tiles;
+  if (band < 1) band = 1;
+  p.band = (int)band;
   return p;
 }
 

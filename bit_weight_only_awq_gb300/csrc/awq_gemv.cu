@@ -450,7 +450,7 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
   static_assert(!BF16 || (T == 16 && !EXACT), "the bf16 variant is the 16-token W4A16 instance");
   // RB = K / 64 row blocks per tile; unit u = (tile u / RB, row block u % RB); units < 2^31 (host check)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint8_t* smem = align_smem_1024(smem_raw);
   using G = Geo<T>;
   constexpr int kStageBytes = G::kStageBytes;
   constexpr int kXBoxBytes = G::kXBoxBytes;
@@ -489,6 +489,8 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
   if (warp == kConsumers) {
     // ------------------------------------------------ TMA producer
     if (lane == 0) {
+      // the activations' tensor map is read by the first copy after the wait: fetch it now
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_x)) : "memory");
       auto tx_bytes = [&](int nh) {
         return (uint32_t)(nh * (kUnitQBytes + kXBoxBytes) + (has_z ? kZBytes : 0) + (EXACT ? 0 : kSBytes));
       };

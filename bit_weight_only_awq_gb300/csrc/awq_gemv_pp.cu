@@ -101,7 +101,7 @@ gemv_pp_kernel(const __grid_constant__ CUtensorMap tm_x, const uint8_t* __restri
                int tiles, int maxc) {
   // unit u = (tile u / G, group u % G); units < 2^31 (host check)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint8_t* smem = align_smem_1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kPpStages * kPpStageBytes);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kPpStages);
   volatile int* ready_flag = abort_flag + 1;
@@ -133,6 +133,8 @@ gemv_pp_kernel(const __grid_constant__ CUtensorMap tm_x, const uint8_t* __restri
   if (warp == kPpConsumers) {
     // ------------------------------------------------ copy producer
     if (lane == 0) {
+      // the activations' tensor map is read by the first copy after the wait: fetch it now
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_x)) : "memory");
       constexpr uint32_t kTx = (uint32_t)(kPrepackUnitBytes + kPpXBytes);
       auto issue_unit = [&](int st, int u) {
         bulk_load(smem_u32(smem + st * kPpStageBytes + kPpXBytes), packed + (size_t)u * kPrepackUnitBytes,

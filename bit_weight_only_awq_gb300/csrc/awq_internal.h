@@ -114,9 +114,11 @@ struct GemmPlan {
   int split;     // K slices (grid.z)
   int ksteps;    // 64-row k-steps per slice
   int nb;        // 128-column M-blocks per CTA (1, or 2 for W4A16 with >= 128-token tiles)
-  int n_tiles;   // (128 nb)-column weight tiles (grid.x)
-  int m_tiles;   // token tiles (grid.y)
+  int n_tiles;   // (128 nb)-column weight tiles
+  int m_tiles;   // token tiles
+  int band;      // token tiles per raster band (the CTA order: bands, then weight tiles, then token tiles)
 };
+constexpr int64_t kRasterBandBytes = 40ll << 20;
 GemmPlan gemm_plan(int64_t M, int64_t K, int64_t N, int split_k, int mode);
 size_t gemm_workspace_bytes(const GemmPlan& p, int64_t M, int64_t K, int64_t N, int mode);
 // x16: fp16 activations [M, K] (for W4A8 the fp16 copy of the int8 codes).

@@ -12,6 +12,12 @@ constexpr long long kWaitLimitNs = 2000000000LL;  // bound of every device-side 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
+// The first 1024-byte-aligned byte at or after `p` in shared memory.  Written as pointer arithmetic
+// on the shared array itself, not through an integer, so that the compiler still knows the result
+// points to shared memory and accesses through it stay shared-memory loads and stores.
+__device__ __forceinline__ uint8_t* align_smem_1024(uint8_t* p) {
+  return p + ((1024u - (smem_u32(p) & 1023u)) & 1023u);
+}
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
