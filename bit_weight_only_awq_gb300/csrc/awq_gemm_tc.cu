@@ -94,8 +94,13 @@ struct Cfg {
   static constexpr int kSmem = kXStages * kXSlotBytes + kFixed + 1024;
   // W4A8: one accumulator per exact K chunk (two of 16384 rows); with group factors as many 1024-row
   // chunks as tensor memory holds (512 columns)
-  static constexpr int kAccs = MODE == kModeW4A8 ? 2 : MODE == kModeW4A8G ? 512 / (NB * BT) : 1;
-  static constexpr int kTmemCols = NB * kAccs * BT < 32 ? 32 : NB * kAccs * BT;
+  // With group factors and 128-token tiles the 1024-row chunks take turns in two accumulators: while
+  // the mmas fill one, the dequant warps drain the other into an int32 running sum (also in tensor
+  // memory, columns 2 BT ..), so a K slice may be any length.
+  static constexpr bool kDrain = MODE == kModeW4A8G && BT == 128 && NB == 1;
+  static constexpr int kAccs = MODE == kModeW4A8 ? 2 : kDrain ? 2 : MODE == kModeW4A8G ? 512 / (NB * BT) : 1;
+  static constexpr int kSumCol = kAccs * NB * BT;  // drain mode: the int32 running sums
+  static constexpr int kTmemCols = kDrain ? 512 : NB * kAccs * BT < 32 ? 32 : NB * kAccs * BT;
   // Warps: 0 copies activations, 1 issues the mmas (one thread), 2 copies packed weights, 16 dequantize.
   // With tiles of at most 64 tokens the mmas are short and their issue rate limits the k-step, so
   // the dequant warps skip the mma warp's sub-partition (warp % 4 == 1): 24 warps, of which 4..19 run
@@ -111,6 +116,7 @@ struct Cfg {
   static_assert(kXStages >= 2 * kXSub, "activation ring");
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
   static_assert(kTmemCols <= 512, "tensor memory");
+  static_assert(!kDrain || kSumCol + BT <= kTmemCols, "drain layout");
 };
 
 // ------------------------------------------------------------------ tcgen05 mma (A, B from shared memory)
@@ -193,8 +199,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
   uint8_t* wring = xring + SX * C::kXSlotBytes;            // kWStages x NB x 16 KB (1024-aligned)
   uint8_t* qring = wring + kWStages * kWBytes;             // kQStages x kQStage (128-aligned)
   uint64_t* bars = reinterpret_cast<uint64_t*>(qring + kQStages * kQStage);
-  // bars: fullx[SX] emptyx[SX] fullq[Q] emptyq[Q] wready[W] wempty[W] accf
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * SX + 2 * kQStages + 2 * kWStages + 1);
+  // bars: fullx[SX] emptyx[SX] fullq[Q] emptyq[Q] wready[W] wempty[W] accf chunkfull[2] drained[2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * SX + 2 * kQStages + 2 * kWStages + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* last_flag = reinterpret_cast<int*>(tmem_slot + 2);
 
@@ -223,6 +229,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
   auto wready = [&](int s) { return smem_u32(bars + 2 * SX + 2 * kQStages + s); };
   auto wempty = [&](int s) { return smem_u32(bars + 2 * SX + 2 * kQStages + kWStages + s); };
   const uint32_t accf_bar = smem_u32(bars + 2 * SX + 2 * kQStages + 2 * kWStages);
+  // drain mode: an accumulator's chunk is complete (mma commit) / drained (all dequant warps)
+  auto chunkfull = [&](int s) { return smem_u32(bars + 2 * SX + 2 * kQStages + 2 * kWStages + 1 + s); };
+  auto drained = [&](int s) { return smem_u32(bars + 2 * SX + 2 * kQStages + 2 * kWStages + 3 + s); };
+  // drain mode: chunks c < n_drained are drained in the main loop (chunk c by both dequant groups at
+  // k-steps (c + 1) chunk_steps + 4 and + 5, which must exist); the last one or two in the epilogue
+  const int n_drained = (C::kDrain && nsteps > chunk_steps + 5) ? (nsteps - 6) / chunk_steps : 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < SX; ++s) {
@@ -238,6 +250,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
       mbar_init(wempty(s), 1);
     }
     mbar_init(accf_bar, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(chunkfull(s), 1);
+      mbar_init(drained(s), kDqWarps);
+    }
     *abort_flag = 0;
     *last_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -299,6 +315,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
       int ws = 0, xs = 0, chunk = 0, within = 0;
       uint32_t wph = 0, xph = 0;
       for (int it = 0; it < nsteps && ok; ++it) {
+        if (C::kDrain && within == 0 && chunk >= 2) {
+          // the accumulator of chunk - 2 must have been drained before this chunk overwrites it
+          ok = wait_bounded(drained(chunk & 1), (uint32_t)((chunk - 2) >> 1) & 1u, abort_flag, err, 204);
+          if (!ok) break;
+          tc_fence_after();
+        }
         ok = wait_bounded(wready(ws), wph, abort_flag, err, 202);
         const uint64_t ad_s = adesc0 + (uint64_t)((ws * kWBytes) >> 4);
         for (int h = 0; h < C::kXSub && ok; ++h) {
@@ -316,7 +338,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
               // A: weights of M-block b, MN-major; 64-column atoms 1024 B apart (LBO), 8-row k groups
               // 2048 B apart (SBO); k16 step kk starts 4096 B further
               const uint64_t ad = ad_s + (uint64_t)((b * kWBlockBytes + kk * 4096) >> 4);
-              mma_f16(tmem + (uint32_t)((chunk * NB + b) * BT), ad, bd, C::kIdesc, (within > 0 || kk > 0) ? 1u : 0u);
+              const int acc = C::kDrain ? (chunk & 1) : chunk;
+              mma_f16(tmem + (uint32_t)((acc * NB + b) * BT), ad, bd, C::kIdesc, (within > 0 || kk > 0) ? 1u : 0u);
             }
           }
           mma_commit(emptyx(xs));  // this part of the activation tile is free once its mmas have read it
@@ -332,6 +355,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         }
         ++within;  // k-steps accumulated into the current chunk (W4A16: one chunk)
         if (kChunked<MODE> && within == chunk_steps) {
+          if (C::kDrain && chunk < n_drained) mma_commit(chunkfull(chunk & 1));  // drained in the main loop
           within = 0;
           ++chunk;
         }
@@ -356,6 +380,34 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     const int cw = c & 15;           // word column within its M-block
     const uint32_t blk_off = (uint32_t)((c >> 4) * kWBlockBytes);
     for (int it = (C::kSoloMma && warp % 4 == 1) ? nsteps : group; it < nsteps; it += kDqGroups) {
+      if constexpr (C::kDrain) {
+        // chunk ch is drained by group 0 at k-step (ch + 1) chunk_steps + 4 and by group 1 at + 5, a few
+        // k-steps after its last mmas were issued: warp w adds its TMEM lane quarter (w % 4) of token
+        // quarter (w - 3) / 4 into the running sums as exact integers
+        const int rel = it - 4 - group;
+        if (rel >= chunk_steps && rel % chunk_steps == 0 && rel / chunk_steps - 1 < n_drained) {
+          const int ch = rel / chunk_steps - 1;
+          if (!wait_bounded(chunkfull(ch & 1), (uint32_t)(ch >> 1) & 1u, abort_flag, err, 303)) break;
+          tc_fence_after();
+          const uint32_t lanes = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+          const uint32_t col = (uint32_t)(((warp - 3) >> 2) * 32);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t v[16], s[16];
+            tmem_ld16_nowait(lanes + (uint32_t)((ch & 1) * BT) + col + 16 * h, v);
+            if (ch > 0) tmem_ld16_nowait(lanes + (uint32_t)C::kSumCol + col + 16 * h, s);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              s[j] = (uint32_t)((ch > 0 ? (int)s[j] : 0) + __float2int_rn(__uint_as_float(v[j])));
+            tmem_st16(lanes + (uint32_t)C::kSumCol + col + 16 * h, s);
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(drained(ch & 1));
+        }
+      }
       const int qs = it % kQStages, ws = it % kWStages;
       if (!wait_bounded(fullq(qs), (uint32_t)(it / kQStages) & 1u, abort_flag, err, 301)) break;
       if (!wait_bounded(wempty(ws), ((uint32_t)(it / kWStages) & 1u) ^ 1u, abort_flag, err, 302)) break;
@@ -408,7 +460,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
       d = ((warp - 4) % kDqGroupWarps) * 32 + lane;
     }
     if (group < NB) {
-    const bool have = wait_bounded(accf_bar, 0, abort_flag, err, 401);
+    bool have = wait_bounded(accf_bar, 0, abort_flag, err, 401);
+    // drain mode: the running sums are complete once the last chunk drained in the main loop is
+    if (C::kDrain && have && n_drained > 0)
+      have = wait_bounded(drained((n_drained - 1) & 1), (uint32_t)((n_drained - 1) >> 1) & 1u, abort_flag, err, 402);
     tc_fence_after();
     const int lq = warp & 3;                 // TMEM lane quarter this warp may access
     const int half = ((warp - (C::kSoloMma ? 4 : 3)) & 7) >> 2;  // which half of the BT token columns
@@ -424,17 +479,34 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
 #pragma unroll 1
       for (int cb = half * kHalf; cb < (half + 1) * kHalf; cb += 8) {
         float v[8];
-        tmem_ld8(tmem + ((uint32_t)(lq * 32) << 16) + dcol + (uint32_t)cb, v);
         int vi[8];
-        if (kIsW4A8<MODE>) {
+        if constexpr (C::kDrain) {
+          // the running sums of the drained chunks, then the accumulators of the last one or two chunks
+          const uint32_t lanes = tmem + ((uint32_t)(lq * 32) << 16);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) vi[j] = __float2int_rn(v[j]);  // exact integers
-          // the other chunks' accumulators, each an exact integer, added as int32
-          for (int ch = 1; kChunked<MODE> && ch < C::kAccs && ch * chunk_steps < nsteps; ++ch) {
-            float v2[8];
-            tmem_ld8(tmem + ((uint32_t)(lq * 32) << 16) + dcol + (uint32_t)(ch * NB * BT + cb), v2);
+          for (int j = 0; j < 8; ++j) vi[j] = 0;
+          if (n_drained > 0) {
+            tmem_ld8(lanes + (uint32_t)(C::kSumCol + cb), v);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) vi[j] += __float2int_rn(v2[j]);
+            for (int j = 0; j < 8; ++j) vi[j] = __float_as_int(v[j]);
+          }
+          for (int ch = n_drained; ch * chunk_steps < nsteps; ++ch) {
+            tmem_ld8(lanes + (uint32_t)((ch & 1) * BT + cb), v);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) vi[j] += __float2int_rn(v[j]);
+          }
+        } else {
+          tmem_ld8(tmem + ((uint32_t)(lq * 32) << 16) + dcol + (uint32_t)cb, v);
+          if (kIsW4A8<MODE>) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) vi[j] = __float2int_rn(v[j]);  // exact integers
+            // the other chunks' accumulators, each an exact integer, added as int32
+            for (int ch = 1; kChunked<MODE> && ch < C::kAccs && ch * chunk_steps < nsteps; ++ch) {
+              float v2[8];
+              tmem_ld8(tmem + ((uint32_t)(lq * 32) << 16) + dcol + (uint32_t)(ch * NB * BT + cb), v2);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) vi[j] += __float2int_rn(v2[j]);
+            }
           }
         }
 #pragma unroll
@@ -573,9 +645,11 @@ cudaError_t launch_mode(const uint16_t* x16, const uint32_t* qw, const uint32_t*
     }
   }
   if (p.nb != 1) return cudaErrorInvalidValue;
-  if constexpr (MODE == kModeW4A8G) {  // token tiles of at most 64: 8 to 32 chunk accumulators
-    if ((int64_t)p.ksteps * kBK > (int64_t)(512 / p.bt) * kW4A8GroupChunk) return cudaErrorInvalidValue;
+  if constexpr (MODE == kModeW4A8G) {
+    // token tiles of at most 64: 8 to 32 chunk accumulators hold a K slice; 128: two, drained in turn
+    if (p.bt <= 64 && (int64_t)p.ksteps * kBK > (int64_t)(512 / p.bt) * kW4A8GroupChunk) return cudaErrorInvalidValue;
     switch (p.bt) {
+      case 128: return launch_t<128, 1, MODE>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters, err, s);
       case 16: return launch_t<16, 1, MODE>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters, err, s);
       case 32: return launch_t<32, 1, MODE>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters, err, s);
       case 64: return launch_t<64, 1, MODE>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters, err, s);
@@ -620,7 +694,9 @@ GemmPlan gemm_plan(int64_t M, int64_t K, int64_t N, int split_k, int mode) {
   p.nb = 1;
   p.bt = bt0;
   while (p.bt > 64 && tiles(p.bt, 1) < 114) p.bt /= 2;
-  if (mode == kModeW4A8G && p.bt > 64) p.bt = 64;  // 512 / 64 = 8 exact chunks of 1024 rows per K slice
+  // with group factors: at most 64 tokens keep every 1024-row chunk accumulator of a K slice in tensor
+  // memory (512 / 64 = 8); 128 tokens take turns in two accumulators, drained during the main loop
+  if (mode == kModeW4A8G && p.bt > 128) p.bt = 128;
   // >= 128-token tiles: 256 weight columns per CTA (two M-blocks on one activation tile) whenever that
   // still fills about a wave.  W4A8 then has one exact accumulator per M-block, which holds K slices of
   // at most 16384 rows: taken only when K fits one slice (at K = 21760 and 4096 tokens, two M-blocks
@@ -645,10 +721,10 @@ GemmPlan gemm_plan(int64_t M, int64_t K, int64_t N, int split_k, int mode) {
   // fill the 152 SMs: largest split (<= 8, >= 8 k-steps per slice) whose CTA count stays <= one wave,
   // if the unsplit grid is under one wave
   int split = split_k > 0 ? split_k : fill_split((int64_t)p.n_tiles * p.m_tiles, total, 8);
-  if (mode == kModeW4A8 || mode == kModeW4A8G) {
+  if (mode == kModeW4A8 || (mode == kModeW4A8G && p.bt <= 64)) {
     // exact accumulators: each K slice spans at most 2 x 16384 rows with one M-block (two
-    // accumulators), at most 16384 with two M-blocks (one each); with group factors 512 / bt chunks of
-    // 1024 rows
+    // accumulators), at most 16384 with two M-blocks (one each); with group factors and at most 64
+    // tokens, 512 / bt chunks of 1024 rows
     const int64_t slice = mode == kModeW4A8G ? (int64_t)(512 / p.bt) * kW4A8GroupChunk
                                              : (p.nb == 2 ? kW4A8MaxKSlice : 2 * kW4A8MaxKSlice);
     const int min_split = (int)((K + slice - 1) / slice);

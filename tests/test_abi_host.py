@@ -104,6 +104,10 @@ def test_gemm_and_w4a8_argument_checks(awq):
     assert awq.lib.awq_unpack(FAKE, 4, 12, FAKE, None) == EINVAL
 
 
+def align256(n):
+    return (n + 255) // 256 * 256
+
+
 def test_workspace_layout(awq):
     counters = 65536
     # GEMV: counters block + split x M x N fp32 partials (256-byte rounded)
@@ -121,6 +125,13 @@ def test_workspace_layout(awq):
         counters + 4096 * 40960 * 2 + 2 * 4096 * 8192 * 4
     # small-K W4A8 without split still needs the fp16 copy of the codes
     assert awq.awq_workspace_bytes(awq.OP_W4A8_GEMM, 4096, 4096, 8192, 1) == counters + 4096 * 4096 * 2
+    # W4A8 with group factors: 64-token tiles keep at most 8 chunks of 1024 rows per K slice, so
+    # K = 21760 splits in three (int32 partials); 128-token tiles drain their chunks during the main
+    # loop and need no split
+    g = awq.OP_W4A8_GROUPED
+    assert awq.awq_workspace_bytes(g, 64, 21760, 8192, 0) == counters + 64 * 21760 * 2 + 3 * 64 * 8192 * 4
+    assert awq.awq_workspace_bytes(g, 1000, 21760, 8192, 0) == counters + align256(1000 * 21760 * 2)
+    assert awq.awq_workspace_bytes(g, 4096, 21760, 8192, 0) == counters + 4096 * 21760 * 2
     # invalid shapes need nothing (the compute call reports the error)
     assert awq.awq_workspace_bytes(awq.OP_GEMM, 16, 100, 4096, 0) == 0
 

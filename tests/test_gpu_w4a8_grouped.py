@@ -3,8 +3,9 @@
 acc[m, n] = sum_k xq[m, k] (u[k, n] - 8) s3[k / 128, n] is an exact integer and y =
 fp16((fp32(acc) s_tok[m]) s2[n]): both are compared bit for bit (the oracle's
 w4a8_group_linear), on small ragged shapes spanning several 1024-row chunks and K slices, on
-the W4A8 configuration's shape with sampled columns, and on extreme codes where every chunk's
-sum reaches 2^24.
+128-token tiles whose chunks are drained into int32 sums during the main loop (0 to 2 chunks
+drained there, the rest in the epilogue), on the W4A8 configuration's shape with sampled
+columns, and on extreme codes where every chunk's sum reaches 2^24.
 """
 
 import numpy as np
@@ -88,6 +89,44 @@ def test_w4a8_grouped_extreme_chunks(awq, split_k):
     assert want_acc[0, 0] == K * 16384
     assert np.array_equal(acc, want_acc)
     assert np.array_equal(y.view(np.uint16), want_y.view(np.uint16))
+
+
+@pytest.mark.parametrize("split_k", [0, 2])
+@pytest.mark.parametrize("K", [1280, 1408, 2304, 2432, 3200])
+def test_w4a8_grouped_drained_chunks_sampled(awq, K, split_k):
+    # 1000 tokens over 1952 columns take 128-token tiles (the last one 104 tokens, the last column tile 32
+    # columns), whose 1024-row chunks alternate between two accumulators, each drained into int32 sums
+    # during the main loop once the next chunk is a few k-steps in.  K = 1280, 1408, 2304, 2432, 3200
+    # (20 .. 50 k-steps per slice without a split) leave 0, 1, 1, 2, 2 chunks drained in the loop and
+    # the last one or two to the epilogue; split 2 halves every slice.
+    M, N = 1000, 1952
+    p = synth.w4a8_group_problem(M, K, N, seed=9400 + K + split_k)
+    xq, s, y, acc = run(awq, p, split_k)
+    wc = sample_word_cols(N // 8, seed=K + split_k, count=6)
+    cols = (8 * wc[:, None] + np.arange(8)[None, :]).ravel()
+    want_y, want_acc = oracle.w4a8_group_linear(xq, s, p["wq"][:, wc], p["s3"][:, cols], p["s2"][cols], 128)
+    assert np.array_equal(acc[:, cols], want_acc)
+    assert np.array_equal(y[:, cols].view(np.uint16), want_y.view(np.uint16))
+    assert awq.awq_last_device_error() == 0
+
+
+def test_w4a8_grouped_drained_extreme_chunks(awq):
+    # every 1024-row chunk sums to exactly 2^24 in its fp32 accumulator (codes -128 against weights
+    # (0 - 8) * 16), and the drained int32 sums reach 21760 * 2^14 = 356 million: 256 tokens over 7424
+    # columns take 128-token tiles (58 x 2 tiles fill the SMs without a K split)
+    M, K, N = 256, 21760, 7424
+    xq = np.full((M, K), -128, dtype=np.int8)
+    xq[1::3, 1::2] = 127
+    wq = np.zeros((K, N // 8), dtype=np.int32)
+    p = {"x": np.zeros((M, K), np.float16), "wq": wq, "s3": np.full((K // 128, N), 16, np.float16),
+         "s2": np.full(N, 1e-6, np.float16)}
+    _, s, y, acc = run(awq, p, 0, xq=xq)
+    wc = np.array([0, 17, N // 8 - 1])
+    cols = (8 * wc[:, None] + np.arange(8)[None, :]).ravel()
+    want_y, want_acc = oracle.w4a8_group_linear(xq, s, wq[:, wc], p["s3"][:, cols], p["s2"][cols], 128)
+    assert want_acc[0, 0] == K * 16384
+    assert np.array_equal(acc[:, cols], want_acc)
+    assert np.array_equal(y[:, cols].view(np.uint16), want_y.view(np.uint16))
 
 
 @pytest.mark.parametrize("M,K,N", [(1, 21760, 8192), (300, 4096, 1024)])
