@@ -269,11 +269,17 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Launched with programmatic dependent launch: the next kernel in the stream may launch now (it waits
+  // for this grid before it touches shared data), and this grid's own setup and weight stream overlap
+  // the previous kernel.  Only the activation copies (warp 0) and the epilogue, which writes every
+  // global result and reads the per-token scales, wait for it.
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (warp == 0 || warp == 2) {
     // ------------------------------------------------ TMA producers: activations (warp 0), weights (warp 2)
     if (lane == 0) {
       const bool is_x = warp == 0;
+      if (is_x) asm volatile("griddepcontrol.wait;" ::: "memory");
       const int S = is_x ? SX : kQStages;
       const uint32_t tx = is_x ? (uint32_t)C::kXSlotBytes
                                : (uint32_t)(kQBytes + (kHasZeros<MODE> ? C::kZBytes : 0) +
@@ -460,6 +466,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
       d = ((warp - 4) % kDqGroupWarps) * 32 + lane;
     }
     if (group < NB) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // outputs, workspace and s_tok of the previous kernels
     bool have = wait_bounded(accf_bar, 0, abort_flag, err, 401);
     // drain mode: the running sums are complete once the last chunk drained in the main loop is
     if (C::kDrain && have && n_drained > 0)
@@ -620,12 +627,21 @@ cudaError_t launch_t(const uint16_t* x16, const uint32_t* qw, const uint32_t* qz
   auto kern = gemm_kernel<BT, NB, MODE>;
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), C::kSmem);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)(p.n_tiles * p.m_tiles), 1, p.split);
-  kern<<<grid, C::kThreads, C::kSmem, s>>>(tx, tq, tz, ts, reinterpret_cast<__half*>(y), acc_out, s_tok,
-                                       reinterpret_cast<const __half*>(s_ch), part, counters, err, (int)M,
-                                       (int)N, (int)K, p.ksteps,
-                                       (MODE == kModeW4A8G ? kW4A8GroupChunk : kW4A8MaxKSlice) / kBK,
-                                       p.m_tiles, p.band);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3((unsigned)(p.n_tiles * p.m_tiles), 1, p.split);
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, tx, tq, tz, ts, reinterpret_cast<__half*>(y), acc_out, s_tok,
+                         reinterpret_cast<const __half*>(s_ch), part, counters, err, (int)M, (int)N, (int)K,
+                         p.ksteps, (MODE == kModeW4A8G ? kW4A8GroupChunk : kW4A8MaxKSlice) / kBK, p.m_tiles,
+                         p.band);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -48,6 +48,9 @@ __device__ __forceinline__ void store_codes(const uint32_t (&out)[2], int8_t* xq
 __global__ void __launch_bounds__(kQThreads)
 quant_act_smem_kernel(const __half* __restrict__ x, int8_t* __restrict__ xq, float* __restrict__ s_tok,
                       __half* __restrict__ x16, int K) {
+  // the GEMM that reads these codes is launched as a programmatic dependent: it may start its setup
+  // and weight stream now and waits for this grid to complete before it reads them
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   extern __shared__ uint4 row[];
   __shared__ uint32_t warp_max[kQThreads / 32];
   __shared__ float s_shared;
@@ -99,6 +102,7 @@ quant_act_smem_kernel(const __half* __restrict__ x, int8_t* __restrict__ xq, flo
 __global__ void __launch_bounds__(kQThreads)
 quant_act_kernel(const __half* __restrict__ x, int8_t* __restrict__ xq, float* __restrict__ s_tok,
                  __half* __restrict__ x16, int K) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __shared__ uint32_t warp_max[kQThreads / 32];
   __shared__ float s_shared;
   const int64_t row = blockIdx.x;
@@ -148,6 +152,7 @@ quant_act_kernel(const __half* __restrict__ x, int8_t* __restrict__ xq, float* _
 }
 
 __global__ void i8_to_f16_kernel(const int8_t* __restrict__ xq, __half* __restrict__ out, int64_t nvec) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < nvec; i += (int64_t)gridDim.x * blockDim.x) {
     const uint2 v = __ldg(reinterpret_cast<const uint2*>(xq) + i);
     uint32_t o[4];
