@@ -94,11 +94,15 @@ struct Cfg {
   static constexpr int kSmem = kXStages * kXSlotBytes + kFixed + 1024;
   // W4A8: one accumulator per exact K chunk (two of 16384 rows); with group factors as many 1024-row
   // chunks as tensor memory holds (512 columns)
-  // With group factors and 128-token tiles the 1024-row chunks take turns in two accumulators: while
-  // the mmas fill one, the dequant warps drain the other into an int32 running sum (also in tensor
-  // memory, columns 2 BT ..), so a K slice may be any length.
-  static constexpr bool kDrain = MODE == kModeW4A8G && BT == 128 && NB == 1;
-  static constexpr int kAccs = MODE == kModeW4A8 ? 2 : kDrain ? 2 : MODE == kModeW4A8G ? 512 / (NB * BT) : 1;
+  // With group factors and 128- or 256-token tiles every finished 1024-row chunk is drained by the
+  // dequant warps into an int32 running sum (also in tensor memory, after the accumulators), so a K
+  // slice may be any length.  128 tokens: the chunks take turns in two accumulators, the mmas fill one
+  // while the other drains; 256 tokens: one accumulator, and the mmas of a chunk wait for the drain of
+  // the one before.
+  static constexpr bool kDrain = MODE == kModeW4A8G && NB == 1 && (BT == 128 || BT == 256);
+  static constexpr int kAccSlots = BT == 128 ? 2 : 1;                 // drain mode
+  static constexpr int kDrainLag = kAccSlots == 2 ? 4 : 0;           // k-steps into the next chunk
+  static constexpr int kAccs = MODE == kModeW4A8 ? 2 : kDrain ? kAccSlots : MODE == kModeW4A8G ? 512 / (NB * BT) : 1;
   static constexpr int kSumCol = kAccs * NB * BT;  // drain mode: the int32 running sums
   static constexpr int kTmemCols = kDrain ? 512 : NB * kAccs * BT < 32 ? 32 : NB * kAccs * BT;
   // Warps: 0 copies activations, 1 issues the mmas (one thread), 2 copies packed weights, 16 dequantize.
@@ -117,6 +121,7 @@ struct Cfg {
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
   static_assert(kTmemCols <= 512, "tensor memory");
   static_assert(!kDrain || kSumCol + BT <= kTmemCols, "drain layout");
+  static_assert(kDrainLag % 2 == 0, "the two dequant groups drain at one even and the next odd k-step");
 };
 
 // ------------------------------------------------------------------ tcgen05 mma (A, B from shared memory)
@@ -232,9 +237,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
   // drain mode: an accumulator's chunk is complete (mma commit) / drained (all dequant warps)
   auto chunkfull = [&](int s) { return smem_u32(bars + 2 * SX + 2 * kQStages + 2 * kWStages + 1 + s); };
   auto drained = [&](int s) { return smem_u32(bars + 2 * SX + 2 * kQStages + 2 * kWStages + 3 + s); };
-  // drain mode: chunks c < n_drained are drained in the main loop (chunk c by both dequant groups at
-  // k-steps (c + 1) chunk_steps + 4 and + 5, which must exist); the last one or two in the epilogue
-  const int n_drained = (C::kDrain && nsteps > chunk_steps + 5) ? (nsteps - 6) / chunk_steps : 0;
+  // drain mode: every chunk but the slice's last is drained into the running sums (group g at its first
+  // k-step from (c + 1) chunk_steps + kDrainLag on, or after its loop if it has none); the epilogue adds
+  // the last chunk's accumulator
+  const int n_chunks = kChunked<MODE> ? (nsteps + chunk_steps - 1) / chunk_steps : 1;
+  constexpr int kS = C::kAccSlots;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < SX; ++s) {
@@ -321,9 +328,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
       int ws = 0, xs = 0, chunk = 0, within = 0;
       uint32_t wph = 0, xph = 0;
       for (int it = 0; it < nsteps && ok; ++it) {
-        if (C::kDrain && within == 0 && chunk >= 2) {
-          // the accumulator of chunk - 2 must have been drained before this chunk overwrites it
-          ok = wait_bounded(drained(chunk & 1), (uint32_t)((chunk - 2) >> 1) & 1u, abort_flag, err, 204);
+        if (C::kDrain && within == 0 && chunk >= kS) {
+          // the accumulator of chunk - kS must have been drained before this chunk overwrites it
+          ok = wait_bounded(drained(chunk % kS), (uint32_t)((chunk - kS) / kS) & 1u, abort_flag, err, 204);
           if (!ok) break;
           tc_fence_after();
         }
@@ -344,7 +351,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
               // A: weights of M-block b, MN-major; 64-column atoms 1024 B apart (LBO), 8-row k groups
               // 2048 B apart (SBO); k16 step kk starts 4096 B further
               const uint64_t ad = ad_s + (uint64_t)((b * kWBlockBytes + kk * 4096) >> 4);
-              const int acc = C::kDrain ? (chunk & 1) : chunk;
+              const int acc = C::kDrain ? chunk % kS : chunk;
               mma_f16(tmem + (uint32_t)((acc * NB + b) * BT), ad, bd, C::kIdesc, (within > 0 || kk > 0) ? 1u : 0u);
             }
           }
@@ -361,7 +368,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         }
         ++within;  // k-steps accumulated into the current chunk (W4A16: one chunk)
         if (kChunked<MODE> && within == chunk_steps) {
-          if (C::kDrain && chunk < n_drained) mma_commit(chunkfull(chunk & 1));  // drained in the main loop
+          if (C::kDrain && chunk < n_chunks - 1) mma_commit(chunkfull(chunk % kS));  // to be drained
           within = 0;
           ++chunk;
         }
@@ -385,33 +392,40 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     const int r0 = d / kQWords;      // first of the thread's rows (r0 + kRowsPerPass j)
     const int cw = c & 15;           // word column within its M-block
     const uint32_t blk_off = (uint32_t)((c >> 4) * kWBlockBytes);
+    // drain mode: warp w adds its TMEM lane quarter (w % 4) of token quarter (w - 3) / 4 of chunk ch's
+    // accumulator into the running sums, as exact integers, then arrives on drained
+    int next_drain = 0;
+    auto drain = [&](int ch) -> bool {
+      if (!wait_bounded(chunkfull(ch % kS), (uint32_t)(ch / kS) & 1u, abort_flag, err, 303)) return false;
+      tc_fence_after();
+      const uint32_t lanes = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+      const uint32_t col = (uint32_t)(((warp - 3) >> 2) * (BT / 4));
+#pragma unroll
+      for (int h = 0; h < BT / 64; ++h) {
+        uint32_t v[16], s[16];
+        tmem_ld16_nowait(lanes + (uint32_t)((ch % kS) * BT) + col + 16 * h, v);
+        if (ch > 0) tmem_ld16_nowait(lanes + (uint32_t)C::kSumCol + col + 16 * h, s);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          s[j] = (uint32_t)((ch > 0 ? (int)s[j] : 0) + __float2int_rn(__uint_as_float(v[j])));
+        tmem_st16(lanes + (uint32_t)C::kSumCol + col + 16 * h, s);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(drained(ch % kS));
+      return true;
+    };
     for (int it = (C::kSoloMma && warp % 4 == 1) ? nsteps : group; it < nsteps; it += kDqGroups) {
       if constexpr (C::kDrain) {
-        // chunk ch is drained by group 0 at k-step (ch + 1) chunk_steps + 4 and by group 1 at + 5, a few
-        // k-steps after its last mmas were issued: warp w adds its TMEM lane quarter (w % 4) of token
-        // quarter (w - 3) / 4 into the running sums as exact integers
-        const int rel = it - 4 - group;
-        if (rel >= chunk_steps && rel % chunk_steps == 0 && rel / chunk_steps - 1 < n_drained) {
-          const int ch = rel / chunk_steps - 1;
-          if (!wait_bounded(chunkfull(ch & 1), (uint32_t)(ch >> 1) & 1u, abort_flag, err, 303)) break;
-          tc_fence_after();
-          const uint32_t lanes = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-          const uint32_t col = (uint32_t)(((warp - 3) >> 2) * 32);
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            uint32_t v[16], s[16];
-            tmem_ld16_nowait(lanes + (uint32_t)((ch & 1) * BT) + col + 16 * h, v);
-            if (ch > 0) tmem_ld16_nowait(lanes + (uint32_t)C::kSumCol + col + 16 * h, s);
-            tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              s[j] = (uint32_t)((ch > 0 ? (int)s[j] : 0) + __float2int_rn(__uint_as_float(v[j])));
-            tmem_st16(lanes + (uint32_t)C::kSumCol + col + 16 * h, s);
-          }
-          tmem_wait_st();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(drained(ch & 1));
+        // chunk ch is drained by group 0 at k-step (ch + 1) chunk_steps + kDrainLag and by group 1 one
+        // later (with one accumulator, at the first two k-steps of the next chunk, whose mmas wait for it)
+        const int rel = it - C::kDrainLag - group;
+        if (rel >= chunk_steps && rel % chunk_steps == 0 && rel / chunk_steps - 1 == next_drain &&
+            next_drain < n_chunks - 1) {
+          if (!drain(next_drain)) break;
+          ++next_drain;
         }
       }
       const int qs = it % kQStages, ws = it % kWStages;
@@ -459,6 +473,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
       __syncwarp();
       if (lane == 0) mbar_arrive(wready(ws));
     }
+    // drain mode: chunks whose drain step this warp's group never reached
+    if constexpr (C::kDrain)
+      while (next_drain < n_chunks - 1 && drain(next_drain)) ++next_drain;
 
     // ------------------------------------------------ epilogue (dequant group b reads M-block b)
     if (C::kSoloMma) {  // warps 4..19
@@ -468,9 +485,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     if (group < NB) {
     asm volatile("griddepcontrol.wait;" ::: "memory");  // outputs, workspace and s_tok of the previous kernels
     bool have = wait_bounded(accf_bar, 0, abort_flag, err, 401);
-    // drain mode: the running sums are complete once the last chunk drained in the main loop is
-    if (C::kDrain && have && n_drained > 0)
-      have = wait_bounded(drained((n_drained - 1) & 1), (uint32_t)((n_drained - 1) >> 1) & 1u, abort_flag, err, 402);
+    // drain mode: the running sums are complete once the slice's next-to-last chunk is drained
+    if (C::kDrain && have && n_chunks > 1)
+      have = wait_bounded(drained((n_chunks - 2) % kS), (uint32_t)((n_chunks - 2) / kS) & 1u, abort_flag, err, 402);
     tc_fence_after();
     const int lq = warp & 3;                 // TMEM lane quarter this warp may access
     const int half = ((warp - (C::kSoloMma ? 4 : 3)) & 7) >> 2;  // which half of the BT token columns
@@ -488,20 +505,18 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         float v[8];
         int vi[8];
         if constexpr (C::kDrain) {
-          // the running sums of the drained chunks, then the accumulators of the last one or two chunks
+          // the running sums of the drained chunks, then the accumulator of the slice's last chunk
           const uint32_t lanes = tmem + ((uint32_t)(lq * 32) << 16);
 #pragma unroll
           for (int j = 0; j < 8; ++j) vi[j] = 0;
-          if (n_drained > 0) {
+          if (n_chunks > 1) {
             tmem_ld8(lanes + (uint32_t)(C::kSumCol + cb), v);
 #pragma unroll
             for (int j = 0; j < 8; ++j) vi[j] = __float_as_int(v[j]);
           }
-          for (int ch = n_drained; ch * chunk_steps < nsteps; ++ch) {
-            tmem_ld8(lanes + (uint32_t)((ch & 1) * BT + cb), v);
+          tmem_ld8(lanes + (uint32_t)(((n_chunks - 1) % kS) * BT + cb), v);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) vi[j] += __float2int_rn(v[j]);
-          }
+          for (int j = 0; j < 8; ++j) vi[j] += __float2int_rn(v[j]);
         } else {
           tmem_ld8(tmem + ((uint32_t)(lq * 32) << 16) + dcol + (uint32_t)cb, v);
           if (kIsW4A8<MODE>) {
@@ -666,6 +681,7 @@ cudaError_t launch_mode(const uint16_t* x16, const uint32_t* qw, const uint32_t*
     if (p.bt <= 64 && (int64_t)p.ksteps * kBK > (int64_t)(512 / p.bt) * kW4A8GroupChunk) return cudaErrorInvalidValue;
     switch (p.bt) {
       case 128: return launch_t<128, 1, MODE>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters, err, s);
+      case 256: return launch_t<256, 1, MODE>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters, err, s);
       case 16: return launch_t<16, 1, MODE>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters, err, s);
       case 32: return launch_t<32, 1, MODE>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters, err, s);
       case 64: return launch_t<64, 1, MODE>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters, err, s);
@@ -711,8 +727,7 @@ GemmPlan gemm_plan(int64_t M, int64_t K, int64_t N, int split_k, int mode) {
   p.bt = bt0;
   while (p.bt > 64 && tiles(p.bt, 1) < 114) p.bt /= 2;
   // with group factors: at most 64 tokens keep every 1024-row chunk accumulator of a K slice in tensor
-  // memory (512 / 64 = 8); 128 tokens take turns in two accumulators, drained during the main loop
-  if (mode == kModeW4A8G && p.bt > 128) p.bt = 128;
+  // memory (512 / 64 = 8); 128 and 256 tokens drain their chunks during the main loop
   // >= 128-token tiles: 256 weight columns per CTA (two M-blocks on one activation tile) whenever that
   // still fills about a wave.  W4A8 then has one exact accumulator per M-block, which holds K slices of
   // at most 16384 rows: taken only when K fits one slice (at K = 21760 and 4096 tokens, two M-blocks

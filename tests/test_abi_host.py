@@ -126,8 +126,8 @@ def test_workspace_layout(awq):
     # small-K W4A8 without split still needs the fp16 copy of the codes
     assert awq.awq_workspace_bytes(awq.OP_W4A8_GEMM, 4096, 4096, 8192, 1) == counters + 4096 * 4096 * 2
     # W4A8 with group factors: 64-token tiles keep at most 8 chunks of 1024 rows per K slice, so
-    # K = 21760 splits in three (int32 partials); 128-token tiles drain their chunks during the main
-    # loop and need no split
+    # K = 21760 splits in three (int32 partials); 128- and 256-token tiles drain their chunks during the
+    # main loop and need no split
     g = awq.OP_W4A8_GROUPED
     assert awq.awq_workspace_bytes(g, 64, 21760, 8192, 0) == counters + 64 * 21760 * 2 + 3 * 64 * 8192 * 4
     assert awq.awq_workspace_bytes(g, 1000, 21760, 8192, 0) == counters + align256(1000 * 21760 * 2)

@@ -95,10 +95,10 @@ def test_w4a8_grouped_extreme_chunks(awq, split_k):
 @pytest.mark.parametrize("K", [1280, 1408, 2304, 2432, 3200])
 def test_w4a8_grouped_drained_chunks_sampled(awq, K, split_k):
     # 1000 tokens over 1952 columns take 128-token tiles (the last one 104 tokens, the last column tile 32
-    # columns), whose 1024-row chunks alternate between two accumulators, each drained into int32 sums
-    # during the main loop once the next chunk is a few k-steps in.  K = 1280, 1408, 2304, 2432, 3200
-    # (20 .. 50 k-steps per slice without a split) leave 0, 1, 1, 2, 2 chunks drained in the loop and
-    # the last one or two to the epilogue; split 2 halves every slice.
+    # columns), whose 1024-row chunks alternate between two accumulators; every chunk but a slice's last
+    # is drained into int32 sums once the next chunk is four k-steps in, or after the loop when the slice
+    # ends first (K = 1280: 20 k-steps).  K = 1280 .. 3200 gives 2 to 4 chunks per slice; split 2 halves
+    # every slice.
     M, N = 1000, 1952
     p = synth.w4a8_group_problem(M, K, N, seed=9400 + K + split_k)
     xq, s, y, acc = run(awq, p, split_k)
@@ -110,11 +110,31 @@ def test_w4a8_grouped_drained_chunks_sampled(awq, K, split_k):
     assert awq.awq_last_device_error() == 0
 
 
-def test_w4a8_grouped_drained_extreme_chunks(awq):
+@pytest.mark.parametrize("split_k", [0, 2])
+@pytest.mark.parametrize("K", [1024, 1152, 2176, 3200])
+def test_w4a8_grouped_drained_chunks_256_token_tiles_sampled(awq, K, split_k):
+    # 2000 tokens over 1952 columns take 256-token tiles (the last one 208 tokens) with one chunk
+    # accumulator: the mmas of a chunk wait until the dequant warps have drained the one before, at the
+    # first two k-steps of the new chunk.  K = 1024 (one chunk, nothing drained), 1152 (a last chunk of
+    # two k-steps), 2176, 3200; with split 2 the 2176 slices end in a one-k-step chunk whose predecessor
+    # one dequant group drains after its loop.
+    M, N = 2000, 1952
+    p = synth.w4a8_group_problem(M, K, N, seed=9450 + K + split_k)
+    xq, s, y, acc = run(awq, p, split_k)
+    wc = sample_word_cols(N // 8, seed=K + split_k + 1, count=5)
+    cols = (8 * wc[:, None] + np.arange(8)[None, :]).ravel()
+    want_y, want_acc = oracle.w4a8_group_linear(xq, s, p["wq"][:, wc], p["s3"][:, cols], p["s2"][cols], 128)
+    assert np.array_equal(acc[:, cols], want_acc)
+    assert np.array_equal(y[:, cols].view(np.uint16), want_y.view(np.uint16))
+    assert awq.awq_last_device_error() == 0
+
+
+@pytest.mark.parametrize("M", [256, 512])
+def test_w4a8_grouped_drained_extreme_chunks(awq, M):
     # every 1024-row chunk sums to exactly 2^24 in its fp32 accumulator (codes -128 against weights
-    # (0 - 8) * 16), and the drained int32 sums reach 21760 * 2^14 = 356 million: 256 tokens over 7424
-    # columns take 128-token tiles (58 x 2 tiles fill the SMs without a K split)
-    M, K, N = 256, 21760, 7424
+    # (0 - 8) * 16), and the drained int32 sums reach 21760 * 2^14 = 356 million: over 7424 columns, 256
+    # tokens take 128-token tiles (two accumulators), 512 tokens 256-token tiles (one)
+    K, N = 21760, 7424
     xq = np.full((M, K), -128, dtype=np.int8)
     xq[1::3, 1::2] = 127
     wq = np.zeros((K, N // 8), dtype=np.int32)
