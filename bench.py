@@ -602,7 +602,7 @@ def dominant_kernel(workload):
             "crossover": ("awq_gemv + awq_gemm", "hbm"), "crossover_sym": ("awq_gemv + awq_gemm", "hbm"),
             "w4a8": ("w4a8_linear (gemm_kernel<W4A8>)", "tensor"),
             "w4a8_grouped": ("w4a8_linear_grouped (gemm_kernel<W4A8, group factors>)", "tensor"),
-            "decode_bf16": ("awq_gemv_bf16 (gemv_kernel<16, bf16>)", "hbm"),
+            "decode_bf16": ("awq_gemv_bf16 (gemv_kernel<8, bf16>)", "hbm"),
             "prefill_bf16": ("awq_gemm_bf16 (gemm_kernel<bf16>)", "tensor")}[workload]
 
 

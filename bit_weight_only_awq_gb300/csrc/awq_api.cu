@@ -183,7 +183,7 @@ size_t awq_workspace_bytes(awq_op op, int64_t M, int64_t K, int64_t N, int32_t s
     case AWQ_OP_GEMM:
       if (!gemm_shape_ok(M, K, N, split_k) || M == 0) return 0;
       return gemm_workspace_bytes(gemm_plan(M, K, N, split_k, kModeZeroPoint), M, K, N, kModeZeroPoint);
-    case AWQ_OP_GEMV_BF16:  // the 16-token instance: partials of 16 token rows
+    case AWQ_OP_GEMV_BF16:  // sized for the 16-token instance's partials (the 8-token one needs half)
       if (!gemv_shape_ok(M, K, N, kGroup, split_k) || M == 0) return 0;
       return gemv_workspace_bytes(gemv_plan(M, K, N, split_k), 16, N);
     case AWQ_OP_GEMM_BF16:

@@ -308,9 +308,9 @@ __device__ __forceinline__ void group_consts_bf16(uint32_t zword, const uint4& s
 // acc[h] += W^T x_h over the 64 rows held in `sr`, for the two 8-token halves h.  HSUB2 of the zero
 // (exact) then HMUL2 by the scale (s / 16 for the 16 q of the high nibble) give W = fp16_RN((q - z) s);
 // BF16: the bf16 forms, W = bf16_RN((q - z) s).
-template <bool BF16 = false>
-__device__ __forceinline__ void compute_stage16(const StageRegs<16>& sr, const GroupConstsH& c,
-                                                float (&acc)[2][4][4]) {
+template <int T, bool BF16 = false>
+__device__ __forceinline__ void compute_stage_exact(const StageRegs<T>& sr, const GroupConstsH& c,
+                                                    float (&acc)[T / 8][4][4]) {
   if constexpr (BF16) {
 #pragma unroll
     for (int it = 0; it < 4; ++it) {
@@ -328,7 +328,7 @@ __device__ __forceinline__ void compute_stage16(const StageRegs<16>& sr, const G
         a[b][3] = bmul2(bsub2(magic_bf16(p23[b] >> 4), c.zhi[b]), c.shi[b]);
       }
 #pragma unroll
-      for (int h = 0; h < 2; ++h)
+      for (int h = 0; h < T / 8; ++h)
 #pragma unroll
         for (int b = 0; b < 4; ++b)
           mma16816_bf16(acc[h][b], a[b][0], a[b][1], a[b][2], a[b][3], sr.b[h][it][0], sr.b[h][it][1]);
@@ -351,7 +351,7 @@ __device__ __forceinline__ void compute_stage16(const StageRegs<16>& sr, const G
       a[b][3] = hmul2(hsub2(magic<0x00F000F0u>(p23[b]), c.zhi[b]), c.shi[b]);
     }
 #pragma unroll
-    for (int h = 0; h < 2; ++h)
+    for (int h = 0; h < T / 8; ++h)
 #pragma unroll
       for (int b = 0; b < 4; ++b)
         mma16816(acc[h][b], a[b][0], a[b][1], a[b][2], a[b][3], sr.b[h][it][0], sr.b[h][it][1]);
@@ -447,7 +447,10 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             int M, int N, int RB, int tiles, int maxc, const float* __restrict__ s_tok,
             const __half* __restrict__ s_ch, int32_t* __restrict__ acc_out) {
   static_assert(!EXACT || T == 16, "the exact product uses the 16-token instance");
-  static_assert(!BF16 || (T == 16 && !EXACT), "the bf16 variant is the 16-token W4A16 instance");
+  static_assert(!BF16 || !EXACT, "the bf16 variant is a W4A16 instance");
+  // fp16 with up to 8 tokens folds zero point and scale into the fp32 sums; the others make every
+  // weight exactly (bf16 keeps exact weights at 8 tokens too: its 8-bit weights would not fit the fold)
+  constexpr bool kFold = T == 8 && !BF16;
   // RB = K / 64 row blocks per tile; unit u = (tile u / RB, row block u % RB); units < 2^31 (host check)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = align_smem_1024(smem_raw);
@@ -554,7 +557,7 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     float hold[kHalves][4][4];        // own_tile's sums, kept in registers for its reduction
     bool failed = false;              // a wait ran out: error recorded, the rest of the call skipped
     // zero / scale constants of the current group (cached_grp)
-    typename std::conditional<T == 8, GroupConsts, GroupConstsH>::type gc;
+    typename std::conditional<kFold, GroupConsts, GroupConstsH>::type gc;
     int cached_grp = -1;
     int i = 0;                        // stage counter, identical to the producer's
     int cst = 0;                      // its ring slot (i % kStages) and phase ((i / kStages) & 1)
@@ -591,12 +594,12 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
           const uint32_t zword = has_z ? reinterpret_cast<const uint32_t*>(sb + kZOff)[word] : 0x88888888u;
           const uint4 sv = EXACT ? make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u)  // 1.0
                                  : reinterpret_cast<const uint4*>(sb + kSOff)[word];
-          if constexpr (T == 8) group_consts(zword, sv, gc);
+          if constexpr (kFold) group_consts(zword, sv, gc);
           else if constexpr (BF16) group_consts_bf16(zword, sv, gc);
           else group_consts_h(zword, sv, gc);
           cached_grp = grp;
         }
-        if constexpr (T == 8) {
+        if constexpr (kFold) {
           float gacc[4][4], sx[4];  // this stage's (1024 + q)^T x and sum_k x
 #pragma unroll
           for (int b = 0; b < 4; ++b) {
@@ -620,15 +623,15 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             for (int e = 0; e < 4; ++e)
               acc[0][b][e] = fmaf(gacc[b][e], gc.sf[b][e >> 1], fmaf(-gc.szc[b][e >> 1], sx[e & 1], acc[0][b][e]));
         } else {
-          StageRegs<16> sr;
-          load_stage<16>(sb, 0, lo, sr);
+          StageRegs<T> sr;
+          load_stage<T>(sb, 0, lo, sr);
           if (nh == 2) {
-            compute_stage16<BF16>(sr, gc, acc);
-            load_stage<16>(sb, 1, lo, sr);
+            compute_stage_exact<T, BF16>(sr, gc, acc);
+            load_stage<T>(sb, 1, lo, sr);
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(empty_bar(st));  // slot free before the last unit's arithmetic
-          compute_stage16<BF16>(sr, gc, acc);
+          compute_stage_exact<T, BF16>(sr, gc, acc);
         }
       }
       if (failed) break;
@@ -899,7 +902,7 @@ GemvPlan gemv_plan(int64_t M, int64_t K, int64_t N, int split_k) {
 size_t gemv_workspace_bytes(const GemvPlan& p, int64_t M, int64_t N) {
   (void)N;
   if (p.maxc <= 1) return 0;
-  const size_t tokens = M <= 8 ? 8 : 16;  // token rows of a partial: the kernel's T (bf16 always runs T = 16)
+  const size_t tokens = M <= 8 ? 8 : 16;  // token rows of a partial: the kernel's T
   return kCounterBytes + align256((size_t)p.tiles * p.maxc * tokens * kTileCols * sizeof(float));
 }
 
@@ -958,7 +961,10 @@ cudaError_t launch_gemv(const uint16_t* x, const uint32_t* qw, const uint32_t* q
                         int* err, cudaStream_t s, bool bf16) {
   // the kernel counts (tile, 64-row block) units in 32 bits; any tensor that fits a GPU stays far below
   if ((int64_t)p.tiles * p.groups >= ((int64_t)1 << 31)) return cudaErrorInvalidValue;
-  if (bf16) return launch_gemv_t<16, false, true>(x, qw, qz, sc, y, M, K, N, p, ws, err, s);
+  if (bf16) {
+    if (M <= 8) return launch_gemv_t<8, false, true>(x, qw, qz, sc, y, M, K, N, p, ws, err, s);
+    return launch_gemv_t<16, false, true>(x, qw, qz, sc, y, M, K, N, p, ws, err, s);
+  }
   if (M <= 8) return launch_gemv_t<8, false>(x, qw, qz, sc, y, M, K, N, p, ws, err, s);
   return launch_gemv_t<16, false>(x, qw, qz, sc, y, M, K, N, p, ws, err, s);
 }

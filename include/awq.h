@@ -262,9 +262,9 @@ awq_status awq_gemm(const uint16_t *x, const int32_t *qweight, const int32_t *qz
  *
  * awq_gemv_bf16 -- y = x * W for M <= 16 tokens, bf16 x [M, K], scales, y [M, N].  Every weight is
  * made exactly as awq_dequant_bf16 makes it and multiplied on the tensor pipe with fp32 accumulation;
- * the output is rounded once.  Runs the 16-token instance of the decode kernel for every M (its
- * workspace: awq_workspace_bytes(AWQ_OP_GEMV_BF16, ...)); split_k and the residency assumption as for
- * awq_gemv.
+ * the output is rounded once.  Runs the 8-token instance of the decode kernel up to 8 tokens and the
+ * 16-token one above (workspace: awq_workspace_bytes(AWQ_OP_GEMV_BF16, ...), sized for 16 token rows
+ * of partials whatever M); split_k and the residency assumption as for awq_gemv.
  *
  * awq_gemm_bf16 -- the tensor-core GEMM (tcgen05 kind::f16 with bf16 A and B) for any M >= 1, bf16
  * x, scales and y; workspace awq_workspace_bytes(AWQ_OP_GEMM_BF16, ...); otherwise as awq_gemm.
