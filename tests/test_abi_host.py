@@ -143,10 +143,15 @@ def test_gemm_plan_split_choices(awq):
     ws = lambda M, K, N: awq.awq_workspace_bytes(awq.OP_GEMM, M, K, N, 0)
     # one M-block fits one wave (128 CTAs of 64 tokens): no split
     assert ws(256, 4096, 4096) == 0
-    # one M-block would need a second wave (192 CTAs): two M-blocks with a split of three
-    assert ws(256, 4096, 6144) == counters + 3 * 256 * 6144 * 4
-    # two M-blocks fill the wave with slices of 56 k-steps: split of four
+    # above 64 tokens the measured cost model may replace that plan: 256 tokens over 6144 columns take
+    # one M-block of 128-token tiles in one wave (96 CTAs) instead of two M-blocks with a split of three
+    assert ws(256, 4096, 6144) == 0
+    # two M-blocks fill the wave with slices of 56 k-steps: split of four (the model's best differs by
+    # less than 5 %, so the plan stays)
     assert ws(256, 14336, 4096) == counters + 4 * 256 * 4096 * 4
+    # 1024 tokens at K = 14336: two M-blocks of 256 tokens with a split of two (128 CTAs) instead of 128
+    # CTAs of 128-token tiles running 224 k-steps each
+    assert ws(1024, 14336, 4096) == counters + 2 * 1024 * 4096 * 4
     # under a wave with one M-block: the largest split that stays within one wave (32 x 4 CTAs)
     assert ws(64, 4096, 4096) == counters + 4 * 64 * 4096 * 4
     # a full wave without splitting
