@@ -712,22 +712,24 @@ int fill_split(int64_t tiles, int total_k, int min_slice) {
   return sp;
 }
 
-// Modelled time (us) of a W4A16 call: waves of one CTA per SM, each running its K slice at a per-k-step
+// Modelled time (us) of a GEMM call: waves of one CTA per SM, each running its K slice at a per-k-step
 // time that grows with the tile (128-column M-blocks x token tile), plus a fixed cost and, with a K
-// split, the partials' reduction, which grows with the bytes each tile's last CTA reads.  The constants
-// are a least-squares fit to timings of every (token tile, M-blocks, split) plan on the prefill and
-// crossover shapes (K = 4096 / 14336, N = 4096 .. 28672, 64 .. 4096 tokens) on GB300; the plan picked
-// by the fit was within 6.5 % of the best measured one on all of them.
+// split, the partials' reduction: a term that grows with the bytes each tile's last CTA reads, and the
+// partials' DRAM time (written and read once at 6 TB/s).  The constants are a least-squares fit to
+// timings of every (token tile, M-blocks, split) plan on the prefill and crossover shapes (K = 4096 /
+// 14336, N = 4096 .. 28672, 64 .. 4096 tokens) on GB300; the plan picked by the fit was within 6.5 % of
+// the best measured one on all of them, and picked the best measured plan for per-channel W4A8
+// (K = 21760, N = 8192) at 256, 1024 and 4096 tokens.
 double gemm_plan_cost(int64_t M, int64_t N, int total, int bt, int nb, int split) {
   const int ks = (total + split - 1) / split;
   const int sp = (total + ks - 1) / ks;
   const int64_t tiles = ((N + (int64_t)nb * kBN - 1) / ((int64_t)nb * kBN)) * ((M + bt - 1) / bt);
   const int64_t waves = (tiles * sp + 151) / 152;
-  double step = 0.363;  // 64 tokens, one M-block
-  if (bt == 128) step = nb == 2 ? 0.642 : 0.470;
-  if (bt == 256) step = nb == 2 ? 0.852 : 0.593;
-  double t = (double)waves * ks * step + 8.25;
-  if (sp > 1) t += 11.30 + 9.42 * (sp - 1) * bt * nb / 512.0;
+  double step = 0.358;  // 64 tokens, one M-block
+  if (bt == 128) step = nb == 2 ? 0.603 : 0.451;
+  if (bt == 256) step = nb == 2 ? 0.804 : 0.560;
+  double t = (double)waves * ks * step + 10.31;
+  if (sp > 1) t += 7.43 + 7.05 * (sp - 1) * bt * nb / 512.0 + 2.0 * sp * (double)M * (double)N * 4.0 / 6.0e6;
   return t;
 }
 
@@ -784,12 +786,13 @@ GemmPlan gemm_plan(int64_t M, int64_t K, int64_t N, int split_k, int mode) {
   if (split < 1) split = 1;
   p.ksteps = (total + split - 1) / split;
   p.split = (total + p.ksteps - 1) / p.ksteps;
-  // W4A16 above 64 tokens with an automatic split: the plan that the measured cost model (below) rates at
-  // least 5 % faster replaces the one above.  Up to 64 tokens and for W4A8 (whose K slices the exact
-  // accumulators bound) the rules above stand.
+  // W4A16 and per-channel W4A8 above 64 tokens with an automatic split: the plan that the measured cost
+  // model (below) rates at least 5 % faster replaces the one above; for W4A8 only plans whose K slices
+  // keep the exact accumulators (16384 rows with two M-blocks, 2 x 16384 with one).  Up to 64 tokens and
+  // for W4A8 with group factors the rules above stand.
   const bool w4a16 = mode == kModeZeroPoint || mode == kModeSymmetric || mode == kModeZeroPointBF16 ||
                      mode == kModeSymmetricBF16;
-  if (w4a16 && split_k == 0 && M > 64) {
+  if ((w4a16 || mode == kModeW4A8) && split_k == 0 && M > 64) {
     const double cur = gemm_plan_cost(M, N, total, p.bt, p.nb, p.split);
     double best = cur;
     int bbt = p.bt, bnb = p.nb, bsp = p.split;
@@ -799,6 +802,11 @@ GemmPlan gemm_plan(int64_t M, int64_t K, int64_t N, int split_k, int mode) {
           if (total / sp < 8) break;
           const int64_t tl = tiles(bt, nb);
           if (sp > 1 && tl > kMaxCounters) break;
+          if (mode == kModeW4A8) {
+            const int64_t rows = (int64_t)((total + sp - 1) / sp) * kBK;
+            if (nb == 2 && (K > kW4A8MaxKSlice || rows > kW4A8MaxKSlice)) continue;
+            if (rows > 2 * kW4A8MaxKSlice) continue;
+          }
           const double c = gemm_plan_cost(M, N, total, bt, nb, sp);
           if (c < best) {
             best = c;

@@ -120,6 +120,10 @@ def test_workspace_layout(awq):
     x16 = 4096 * 21760 * 2
     assert awq.awq_workspace_bytes(awq.OP_W4A8_GEMM, 4096, 21760, 8192, 0) == counters + x16
     assert awq.awq_workspace_bytes(awq.OP_W4A8_GEMM, 16, 21760, 8192, 1) == counters + 16 * 21760 * 2
+    # 256 tokens: 256-token tiles with a K split of two (128 CTAs, slices of 10880 rows) are rated faster
+    # by the plan's cost model than 128-token tiles running all 21760 rows
+    assert awq.awq_workspace_bytes(awq.OP_W4A8_GEMM, 256, 21760, 8192, 0) == \
+        counters + 256 * 21760 * 2 + 2 * 256 * 8192 * 4
     # K beyond 2 x 16384 rows forces a K split across CTAs with int32 partials
     assert awq.awq_workspace_bytes(awq.OP_W4A8_GEMM, 4096, 40960, 8192, 1) == \
         counters + 4096 * 40960 * 2 + 2 * 4096 * 8192 * 4
