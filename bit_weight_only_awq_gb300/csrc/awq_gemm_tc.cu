@@ -786,13 +786,13 @@ GemmPlan gemm_plan(int64_t M, int64_t K, int64_t N, int split_k, int mode) {
   if (split < 1) split = 1;
   p.ksteps = (total + split - 1) / split;
   p.split = (total + p.ksteps - 1) / p.ksteps;
-  // W4A16 and per-channel W4A8 above 64 tokens with an automatic split: the plan that the measured cost
-  // model (below) rates at least 5 % faster replaces the one above; for W4A8 only plans whose K slices
-  // keep the exact accumulators (16384 rows with two M-blocks, 2 x 16384 with one).  Up to 64 tokens and
-  // for W4A8 with group factors the rules above stand.
+  // Above 64 tokens with an automatic split: the plan that the measured cost model (below) rates at
+  // least 5 % faster replaces the one above; for per-channel W4A8 only plans whose K slices keep the
+  // exact accumulators (16384 rows with two M-blocks, 2 x 16384 with one), with group factors only the
+  // chunk-draining tiles (128 or 256 tokens, one M-block).  Up to 64 tokens the rules above stand.
   const bool w4a16 = mode == kModeZeroPoint || mode == kModeSymmetric || mode == kModeZeroPointBF16 ||
                      mode == kModeSymmetricBF16;
-  if ((w4a16 || mode == kModeW4A8) && split_k == 0 && M > 64) {
+  if ((w4a16 || mode == kModeW4A8 || mode == kModeW4A8G) && split_k == 0 && M > 64) {
     const double cur = gemm_plan_cost(M, N, total, p.bt, p.nb, p.split);
     double best = cur;
     int bbt = p.bt, bnb = p.nb, bsp = p.split;
@@ -802,6 +802,7 @@ GemmPlan gemm_plan(int64_t M, int64_t K, int64_t N, int split_k, int mode) {
           if (total / sp < 8) break;
           const int64_t tl = tiles(bt, nb);
           if (sp > 1 && tl > kMaxCounters) break;
+          if (mode == kModeW4A8G && (bt < 128 || nb != 1)) continue;
           if (mode == kModeW4A8) {
             const int64_t rows = (int64_t)((total + sp - 1) / sp) * kBK;
             if (nb == 2 && (K > kW4A8MaxKSlice || rows > kW4A8MaxKSlice)) continue;

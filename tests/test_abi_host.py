@@ -136,6 +136,9 @@ def test_workspace_layout(awq):
     assert awq.awq_workspace_bytes(g, 64, 21760, 8192, 0) == counters + 64 * 21760 * 2 + 3 * 64 * 8192 * 4
     assert awq.awq_workspace_bytes(g, 1000, 21760, 8192, 0) == counters + align256(1000 * 21760 * 2)
     assert awq.awq_workspace_bytes(g, 4096, 21760, 8192, 0) == counters + 4096 * 21760 * 2
+    # 256 tokens: 256-token tiles with a K split of two (int32 partials) are rated faster by the plan's
+    # cost model than 128-token tiles running all 21760 rows
+    assert awq.awq_workspace_bytes(g, 256, 21760, 8192, 0) == counters + 256 * 21760 * 2 + 2 * 256 * 8192 * 4
     # invalid shapes need nothing (the compute call reports the error)
     assert awq.awq_workspace_bytes(awq.OP_GEMM, 16, 100, 4096, 0) == 0
 

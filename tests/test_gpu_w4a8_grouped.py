@@ -129,18 +129,19 @@ def test_w4a8_grouped_drained_chunks_256_token_tiles_sampled(awq, K, split_k):
     assert awq.awq_last_device_error() == 0
 
 
-@pytest.mark.parametrize("M", [256, 512])
-def test_w4a8_grouped_drained_extreme_chunks(awq, M):
+@pytest.mark.parametrize("M,split_k", [(256, 1), (256, 0), (512, 1)])
+def test_w4a8_grouped_drained_extreme_chunks(awq, M, split_k):
     # every 1024-row chunk sums to exactly 2^24 in its fp32 accumulator (codes -128 against weights
     # (0 - 8) * 16), and the drained int32 sums reach 21760 * 2^14 = 356 million: over 7424 columns, 256
-    # tokens take 128-token tiles (two accumulators), 512 tokens 256-token tiles (one)
+    # tokens without a split take 128-token tiles (two accumulators), with the automatic plan 256-token
+    # tiles and a K split of two; 512 tokens 256-token tiles (one accumulator)
     K, N = 21760, 7424
     xq = np.full((M, K), -128, dtype=np.int8)
     xq[1::3, 1::2] = 127
     wq = np.zeros((K, N // 8), dtype=np.int32)
     p = {"x": np.zeros((M, K), np.float16), "wq": wq, "s3": np.full((K // 128, N), 16, np.float16),
          "s2": np.full(N, 1e-6, np.float16)}
-    _, s, y, acc = run(awq, p, 0, xq=xq)
+    _, s, y, acc = run(awq, p, split_k, xq=xq)
     wc = np.array([0, 17, N // 8 - 1])
     cols = (8 * wc[:, None] + np.arange(8)[None, :]).ravel()
     want_y, want_acc = oracle.w4a8_group_linear(xq, s, wq[:, wc], p["s3"][:, cols], p["s2"][cols], 128)
