@@ -751,8 +751,9 @@ GemmPlan gemm_plan(int64_t M, int64_t K, int64_t N, int split_k, int mode) {
   // memory (512 / 64 = 8); 128 and 256 tokens drain their chunks during the main loop
   // >= 128-token tiles: 256 weight columns per CTA (two M-blocks on one activation tile) whenever that
   // still fills about a wave.  W4A8 then has one exact accumulator per M-block, which holds K slices of
-  // at most 16384 rows: taken only when K fits one slice (at K = 21760 and 4096 tokens, two M-blocks
-  // with a K split of two measured 1375 us against 1150 us for one M-block with two accumulators)
+  // at most 16384 rows: taken here only when K fits one slice (the cost model below may still choose two
+  // M-blocks with a K split: at K = 21760 and 4096 tokens that measured 1132 us against 1263 us for one
+  // M-block with two accumulators)
   if (bt0 >= 128 && mode != kModeW4A8G && (mode != kModeW4A8 || K <= kW4A8MaxKSlice)) {
     int bt = bt0;
     while (bt > 128 && tiles(bt, 2) < 114) bt /= 2;
@@ -805,7 +806,7 @@ GemmPlan gemm_plan(int64_t M, int64_t K, int64_t N, int split_k, int mode) {
           if (mode == kModeW4A8G && (bt < 128 || nb != 1)) continue;
           if (mode == kModeW4A8) {
             const int64_t rows = (int64_t)((total + sp - 1) / sp) * kBK;
-            if (nb == 2 && (K > kW4A8MaxKSlice || rows > kW4A8MaxKSlice)) continue;
+            if (nb == 2 && rows > kW4A8MaxKSlice) continue;
             if (rows > 2 * kW4A8MaxKSlice) continue;
           }
           const double c = gemm_plan_cost(M, N, total, bt, nb, sp);

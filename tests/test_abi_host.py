@@ -115,15 +115,16 @@ def test_workspace_layout(awq):
     assert awq.awq_workspace_bytes(awq.OP_GEMV, 8, 4096, 4096, 4) == counters + 4 * 8 * 4096 * 4
     # 9..16 tokens: partials carry 16 token rows
     assert awq.awq_workspace_bytes(awq.OP_GEMV, 12, 4096, 4096, 4) == counters + 4 * 16 * 4096 * 4
-    # W4A8 at K = 21760: one M-block per CTA with two exact accumulators (16384 rows each) covers K
-    # without a split
+    # W4A8 at K = 21760 and 4096 tokens: two M-blocks per CTA (one exact accumulator each) with a K split
+    # of two (slices of 10880 rows), which the plan's cost model rates faster than one M-block covering
+    # K with its two accumulators
     x16 = 4096 * 21760 * 2
-    assert awq.awq_workspace_bytes(awq.OP_W4A8_GEMM, 4096, 21760, 8192, 0) == counters + x16
+    assert awq.awq_workspace_bytes(awq.OP_W4A8_GEMM, 4096, 21760, 8192, 0) == counters + x16 + 2 * 4096 * 8192 * 4
     assert awq.awq_workspace_bytes(awq.OP_W4A8_GEMM, 16, 21760, 8192, 1) == counters + 16 * 21760 * 2
-    # 256 tokens: 256-token tiles with a K split of two (128 CTAs, slices of 10880 rows) are rated faster
-    # by the plan's cost model than 128-token tiles running all 21760 rows
+    # 256 tokens: 256-token tiles with two M-blocks and a K split of four (128 CTAs, slices of 5440 rows)
+    # are rated faster by the plan's cost model than 128-token tiles running all 21760 rows
     assert awq.awq_workspace_bytes(awq.OP_W4A8_GEMM, 256, 21760, 8192, 0) == \
-        counters + 256 * 21760 * 2 + 2 * 256 * 8192 * 4
+        counters + 256 * 21760 * 2 + 4 * 256 * 8192 * 4
     # K beyond 2 x 16384 rows forces a K split across CTAs with int32 partials
     assert awq.awq_workspace_bytes(awq.OP_W4A8_GEMM, 4096, 40960, 8192, 1) == \
         counters + 4096 * 40960 * 2 + 2 * 4096 * 8192 * 4
