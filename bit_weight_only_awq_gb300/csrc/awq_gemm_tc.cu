@@ -670,6 +670,7 @@ cudaError_t launch_mode(const uint16_t* x16, const uint32_t* qw, const uint32_t*
     constexpr int M2 = MODE == kModeW4A8 ? kModeW4A8One : MODE;
     if (MODE == kModeW4A8 && p.ksteps * kBK > kW4A8MaxKSlice) return cudaErrorInvalidValue;
     switch (p.bt) {
+      case 64: return launch_t<64, 2, M2>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters, err, s);
       case 128: return launch_t<128, 2, M2>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters, err, s);
       case 256: return launch_t<256, 2, M2>(x16, qw, qz, sc, s_tok, s_ch, y, acc_out, M, K, N, p, part, counters, err, s);
       default: return cudaErrorInvalidValue;
@@ -719,13 +720,14 @@ int fill_split(int64_t tiles, int total_k, int min_slice) {
 // timings of every (token tile, M-blocks, split) plan on the prefill and crossover shapes (K = 4096 /
 // 14336, N = 4096 .. 28672, 64 .. 4096 tokens) on GB300; the plan picked by the fit was within 6.5 % of
 // the best measured one on all of them, and picked the best measured plan for per-channel W4A8
-// (K = 21760, N = 8192) at 256, 1024 and 4096 tokens.
+// (K = 21760, N = 8192) at 256, 1024 and 4096 tokens.  The step of 64-token tiles with two M-blocks
+// (0.62 us) was measured separately (gate_up, 64 tokens, one wave).
 double gemm_plan_cost(int64_t M, int64_t N, int total, int bt, int nb, int split) {
   const int ks = (total + split - 1) / split;
   const int sp = (total + ks - 1) / ks;
   const int64_t tiles = ((N + (int64_t)nb * kBN - 1) / ((int64_t)nb * kBN)) * ((M + bt - 1) / bt);
   const int64_t waves = (tiles * sp + 151) / 152;
-  double step = 0.358;  // 64 tokens, one M-block
+  double step = nb == 2 ? 0.62 : 0.358;  // 64 tokens
   if (bt == 128) step = nb == 2 ? 0.603 : 0.451;
   if (bt == 256) step = nb == 2 ? 0.804 : 0.560;
   double t = (double)waves * ks * step + 10.31;
@@ -790,15 +792,16 @@ GemmPlan gemm_plan(int64_t M, int64_t K, int64_t N, int split_k, int mode) {
   // Above 64 tokens with an automatic split: the plan that the measured cost model (below) rates at
   // least 5 % faster replaces the one above; for per-channel W4A8 only plans whose K slices keep the
   // exact accumulators (16384 rows with two M-blocks, 2 x 16384 with one), with group factors only the
-  // chunk-draining tiles (128 or 256 tokens, one M-block).  Up to 64 tokens the rules above stand.
+  // chunk-draining tiles (128 or 256 tokens, one M-block).  Up to 32 tokens the rules above stand (the
+  // model knows tiles of 64 tokens and more).
   const bool w4a16 = mode == kModeZeroPoint || mode == kModeSymmetric || mode == kModeZeroPointBF16 ||
                      mode == kModeSymmetricBF16;
-  if ((w4a16 || mode == kModeW4A8 || mode == kModeW4A8G) && split_k == 0 && M > 64) {
+  if ((w4a16 || mode == kModeW4A8 || mode == kModeW4A8G) && split_k == 0 && M > 32) {
     const double cur = gemm_plan_cost(M, N, total, p.bt, p.nb, p.split);
     double best = cur;
     int bbt = p.bt, bnb = p.nb, bsp = p.split;
     for (int bt = 64; bt <= bt0; bt *= 2)
-      for (int nb = 1; nb <= (bt >= 128 ? 2 : 1); ++nb)
+      for (int nb = 1; nb <= 2; ++nb)
         for (int sp = 1; sp <= 8; ++sp) {
           if (total / sp < 8) break;
           const int64_t tl = tiles(bt, nb);
