@@ -26,7 +26,8 @@
 //  * Warp roles: warp 0 copies activations, warp 2 copies packed weights (TMA), warp 1
 //    owns tensor memory and issues tcgen05.mma (one thread), warps 3..18 dequantize in
 //    two groups of eight that take alternate k-steps, and the first group then runs the
-//    epilogue (tcgen05.ld -> fp16 / int32 -> global).  Rings are chained by mbarriers;
+//    epilogue (tcgen05.ld -> fp16 staged in the idle rings -> one TMA tensor store per
+//    M-block; int32 partials go out with plain stores).  Rings are chained by mbarriers;
 //    every wait is bounded in time and records an error id instead of hanging.
 //  * split > 1: each K slice writes fp32 (W4A16) or int32 (W4A8) partials; the last
 //    CTA of an output tile (atomic ticket) sums them in slice order.
@@ -119,6 +120,8 @@ struct Cfg {
                                      ((uint32_t)(kBN >> 4) << 24);
   static_assert(kXStages >= 2 * kXSub, "activation ring");
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
+  // the epilogue stages each M-block's output tile ([token][128 columns], 16-bit) in the idle rings
+  static_assert(kXStages * kXSlotBytes + kWStages * kWBytes >= NB * BT * kBN * 2, "output staging");
   static_assert(kTmemCols <= 512, "tensor memory");
   static_assert(!kDrain || kSumCol + BT <= kTmemCols, "drain layout");
   static_assert(kDrainLag % 2 == 0, "the two dequant groups drain at one even and the next odd k-step");
@@ -182,6 +185,7 @@ template <int BT, int NB, int MODE>
 __global__ void __launch_bounds__(Cfg<BT, NB, MODE>::kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_q,
             const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_s,
+            const __grid_constant__ CUtensorMap tm_y,
             __half* __restrict__ y, int32_t* __restrict__ acc_out, const float* __restrict__ s_tok,
             const __half* __restrict__ s_ch, void* __restrict__ part, int* __restrict__ counters,
             int* __restrict__ err, int M, int N, int K, int ksteps_per_split, int chunk_steps, int m_tiles,
@@ -499,6 +503,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     constexpr int kHalf = BT / 2;
     float sch = 0.f;
     if (kIsW4A8<MODE> && n_ok) sch = __half2float(s_ch[n]);
+    // without a K split the outputs are staged in the idle rings, [token][128 columns] per M-block, for
+    // one tensor store per M-block
+    __half* stg = reinterpret_cast<__half*>(xring) + (size_t)group * BT * kBN;
     if (have) {
 #pragma unroll 1
       for (int cb = half * kHalf; cb < (half + 1) * kHalf; cb += 8) {
@@ -534,21 +541,32 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const int m = m0 + cb + j;
-          if (!n_ok || m >= M) continue;
+          const bool in = n_ok && m < M;
           const size_t o = (size_t)m * N + n;
-          if (kIsW4A8<MODE>) {
-            const int a = vi[j];
-            if (split == 1) {
-              if (acc_out) __stcs(acc_out + o, a);
-              __stcs(y + o, __float2half_rn(__fmul_rn(__fmul_rn((float)a, s_tok[m]), sch)));
+          if (split == 1) {
+            __half hv;  // rows and columns beyond the tensor are staged too; the tensor store clips them
+            if constexpr (kIsW4A8<MODE>) {
+              if (acc_out && in) __stcs(acc_out + o, vi[j]);
+              hv = __float2half_rn(in ? __fmul_rn(__fmul_rn((float)vi[j], s_tok[m]), sch) : 0.f);
             } else {
-              reinterpret_cast<int32_t*>(part)[(size_t)blockIdx.z * M * N + o] = a;
+              hv = out_cvt<MODE>(v[j]);
             }
-          } else {
-            if (split == 1) __stcs(y + o, out_cvt<MODE>(v[j]));
+            stg[(cb + j) * kBN + nl] = hv;
+          } else if (in) {
+            if constexpr (kIsW4A8<MODE>) reinterpret_cast<int32_t*>(part)[(size_t)blockIdx.z * M * N + o] = vi[j];
             else reinterpret_cast<float*>(part)[(size_t)blockIdx.z * M * N + o] = v[j];
           }
         }
+      }
+    }
+    if (split == 1) {
+      // this group's tile out in one tensor store, after its staging writes are visible to the async proxy
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      asm volatile("bar.sync %0, %1;" ::"r"(2 + group), "r"(kDqGroupWarps * 32) : "memory");
+      if (d == 0 && have) {
+        tma_store_2d(&tm_y, smem_u32(stg), n0 + group * kBN, m0);
+        bulk_commit();
+        bulk_wait_read0();  // the staged tile has been read before this thread reaches the exit barrier
       }
     }
     if (split > 1) {
@@ -622,7 +640,7 @@ cudaError_t launch_t(const uint16_t* x16, const uint32_t* qw, const uint32_t* qz
                      cudaStream_t s) {
   using C = Cfg<BT, NB, MODE>;
   constexpr int kQWords = C::kQWords;
-  CUtensorMap tx, tq, tz, ts;
+  CUtensorMap tx, tq, tz, ts, ty;
   const uint64_t nw = (uint64_t)N / 8, ng = (uint64_t)K / kGroup;
   constexpr CUtensorMapDataType kHalfType = kIsBF16<MODE> ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                           : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
@@ -638,6 +656,8 @@ cudaError_t launch_t(const uint16_t* x16, const uint32_t* qw, const uint32_t* qz
                                 CU_TENSOR_MAP_SWIZZLE_NONE)
                   : make_map_2d(&ts, kHalfType, 2, sc, (uint64_t)N, ng, NB * kBN, 1,
                                 CU_TENSOR_MAP_SWIZZLE_NONE));
+  // output map: [M, N] 16-bit, boxes of one M-block's 128 columns x BT tokens (the epilogue's tensor stores)
+  ok = ok && make_map_2d(&ty, kHalfType, 2, y, (uint64_t)N, (uint64_t)M, kBN, BT, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (!ok) return cudaErrorInvalidValue;
   auto kern = gemm_kernel<BT, NB, MODE>;
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), C::kSmem);
@@ -652,7 +672,7 @@ cudaError_t launch_t(const uint16_t* x16, const uint32_t* qw, const uint32_t* qz
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, kern, tx, tq, tz, ts, reinterpret_cast<__half*>(y), acc_out, s_tok,
+  e = cudaLaunchKernelEx(&cfg, kern, tx, tq, tz, ts, ty, reinterpret_cast<__half*>(y), acc_out, s_tok,
                          reinterpret_cast<const __half*>(s_ch), part, counters, err, (int)M, (int)N, (int)K,
                          p.ksteps, (MODE == kModeW4A8G ? kW4A8GroupChunk : kW4A8MaxKSlice) / kBK, p.m_tiles,
                          p.band);
