@@ -422,16 +422,6 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
       return true;
     };
     for (int it = (C::kSoloMma && warp % 4 == 1) ? nsteps : group; it < nsteps; it += kDqGroups) {
-      if constexpr (C::kDrain) {
-        // chunk ch is drained by group 0 at k-step (ch + 1) chunk_steps + kDrainLag and by group 1 one
-        // later (with one accumulator, at the first two k-steps of the next chunk, whose mmas wait for it)
-        const int rel = it - C::kDrainLag - group;
-        if (rel >= chunk_steps && rel % chunk_steps == 0 && rel / chunk_steps - 1 == next_drain &&
-            next_drain < n_chunks - 1) {
-          if (!drain(next_drain)) break;
-          ++next_drain;
-        }
-      }
       const int qs = it % kQStages, ws = it % kWStages;
       if (!wait_bounded(fullq(qs), (uint32_t)(it / kQStages) & 1u, abort_flag, err, 301)) break;
       if (!wait_bounded(wempty(ws), ((uint32_t)(it / kWStages) & 1u) ^ 1u, abort_flag, err, 302)) break;
@@ -476,6 +466,17 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
       if (lane == 0) mbar_arrive(wready(ws));
+      if constexpr (C::kDrain) {
+        // chunk ch is drained by group 0 after it has dequantized k-step (ch + 1) chunk_steps + kDrainLag
+        // and by group 1 after the step that follows (with one accumulator: after the first two k-steps
+        // of the next chunk, whose mmas wait for the drain; their weights are then already in the ring)
+        const int rel = it - C::kDrainLag - group;
+        if (rel >= chunk_steps && rel % chunk_steps == 0 && rel / chunk_steps - 1 == next_drain &&
+            next_drain < n_chunks - 1) {
+          if (!drain(next_drain)) break;
+          ++next_drain;
+        }
+      }
     }
     // drain mode: chunks whose drain step this warp's group never reached
     if constexpr (C::kDrain)
