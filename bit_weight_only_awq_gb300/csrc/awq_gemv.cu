@@ -333,28 +333,28 @@ __device__ __forceinline__ void compute_stage_exact(const StageRegs<T>& sr, cons
         for (int b = 0; b < 4; ++b)
           mma16816_bf16(acc[h][b], a[b][0], a[b][1], a[b][2], a[b][3], sr.b[h][it][0], sr.b[h][it][1]);
     }
-    return;
-  }
+  } else {
 #pragma unroll
-  for (int it = 0; it < 4; ++it) {
-    uint32_t p01[4], p23[4], a[4][4];
+    for (int it = 0; it < 4; ++it) {
+      uint32_t p01[4], p23[4], a[4][4];
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      p01[b] = prmt(sr.r[it][0], sr.r[it][1], byte_sel(b));
-      p23[b] = prmt(sr.r[it][2], sr.r[it][3], byte_sel(b));
+      for (int b = 0; b < 4; ++b) {
+        p01[b] = prmt(sr.r[it][0], sr.r[it][1], byte_sel(b));
+        p23[b] = prmt(sr.r[it][2], sr.r[it][3], byte_sel(b));
+      }
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        a[b][0] = hmul2(hsub2(magic<0x000F000Fu>(p01[b]), c.zlo[b]), c.slo[b]);
+        a[b][1] = hmul2(hsub2(magic<0x00F000F0u>(p01[b]), c.zhi[b]), c.shi[b]);
+        a[b][2] = hmul2(hsub2(magic<0x000F000Fu>(p23[b]), c.zlo[b]), c.slo[b]);
+        a[b][3] = hmul2(hsub2(magic<0x00F000F0u>(p23[b]), c.zhi[b]), c.shi[b]);
+      }
+#pragma unroll
+      for (int h = 0; h < T / 8; ++h)
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+          mma16816(acc[h][b], a[b][0], a[b][1], a[b][2], a[b][3], sr.b[h][it][0], sr.b[h][it][1]);
     }
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      a[b][0] = hmul2(hsub2(magic<0x000F000Fu>(p01[b]), c.zlo[b]), c.slo[b]);
-      a[b][1] = hmul2(hsub2(magic<0x00F000F0u>(p01[b]), c.zhi[b]), c.shi[b]);
-      a[b][2] = hmul2(hsub2(magic<0x000F000Fu>(p23[b]), c.zlo[b]), c.slo[b]);
-      a[b][3] = hmul2(hsub2(magic<0x00F000F0u>(p23[b]), c.zhi[b]), c.shi[b]);
-    }
-#pragma unroll
-    for (int h = 0; h < T / 8; ++h)
-#pragma unroll
-      for (int b = 0; b < 4; ++b)
-        mma16816(acc[h][b], a[b][0], a[b][1], a[b][2], a[b][3], sr.b[h][it][0], sr.b[h][it][1]);
   }
 }
 
