@@ -16,15 +16,16 @@ namespace {
 constexpr int kQThreads = 256;
 constexpr int kQ1MaxK = 32768;  // rows up to this length are held in shared memory (64 KB)
 
-// code = rint(x / s) for s > 0, clamped to [-128, 127], with the IEEE fp32 quotient of the pages' script.
-// x * (1 / s) differs from the correctly rounded quotient by at most a few ulp, which can change the
-// rounded integer only next to a half-integer; there the quotient is taken exactly.
-__device__ __forceinline__ uint32_t code_of(float xv, float s, float inv) {
+// code = rint(x / s) for s > 0, clamped to [-128, 127], with the IEEE fp32 quotient of the pages'
+// script, as a float (an integer).  x * (1 / s) differs from the correctly rounded quotient by at most
+// a few ulp, which can change the rounded integer only next to a half-integer: where the product lies
+// within 1e-4 of one (|r - rint(r)| within 1e-4 of 0.5; the difference is exact in fp32) the quotient
+// is taken exactly.
+__device__ __forceinline__ float code_value(float xv, float s, float inv) {
   const float r = xv * inv;
-  const float f = r - floorf(r);
-  float q = fabsf(f - 0.5f) < 1.0e-4f ? rintf(__fdiv_rn(xv, s)) : rintf(r);
-  q = fminf(fmaxf(q, -128.f), 127.f);
-  return (uint32_t)(int)q & 0xFFu;
+  float q = rintf(r);
+  if (fabsf(fabsf(r - q) - 0.5f) < 1.0e-4f) q = rintf(__fdiv_rn(xv, s));
+  return fminf(fmaxf(q, -128.f), 127.f);
 }
 
 // The eight codes of one 16-byte activation vector: as int8 into xq (when given) and widened to fp16
@@ -57,17 +58,18 @@ quant_act_smem_kernel(const __half* __restrict__ x, int8_t* __restrict__ xq, flo
   const int64_t r = blockIdx.x;
   const uint4* xr = reinterpret_cast<const uint4*>(x + r * (int64_t)K);
   const int nvec = K / 8;
-  uint32_t mx = 0;  // |x| as fp16 bits: integer order equals magnitude order for finite values
+  // |x| as fp16 bits, two per word (integer order equals magnitude order for finite values)
+  uint32_t mx2 = 0;
+#pragma unroll 4
   for (int i = threadIdx.x; i < nvec; i += kQThreads) {
     const uint4 v = __ldcs(xr + i);
     row[i] = v;
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      mx = max(mx, w[j] & 0x7FFFu);
-      mx = max(mx, (w[j] >> 16) & 0x7FFFu);
-    }
+    mx2 = __vmaxu2(mx2, v.x & 0x7FFF7FFFu);
+    mx2 = __vmaxu2(mx2, v.y & 0x7FFF7FFFu);
+    mx2 = __vmaxu2(mx2, v.z & 0x7FFF7FFFu);
+    mx2 = __vmaxu2(mx2, v.w & 0x7FFF7FFFu);
   }
+  uint32_t mx = max(mx2 & 0xFFFFu, mx2 >> 16);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
   if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = mx;
@@ -83,18 +85,32 @@ quant_act_smem_kernel(const __half* __restrict__ x, int8_t* __restrict__ xq, flo
   __syncthreads();
   const float s = s_shared;
   const float inv = s > 0.f ? __frcp_rn(s) : 0.f;
+#pragma unroll 2
   for (int i = threadIdx.x; i < nvec; i += kQThreads) {
     const uint4 v = row[i];
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t out[2] = {0, 0};
-    if (s > 0.f) {
+    float q[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float xv = __half2float(__ushort_as_half((unsigned short)(w[j >> 1] >> (16 * (j & 1)))));
-        out[j >> 2] |= code_of(xv, s, inv) << (8 * (j & 3));
-      }
+    for (int p = 0; p < 4; ++p) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[p]));
+      q[2 * p] = s > 0.f ? code_value(f.x, s, inv) : 0.f;
+      q[2 * p + 1] = s > 0.f ? code_value(f.y, s, inv) : 0.f;
     }
-    store_codes(out, xq, x16, r, K, i);
+    if (x16) {  // integers of at most 8 bits: exact in fp16
+      uint32_t h[4];
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        const __half2 hv = __floats2half2_rn(q[2 * p], q[2 * p + 1]);
+        h[p] = *reinterpret_cast<const uint32_t*>(&hv);
+      }
+      reinterpret_cast<uint4*>(x16 + r * (int64_t)K)[i] = make_uint4(h[0], h[1], h[2], h[3]);
+    }
+    if (xq) {
+      uint32_t out[2] = {0, 0};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) out[j >> 2] |= ((uint32_t)(int)q[j] & 0xFFu) << (8 * (j & 3));
+      reinterpret_cast<uint2*>(xq + r * (int64_t)K)[i] = make_uint2(out[0], out[1]);
+    }
   }
 }
 
