@@ -45,15 +45,17 @@ __device__ __forceinline__ void store_codes(const uint32_t (&out)[2], int8_t* xq
 }
 
 // One CTA per token row, the row read from DRAM once: it is kept in shared memory between the absmax
-// pass and the coding pass.
-__global__ void __launch_bounds__(kQThreads)
+// pass and the coding pass.  T threads: 1024 when the rows are too few to fill the GPU (more of a
+// row's loads in flight per CTA), 256 otherwise (more rows per SM).
+template <int T>
+__global__ void __launch_bounds__(T)
 quant_act_smem_kernel(const __half* __restrict__ x, int8_t* __restrict__ xq, float* __restrict__ s_tok,
                       __half* __restrict__ x16, int K) {
   // the GEMM that reads these codes is launched as a programmatic dependent: it may start its setup
   // and weight stream now and waits for this grid to complete before it reads them
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   extern __shared__ uint4 row[];
-  __shared__ uint32_t warp_max[kQThreads / 32];
+  __shared__ uint32_t warp_max[T / 32];
   __shared__ float s_shared;
   const int64_t r = blockIdx.x;
   const uint4* xr = reinterpret_cast<const uint4*>(x + r * (int64_t)K);
@@ -61,7 +63,7 @@ quant_act_smem_kernel(const __half* __restrict__ x, int8_t* __restrict__ xq, flo
   // |x| as fp16 bits, two per word (integer order equals magnitude order for finite values)
   uint32_t mx2 = 0;
 #pragma unroll 4
-  for (int i = threadIdx.x; i < nvec; i += kQThreads) {
+  for (int i = threadIdx.x; i < nvec; i += T) {
     const uint4 v = __ldcs(xr + i);
     row[i] = v;
     mx2 = __vmaxu2(mx2, v.x & 0x7FFF7FFFu);
@@ -76,7 +78,7 @@ quant_act_smem_kernel(const __half* __restrict__ x, int8_t* __restrict__ xq, flo
   __syncthreads();
   if (threadIdx.x == 0) {
     uint32_t m = 0;
-    for (int w = 0; w < kQThreads / 32; ++w) m = max(m, warp_max[w]);
+    for (int w = 0; w < T / 32; ++w) m = max(m, warp_max[w]);
     const float absmax = __half2float(__ushort_as_half((unsigned short)m));
     const float s = __half2float(__float2half_rn(__fdiv_rn(absmax, 127.0f)));
     s_shared = s;
@@ -86,7 +88,7 @@ quant_act_smem_kernel(const __half* __restrict__ x, int8_t* __restrict__ xq, flo
   const float s = s_shared;
   const float inv = s > 0.f ? __frcp_rn(s) : 0.f;
 #pragma unroll 2
-  for (int i = threadIdx.x; i < nvec; i += kQThreads) {
+  for (int i = threadIdx.x; i < nvec; i += T) {
     const uint4 v = row[i];
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     float q[8];
@@ -190,12 +192,19 @@ cudaError_t launch_quant_act(const uint16_t* x, int8_t* xq, float* s_tok, int64_
   if (M == 0) return cudaSuccess;
   if (K <= kQ1MaxK) {
     const int smem = (int)K * 2;
+    const bool wide = M <= 2 * (int64_t)device_sm_count();  // two 1024-thread CTAs fit one SM
+    const void* fn = wide ? reinterpret_cast<const void*>(quant_act_smem_kernel<1024>)
+                          : reinterpret_cast<const void*>(quant_act_smem_kernel<kQThreads>);
     if (smem > 48 * 1024) {
-      const cudaError_t e = set_smem_once(reinterpret_cast<const void*>(quant_act_smem_kernel), kQ1MaxK * 2);
+      const cudaError_t e = set_smem_once(fn, kQ1MaxK * 2);
       if (e != cudaSuccess) return e;
     }
-    quant_act_smem_kernel<<<(unsigned)M, kQThreads, smem, s>>>(reinterpret_cast<const __half*>(x), xq, s_tok,
-                                                               reinterpret_cast<__half*>(x16), (int)K);
+    if (wide)
+      quant_act_smem_kernel<1024><<<(unsigned)M, 1024, smem, s>>>(reinterpret_cast<const __half*>(x), xq, s_tok,
+                                                                   reinterpret_cast<__half*>(x16), (int)K);
+    else
+      quant_act_smem_kernel<kQThreads><<<(unsigned)M, kQThreads, smem, s>>>(
+          reinterpret_cast<const __half*>(x), xq, s_tok, reinterpret_cast<__half*>(x16), (int)K);
   } else {
     quant_act_kernel<<<(unsigned)M, kQThreads, 0, s>>>(reinterpret_cast<const __half*>(x), xq, s_tok,
                                                        reinterpret_cast<__half*>(x16), (int)K);
