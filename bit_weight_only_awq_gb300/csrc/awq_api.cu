@@ -162,14 +162,14 @@ static bool gemm_shape_ok(int64_t M, int64_t K, int64_t N, int32_t split_k) {
          N % 32 == 0 && N <= (int64_t)1 << 30 && split_k >= 0 && M * N < ((int64_t)1 << 40);
 }
 
-// W4A8 with at most 16 tokens runs on the 16-token GEMV (exact products, int32 reduction) when its plan
+// W4A8 with at most 16 tokens runs on the GEMV (exact products, int32 reduction) when its plan
 // keeps every CTA's rows of a tile within 16384; otherwise, and for more tokens, on the GEMM.
 static bool w4a8_on_gemv(int64_t M, int64_t K, int64_t N, int32_t split_k, GemvPlan* plan) {
   if (M < 1 || M > kGemvMaxM) return false;
   *plan = gemv_plan(M, K, N, split_k);
   return gemv_w4a8_ok(*plan, M);
 }
-// counters | fp16 copy of the codes | GEMV partials (16 token rows per slot)
+// counters | fp16 copy of the codes | GEMV partials (16 token rows per slot; the 8-token instance uses 8)
 static size_t w4a8_gemv_workspace_bytes(const GemvPlan& p, int64_t M, int64_t K, int64_t N) {
   const size_t part = gemv_workspace_bytes(p, 16, N);
   return kCounterBytes + align256((size_t)M * (size_t)K * 2) + (part ? part - kCounterBytes : 0);

@@ -433,7 +433,7 @@ struct StageWalk {
 constexpr int kMaxRegs = (65536 / 4) / (((kThreads / 32 + 3) / 4) * 32) / 8 * 8;
 static_assert(kMaxRegs == 168, "9 warps: three on one sub-partition");
 
-// EXACT (16 tokens only): the W4A8 product.  x holds int8 codes widened to fp16, the weights are
+// EXACT (8- or 16-token instance): the W4A8 product.  x holds int8 codes widened to fp16, the weights are
 // u - 8 with u the packed nibble (the symmetric zero point, unit scales), so every product and every
 // fp32 partial sum is an exact integer (the host keeps a CTA's rows of a tile at or below 16384, so
 // |sum| <= 1024 * 16384 = 2^24); partials are added as int32 and the output is
@@ -446,11 +446,12 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             __half* __restrict__ y, float* __restrict__ part, int* __restrict__ counters, int* __restrict__ err,
             int M, int N, int RB, int tiles, int maxc, const float* __restrict__ s_tok,
             const __half* __restrict__ s_ch, int32_t* __restrict__ acc_out) {
-  static_assert(!EXACT || T == 16, "the exact product uses the 16-token instance");
+  static_assert(!EXACT || T == 8 || T == 16, "the exact product has an 8- and a 16-token instance");
   static_assert(!BF16 || !EXACT, "the bf16 variant is a W4A16 instance");
   // fp16 with up to 8 tokens folds zero point and scale into the fp32 sums; the others make every
-  // weight exactly (bf16 keeps exact weights at 8 tokens too: its 8-bit weights would not fit the fold)
-  constexpr bool kFold = T == 8 && !BF16;
+  // weight exactly (bf16 keeps exact weights at 8 tokens too: its 8-bit weights would not fit the fold;
+  // the W4A8 product needs its weights u - 8 exactly)
+  constexpr bool kFold = T == 8 && !BF16 && !EXACT;
   // RB = K / 64 row blocks per tile; unit u = (tile u / RB, row block u % RB); units < 2^31 (host check)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = align_smem_1024(smem_raw);
@@ -979,9 +980,11 @@ cudaError_t launch_gemv_w4a8(const uint16_t* x16, const uint32_t* wq, const floa
                              uint16_t* y, int32_t* acc_out, int64_t M, int64_t K, int64_t N, const GemvPlan& p,
                              void* ws, int* err, cudaStream_t s) {
   if ((int64_t)p.tiles * p.groups >= ((int64_t)1 << 31) || !gemv_w4a8_ok(p, M)) return cudaErrorInvalidValue;
-  // workspace: counters | x16 (the caller's) | partials
-  return launch_gemv_t<16, true>(x16, wq, nullptr, nullptr, y, M, K, N, p, ws, err, s, s_tok, s_ch, acc_out,
-                                 align256((size_t)M * (size_t)K * 2));
+  // workspace: counters | x16 (the caller's) | partials (sized for 16 token rows; up to 8 tokens the
+  // 8-token instance, with half the mma work per stage, uses half of each slot)
+  const size_t off = align256((size_t)M * (size_t)K * 2);
+  if (M <= 8) return launch_gemv_t<8, true>(x16, wq, nullptr, nullptr, y, M, K, N, p, ws, err, s, s_tok, s_ch, acc_out, off);
+  return launch_gemv_t<16, true>(x16, wq, nullptr, nullptr, y, M, K, N, p, ws, err, s, s_tok, s_ch, acc_out, off);
 }
 
 }  // namespace awq

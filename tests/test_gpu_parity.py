@@ -352,10 +352,11 @@ def test_w4a8_linear_matches_two_calls(awq, M, K, N):
     assert np.array_equal(host(y_only).view(np.uint16), y2.view(np.uint16))
 
 
-@pytest.mark.parametrize("M", [1, 9, 16])
+@pytest.mark.parametrize("M", [1, 8, 9, 16])
 def test_w4a8_gemv_and_gemm_agree(awq, M):
-    # up to 16 tokens the automatic plan runs on the GEMV; split_k = 1 at K = 21760 gives one CTA per
-    # tile with more than 16384 rows, which the GEMV does not take, so that call runs on the GEMM
+    # up to 16 tokens the automatic plan runs on the GEMV (its 8-token instance up to 8 tokens, the
+    # 16-token one above); split_k = 1 at K = 21760 gives one CTA per tile with more than 16384 rows,
+    # which the GEMV does not take, so that call runs on the GEMM
     K, N = synth.W4A8_SHAPE
     p = synth.w4a8_problem(M, K, N, seed=700 + M)
     xq, s, y_v, acc_v = _w4a8_run(awq, p, split_k=0)
