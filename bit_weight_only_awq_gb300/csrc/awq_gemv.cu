@@ -449,9 +449,9 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
   static_assert(!EXACT || T == 8 || T == 16, "the exact product has an 8- and a 16-token instance");
   static_assert(!BF16 || !EXACT, "the bf16 variant is a W4A16 instance");
   // fp16 with up to 8 tokens folds zero point and scale into the fp32 sums; the others make every
-  // weight exactly (bf16 keeps exact weights at 8 tokens too: its 8-bit weights would not fit the fold;
-  // the W4A8 product needs its weights u - 8 exactly)
-  constexpr bool kFold = T == 8 && !BF16 && !EXACT;
+  // weight exactly (bf16 keeps exact weights at 8 tokens too: its 8-bit weights would not fit the fold).
+  // The 8-token W4A8 product folds as well, per 64-row stage, where every sum is an exact integer.
+  constexpr bool kFold = T == 8 && !BF16;
   // RB = K / 64 row blocks per tile; unit u = (tile u / RB, row block u % RB); units < 2^31 (host check)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = align_smem_1024(smem_raw);
@@ -618,11 +618,23 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
           if (lane == 0) mbar_arrive(empty_bar(st));  // slot free before the last unit's arithmetic
           compute_stage(sr, gacc, sx);
           // the group's zero point and scale: acc += s (gacc - (1024 + z) sx)  (high nibble: s / 16, 1024 + 16 z)
+          if constexpr (EXACT) {
+            // W4A8 (z = 8, s = 1): over the 64 rows |gacc| <= 64 * 1264 * 128 < 2^24 and |sx| <= 8192 are
+            // exact integers, gacc - (1024 + 8 or 1024 + 128) sx = sum (16) (u - 8) x comes out of one
+            // fused multiply-add exactly, and the power-of-two scale keeps it exact in acc
 #pragma unroll
-          for (int b = 0; b < 4; ++b)
+            for (int b = 0; b < 4; ++b)
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              acc[0][b][e] = fmaf(gacc[b][e], gc.sf[b][e >> 1], fmaf(-gc.szc[b][e >> 1], sx[e & 1], acc[0][b][e]));
+              for (int e = 0; e < 4; ++e)
+                acc[0][b][e] = fmaf((e >> 1) ? 0.0625f : 1.f, fmaf((e >> 1) ? -1152.f : -1032.f, sx[e & 1], gacc[b][e]),
+                                    acc[0][b][e]);
+          } else {
+#pragma unroll
+            for (int b = 0; b < 4; ++b)
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                acc[0][b][e] = fmaf(gacc[b][e], gc.sf[b][e >> 1], fmaf(-gc.szc[b][e >> 1], sx[e & 1], acc[0][b][e]));
+          }
         } else {
           StageRegs<T> sr;
           load_stage<T>(sb, 0, lo, sr);
