@@ -23,8 +23,8 @@
 //  * Residency: 4 consumer warps (64 columns each) and 1 producer warp per CTA, a 5-stage ring of
 //    19 KB, at most 168 registers: two CTAs fit on one SM.  Launched with programmatic dependent
 //    launch, the next call's CTAs therefore become resident while this call's CTAs still run, and
-//    stream their weights into shared memory before they wait for this call (weights do not depend
-//    on it); only the activations, outputs and workspace wait.
+//    stream their first two weight stages into shared memory before they wait for this call
+//    (weights do not depend on it); only the activations, outputs and workspace wait.
 //  * Split K as in the AWQ-layout kernel: a tile shared by several CTAs is completed by the CTA
 //    holding its first group, which waits (bounded) for the others' fp32 partials and adds them in
 //    contributor order (bit-reproducible).  256-column tiles give a quarter of the contributors per
@@ -44,8 +44,11 @@ namespace {
 constexpr int kPpConsumers = 4;
 constexpr int kPpThreads = (kPpConsumers + 1) * 32;
 constexpr int kPpStages = 5;
-// Stages whose weights are streamed before the wait on the previous kernel (all of the ring).
-constexpr int kPpPrefetch = kPpStages;
+// Stages whose weights are streamed before the wait on the previous kernel.  Two of the five: a deeper
+// early stream competes with the previous call's split-K tail for the memory system (measured on the
+// decode sweep, GB/s: 0 stages 2442, 1 2506, 2 2589, 3 2587, 4 2561, 5 2538).
+constexpr int kPpPrefetch = 2;
+static_assert(kPpPrefetch <= kPpStages, "early stages fit the ring");
 constexpr uint32_t kPpProducerSleepNs = 500;
 constexpr int kPpTileCols = kPrepackTileCols;        // 256
 constexpr int kPpTileWords = kPpTileCols / 8;        // 32
