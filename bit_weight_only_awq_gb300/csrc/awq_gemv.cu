@@ -601,34 +601,45 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
           cached_grp = grp;
         }
         if constexpr (kFold) {
-          float gacc[4][4], sx[4];  // this stage's (1024 + q)^T x and sum_k x
+          float gacc[4][4], sx[4];  // (1024 + q)^T x and sum_k x of this stage (W4A8: of one 64-row block)
+          auto clear = [&]() {
 #pragma unroll
-          for (int b = 0; b < 4; ++b) {
-            sx[b] = 0.f;
+            for (int b = 0; b < 4; ++b) {
+              sx[b] = 0.f;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) gacc[b][e] = 0.f;
-          }
-          StageRegs<8> sr;
-          load_stage<8>(sb, 0, lo, sr);
-          if (nh == 2) {
-            compute_stage(sr, gacc, sx);
-            load_stage<8>(sb, 1, lo, sr);
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(empty_bar(st));  // slot free before the last unit's arithmetic
-          compute_stage(sr, gacc, sx);
-          // the group's zero point and scale: acc += s (gacc - (1024 + z) sx)  (high nibble: s / 16, 1024 + 16 z)
-          if constexpr (EXACT) {
-            // W4A8 (z = 8, s = 1): over the 64 rows |gacc| <= 64 * 1264 * 128 < 2^24 and |sx| <= 8192 are
-            // exact integers, gacc - (1024 + 8 or 1024 + 128) sx = sum (16) (u - 8) x comes out of one
-            // fused multiply-add exactly, and the power-of-two scale keeps it exact in acc
+              for (int e = 0; e < 4; ++e) gacc[b][e] = 0.f;
+            }
+          };
+          // W4A8 (z = 8, s = 1), per 64-row block: |gacc| <= 64 * 1264 * 128 < 2^24 and |sx| <= 8192 are
+          // exact integers (over a whole 128-row group gacc could pass 2^24 with an odd value), so
+          // gacc - (1024 + 8 or 1024 + 128) sx = sum (16) (u - 8) x comes out of one fused multiply-add
+          // exactly, and the power-of-two scale keeps it exact in acc
+          auto fold_exact = [&]() {
 #pragma unroll
             for (int b = 0; b < 4; ++b)
 #pragma unroll
               for (int e = 0; e < 4; ++e)
                 acc[0][b][e] = fmaf((e >> 1) ? 0.0625f : 1.f, fmaf((e >> 1) ? -1152.f : -1032.f, sx[e & 1], gacc[b][e]),
                                     acc[0][b][e]);
+          };
+          clear();
+          StageRegs<8> sr;
+          load_stage<8>(sb, 0, lo, sr);
+          if (nh == 2) {
+            compute_stage(sr, gacc, sx);
+            if constexpr (EXACT) {
+              fold_exact();
+              clear();
+            }
+            load_stage<8>(sb, 1, lo, sr);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(empty_bar(st));  // slot free before the last unit's arithmetic
+          compute_stage(sr, gacc, sx);
+          if constexpr (EXACT) {
+            fold_exact();
           } else {
+            // the group's zero point and scale: acc += s (gacc - (1024 + z) sx)  (high nibble: s / 16, 1024 + 16 z)
 #pragma unroll
             for (int b = 0; b < 4; ++b)
 #pragma unroll

@@ -389,6 +389,27 @@ def test_w4a8_gemv_sums_beyond_fp32_integers(awq, split_k):
     assert np.array_equal(y.view(np.uint16), want_y.view(np.uint16))
 
 
+@pytest.mark.parametrize("split_k", [1, 2])
+def test_w4a8_gemv_group_sums_past_fp32_integers(awq, split_k):
+    # Codes 127 against weights 7 (u = 15), with one code 126 in each 128-row group: every group's
+    # sum_k (1024 + u) x is odd and above 2^24 (128 * 1039 * 127 - 1039 = 16,888,945), so a GEMV that
+    # kept such a sum in fp32 would round it.  With one or two CTAs per tile each GEMV stage holds a
+    # whole group; up to 8 tokens the GEMV folds each 64-row block on its own.
+    M, K, N = 2, 4096, 512
+    xq = np.full((M, K), 127, dtype=np.int8)
+    xq[:, ::128] = 126
+    xq[1] = -xq[1]                                  # and the negative side
+    wq = np.full((K, N // 8), -1, dtype=np.int32)   # every nibble 15: q = 7
+    s_ch = np.full(N, 1e-6, dtype=np.float16)
+    s = np.ones(M, np.float32)
+    acc = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    y = awq.w4a8_gemm(dev(xq), dev(s), dev(wq), dev(s_ch), split_k=split_k, acc_out=acc)
+    want_y, want_acc = oracle.w4a8_linear(xq, s, wq, s_ch)
+    assert (128 * 1039 * 127 - 1039) % 2 == 1 and 128 * 1039 * 127 - 1039 > 2 ** 24
+    assert np.array_equal(host(acc), want_acc)
+    assert np.array_equal(host(y).view(np.uint16), want_y.view(np.uint16))
+
+
 @pytest.mark.parametrize("M,K,N", [(1000, 21760, 8192), (1000, 4096, 16384)])
 def test_w4a8_large_tiles_bitexact(awq, M, K, N):
     # >= 128-token tiles: at K = 21760 one M-block with two exact accumulators; at K = 4096 two M-blocks
