@@ -360,7 +360,7 @@ awq_status w4a8_quant_act(const uint16_t* x, int8_t* xq, float* s_tok, int64_t M
 }  // extern "C"
 
 // The W4A8 product once `fill` has written the fp16 codes of the activations into the workspace
-// (from int8 codes, or by quantizing fp16 activations): the 16-token GEMV or the GEMM, as planned.
+// (from int8 codes, or by quantizing fp16 activations): the GEMV (up to 16 tokens) or the GEMM, as planned.
 template <class Fill>
 static awq_status w4a8_product(Fill fill, const float* s_tok, const int32_t* wq, const uint16_t* s_ch, uint16_t* y,
                                int32_t* acc_out, int64_t M, int64_t K, int64_t N, int32_t split_k, void* workspace,

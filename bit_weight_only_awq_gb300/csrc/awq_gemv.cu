@@ -53,11 +53,14 @@
 //    dequant kernel does (HSUB2 of the zero, HMUL2 by the scale) and multiplies it straight into
 //    the accumulators; streaming the weights once for 16 tokens beats the tensor-core GEMM's
 //    16-token tiles by 1.3-2.9x.
-//  * W4A8 up to 16 tokens (gemv_kernel<16, true>): the same instance with the symmetric zero point
-//    and unit scales, on activations that are int8 codes widened to fp16.  Each weight is the exact
-//    half u - 8 and each product an integer of magnitude at most 1024; with at most 16384 rows of a
-//    tile per CTA every fp32 sum is exact, partials are added across CTAs as int32, and the output
-//    is the W4A8 epilogue fp16((acc * s_tok) * s_ch) ("Support W4A8 quantization for vllm").
+//  * W4A8 from 9 to 16 tokens (gemv_kernel<16, true>): the same instance with the symmetric zero
+//    point and unit scales, on activations that are int8 codes widened to fp16.  Each weight is the
+//    exact half u - 8 and each product an integer of magnitude at most 1024; with at most 16384 rows
+//    of a tile per CTA every fp32 sum is exact, partials are added across CTAs as int32, and the
+//    output is the W4A8 epilogue fp16((acc * s_tok) * s_ch) ("Support W4A8 quantization for vllm").
+//    Up to 8 tokens (gemv_kernel<8, true>) the folded loop runs instead, with the fold taken per
+//    64-row block, where sum (1024 + u) x and sum x are exact integers below 2^24, and the offset
+//    subtracted by one fused multiply-add, exactly.
 //  * Lane (g, t) of the mma reads rows 2t, 2t+1 (+8) of each 16-row step; with the
 //    128-byte swizzle those 32-bit shared-memory loads, and the activation loads, are
 //    free of bank conflicts, and every address is a lane constant plus an immediate.
@@ -438,7 +441,8 @@ static_assert(kMaxRegs == 168, "9 warps: three on one sub-partition");
 // fp32 partial sum is an exact integer (the host keeps a CTA's rows of a tile at or below 16384, so
 // |sum| <= 1024 * 16384 = 2^24); partials are added as int32 and the output is
 // fp16((acc * s_tok[m]) * s_ch[n]), with acc also stored to acc_out when given.
-// BF16 (16 tokens only): bf16 activations, scales and output, W = bf16_RN((q - z) s) made exactly.
+// BF16 (8- or 16-token instance): bf16 activations, scales and output, W = bf16_RN((q - z) s) made
+// exactly.
 template <int T, bool EXACT, bool BF16 = false>
 __global__ void __maxnreg__(kMaxRegs)
 gemv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_x,

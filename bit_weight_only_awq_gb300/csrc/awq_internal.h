@@ -64,12 +64,13 @@ struct GemvPlan {
 };
 GemvPlan gemv_plan(int64_t M, int64_t K, int64_t N, int split_k);
 size_t gemv_workspace_bytes(const GemvPlan& p, int64_t M, int64_t N);
-// bf16: bf16 activations, scales and output on the 16-token instance (workspace rows as for M = 16)
+// bf16: bf16 activations, scales and output on the 8- or 16-token instance (workspace rows as for M = 16)
 cudaError_t launch_gemv(const uint16_t* x, const uint32_t* qw, const uint32_t* qz, const uint16_t* sc,
                         uint16_t* y, int64_t M, int64_t K, int64_t N, const GemvPlan& p, void* ws,
                         int* err, cudaStream_t s, bool bf16 = false);
-// W4A8 on the 16-token GEMV (M <= 16): x16 = the int8 codes widened to fp16, wq = AWQ-packed u = q + 8,
-// exact int32 accumulators.  gemv_w4a8_ok: the plan keeps every CTA's rows of a tile within 16384.
+// W4A8 on the GEMV (M <= 16; 8- or 16-token instance): x16 = the int8 codes widened to fp16,
+// wq = AWQ-packed u = q + 8, exact int32 accumulators.  gemv_w4a8_ok: the plan keeps every CTA's rows
+// of a tile within 16384.
 bool gemv_w4a8_ok(const GemvPlan& p, int64_t M);
 cudaError_t launch_gemv_w4a8(const uint16_t* x16, const uint32_t* wq, const float* s_tok, const uint16_t* s_ch,
                              uint16_t* y, int32_t* acc_out, int64_t M, int64_t K, int64_t N, const GemvPlan& p,

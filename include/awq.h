@@ -310,10 +310,12 @@ awq_status w4a8_quant_act(const uint16_t *x, int8_t *xq, float *s_tok, int64_t M
  * split across CTAs.  With 128 or more tokens and K <= 16384 a CTA covers 256
  * output channels with one accumulator each (two 128-channel blocks sharing
  * every activation tile).
- * With at most 16 tokens the product runs on the decode GEMV instead (its 8-
- * or 16-token instance, weights u - 8 made exact in fp16, fp32 partial sums
- * below 2^24 added as int32 across CTAs), whenever its plan for split_k keeps
- * each CTA's rows of a 512-column tile within 16384; otherwise on the GEMM.
+ * With at most 16 tokens the product runs on the decode GEMV instead (up to 8
+ * tokens it takes sum (1024 + u) x and sum x per 64-row block, exact integers
+ * in fp32, and subtracts the offset exactly; from 9 to 16 tokens it makes the
+ * weights u - 8 exactly in fp16; fp32 sums stay below 2^24 within a CTA and
+ * are added as int32 across CTAs), whenever its plan for split_k keeps each
+ * CTA's rows of a 512-column tile within 16384; otherwise on the GEMM.
  * The results are identical either way.
  * Source: "Support W4A8 quantization for vllm": marlin_qqq_gemm(a, b_q_weight,
  * s1, s2, s3, workspace, size_m, size_n, size_k) in tlrmchlsmth's review;

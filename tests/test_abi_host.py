@@ -168,8 +168,8 @@ def test_gemm_plan_split_choices(awq):
 
 
 def test_w4a8_route_by_token_count(awq):
-    # W4A8 with at most 16 tokens runs on the 16-token GEMV when every CTA's rows of a tile stay within
-    # 16384; its workspace is counters | fp16 codes | the GEMV's 16-token partial slots.
+    # W4A8 with at most 16 tokens runs on the GEMV when every CTA's rows of a tile stay within 16384; its
+    # workspace is counters | fp16 codes | the GEMV's partial slots, sized for 16 token rows.
     counters = 65536
     a256 = lambda b: (b + 255) // 256 * 256
     ws = lambda M, K, N, sp: awq.awq_workspace_bytes(awq.OP_W4A8_GEMM, M, K, N, sp)
